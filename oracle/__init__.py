@@ -1,0 +1,175 @@
+"""CPU oracle for the fused cross-entropy path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline and
+reference legs may import this package.  The product (``cross_entropy_loss_gb300``)
+never does, and the two share no code: this side is plain float64 C
+(``ce_oracle.c``) plus numpy matrix products for the linear layer.
+
+Definitions followed (the FOAK pages name the kernels but print no formula; the
+reading is the textbook one, stated in ``ce_oracle.c``):
+
+* ``ce`` -- softmax cross-entropy over the rows of an N x V logits matrix, mean
+  over rows whose label is not ``ignore_index`` ("Fast Cross Entropy Triton
+  Kernels", fms-acceleration-foak 0.7.4 page, list of fused operations and
+  kernels; FastCrossEntropyLoss, fms-acceleration PR #79, Description item 4),
+  with the gradient ``(softmax - onehot) * g / D``.
+* ``linear_ce`` -- the same loss applied to ``Z = H W^T`` with the gradients
+  ``dH = dZ W`` and ``dW = dZ^T H`` (the fused linear + cross-entropy the pages
+  call LigerFusedLinearCrossEntropy -- "Running Liger Kernel Benchmarks" on the
+  foak page -- and "chunked loss" -- PR #79, TODO list).  Chunking is a schedule,
+  not a different result, so the oracle does not chunk.
+
+Parity pins (closed forms, invariants, finite differences, brute force, a
+hand-worked example) live in ``tests/test_oracle_pins.py``; every function here
+is pinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ce_oracle.c")
+_LIB = os.path.join(_HERE, "libce_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16, F64 = 0, 1, 2
+IGNORED, VALID, BAD_LABEL = 0, 1, 2
+
+
+def build_lib(force: bool = False) -> str:
+    """Compile ce_oracle.c with the host gcc (plain -O2, no fast-math, no arch flags)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _get():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build_lib())
+            i64, dbl, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+            lib.oracle_ce_count.argtypes = [vp, i64, i64, i64, vp, vp]
+            lib.oracle_ce_rows.argtypes = [vp, i32, i64, vp, i64, i64, i64, i64, dbl, vp, vp, vp, vp]
+            lib.oracle_ce_mean.argtypes = [vp, vp, i64, dbl]
+            lib.oracle_ce_mean.restype = dbl
+            _lib = lib
+    return _lib
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:  # bfloat16 bit patterns
+        return BF16
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"oracle: unsupported logits dtype {a.dtype}")
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def count(labels: np.ndarray, V: int, ignore_index: int = -100):
+    """(n_valid, n_bad): rows with a label in [0, V), rows with any other non-ignored label."""
+    labels = np.ascontiguousarray(labels, dtype=np.int64)
+    nv, nb = ctypes.c_int64(), ctypes.c_int64()
+    _get().oracle_ce_count(labels.ctypes.data, labels.size, V, ignore_index,
+                           ctypes.byref(nv), ctypes.byref(nb))
+    return int(nv.value), int(nb.value)
+
+
+def scale_of(g: float, denom: float, n_valid: int) -> float:
+    """g / D with D = denom if denom > 0 else n_valid (inf/NaN when D == 0; no row uses it then)."""
+    D = float(denom) if denom > 0 else float(n_valid)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return float(np.float64(g) / np.float64(D))
+
+
+def rows(logits: np.ndarray, labels: np.ndarray, V: int, *, ignore_index: int = -100,
+         scale: float = 1.0, want_grad: bool = True, threads: int | None = None):
+    """Per-row quantities for every row of ``logits`` (shape rows x ld, ld >= V).
+
+    Returns (lse, row_loss, state, grad) as float64 / int8 arrays; grad is rows x V
+    (or None).  ``scale`` multiplies the gradient (g / D of the whole batch).
+    """
+    logits = np.ascontiguousarray(logits)
+    labels = np.ascontiguousarray(labels, dtype=np.int64)
+    n, ld = logits.shape
+    assert ld >= V and labels.shape == (n,)
+    dt = _dtype_code(logits)
+    lse = np.zeros(n, dtype=np.float64)
+    rl = np.zeros(n, dtype=np.float64)
+    st = np.zeros(n, dtype=np.int8)
+    grad = np.zeros((n, V), dtype=np.float64) if want_grad else None
+    lib = _get()
+    nt = max(1, min(threads or default_threads(), n))
+    bounds = np.linspace(0, n, nt + 1).astype(np.int64)
+    xp, yp = logits.ctypes.data, labels.ctypes.data
+
+    def work(t):
+        a, b = int(bounds[t]), int(bounds[t + 1])
+        if b > a:
+            gp = grad[a:].ctypes.data if grad is not None else None
+            lib.oracle_ce_rows(xp, dt, ld, yp, a, b, V, ignore_index, scale,
+                               lse[a:].ctypes.data, rl[a:].ctypes.data, st[a:].ctypes.data, gp)
+
+    if nt == 1:
+        work(0)
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(work, range(nt)))
+    return lse, rl, st, grad
+
+
+def mean(row_loss: np.ndarray, state: np.ndarray, denom: float = 0.0) -> float:
+    row_loss = np.ascontiguousarray(row_loss, dtype=np.float64)
+    state = np.ascontiguousarray(state, dtype=np.int8)
+    return float(_get().oracle_ce_mean(row_loss.ctypes.data, state.ctypes.data, row_loss.size,
+                                       float(denom)))
+
+
+def ce(logits: np.ndarray, labels: np.ndarray, V: int | None = None, *, ignore_index: int = -100,
+       g: float = 1.0, denom: float = 0.0, want_grad: bool = True, threads: int | None = None):
+    """The whole definition on one batch: loss, n_valid, n_bad, lse, row_loss, state, grad, scale."""
+    V = logits.shape[1] if V is None else V
+    n_valid, n_bad = count(labels, V, ignore_index)
+    scale = scale_of(g, denom, n_valid)
+    lse, rl, st, grad = rows(logits, labels, V, ignore_index=ignore_index, scale=scale,
+                             want_grad=want_grad, threads=threads)
+    loss = mean(rl, st, denom)
+    return dict(loss=loss, n_valid=n_valid, n_bad=n_bad, lse=lse, row_loss=rl, state=st,
+                grad=grad, scale=scale)
+
+
+def _to_f64(a: np.ndarray) -> np.ndarray:
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def linear_ce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *, ignore_index: int = -100,
+              g: float = 1.0, denom: float = 0.0, threads: int | None = None):
+    """Loss, dH and dW of cross-entropy over Z = H W^T, all in float64.
+
+    H: N x D, W: V x D (float32, float64 or bf16 bit patterns).  Steps: Z = H W^T;
+    the ``ce`` definition on Z gives loss and dZ; dH = dZ W; dW = dZ^T H.
+    """
+    Hd, Wd = _to_f64(H), _to_f64(W)
+    Z = Hd @ Wd.T
+    r = ce(Z, labels, Z.shape[1], ignore_index=ignore_index, g=g, denom=denom, threads=threads)
+    dZ = r["grad"]
+    dH = dZ @ Wd
+    dW = dZ.T @ Hd
+    return dict(loss=r["loss"], n_valid=r["n_valid"], n_bad=r["n_bad"], dH=dH, dW=dW, Z=Z, dZ=dZ,
+                lse=r["lse"], row_loss=r["row_loss"], state=r["state"], scale=r["scale"])
