@@ -1,0 +1,202 @@
+"""GB300 (sm_103a) fused cross-entropy -- Python binding of ``libfoak_ce.so``.
+
+The library is the FastCrossEntropyLoss of the fms-acceleration FOAK plugin
+(fms-acceleration PR #79, Description item 4) rebuilt as hand-written CUDA for
+sm_103a behind a C ABI (``include/foak_ce.h``).  This module only marshals
+arguments: it takes torch tensors for device memory and the current stream,
+passes their pointers through ctypes, and raises on a non-zero status.  Every
+step of the computation runs in the library's kernels; there is no CPU or
+PyTorch fallback -- importing fails loudly when the library is missing.
+
+Build it with ``python -c "import __graft_entry__ as g; g.build()"`` (or
+``cross_entropy_loss_gb300._build.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+LIB_PATH = _build.LIB
+
+FOAK_OK = 0
+FOAK_ERR_INVALID_ARG = 1
+FOAK_ERR_UNSUPPORTED = 2
+FOAK_ERR_LABEL_RANGE = 3
+FOAK_ERR_WORKSPACE = 4
+FOAK_ERR_CUDA = 5
+FOAK_ERR_TIMEOUT = 6
+FOAK_F32 = 0
+FOAK_BF16 = 1
+FOAK_ERRBIT_LABEL_RANGE = 1
+FOAK_ERRBIT_TIMEOUT = 2
+
+# C entry points and their ctypes signatures (restype, argtypes).
+_vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "foak_status_string": (ctypes.c_char_p, [_i32]),
+    "foak_abi_version": (_i32, []),
+    "foak_ce_max_vocab": (_i64, [_i32]),
+    "foak_ce_workspace_size": (_sz, [_i64]),
+    "foak_ce_forward": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                               _vp]),
+    "foak_ce_backward": (_i32, [_vp, _vp, _i32, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp]),
+    "foak_ce_fwd_bwd": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _sz,
+                               _vp]),
+    "foak_test_fail_next_launches": (None, [_i32]),
+}
+
+
+class FoakError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"cross_entropy_loss_gb300: {LIB_PATH} is missing; build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()'). There is no fallback path.")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.foak_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != FOAK_OK:
+        raise FoakError(status, where)
+
+
+def foak_ce_workspace_size(N: int) -> int:
+    return int(lib.foak_ce_workspace_size(int(N)))
+
+
+def foak_ce_max_vocab(dtype: int) -> int:
+    return int(lib.foak_ce_max_vocab(int(dtype)))
+
+
+# --------------------------------------------------------------------- torch glue
+import torch  # noqa: E402  (device memory and streams only)
+
+_DT = {torch.bfloat16: FOAK_BF16, torch.float32: FOAK_F32}
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _logits_args(logits):
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D tensor with unit column stride (N x V, row stride ld)")
+    if logits.dtype not in _DT:
+        raise TypeError("logits must be bfloat16 or float32")
+    if not logits.is_cuda:
+        raise ValueError("logits must be on a CUDA device")
+    N, V = logits.shape
+    ld = logits.stride(0) if N > 1 else max(V, logits.stride(0))
+    return N, V, ld, _DT[logits.dtype]
+
+
+def _labels_arg(labels, N, device):
+    if labels.dtype != torch.int64 or labels.dim() != 1 or labels.numel() != N or not labels.is_contiguous():
+        raise ValueError("labels must be a contiguous int64 vector of length N")
+    if labels.device != device:
+        raise ValueError("labels must live on the logits' device")
+    return labels
+
+
+def workspace(N: int, device) -> torch.Tensor:
+    """A zero-filled, reusable workspace of at least foak_ce_workspace_size(N) bytes.
+
+    Calls leave it zeroed again, so the cached buffer serves every stream-ordered
+    call on its device.  Calls on different streams should pass their own buffer.
+    """
+    need = foak_ce_workspace_size(N)
+    dev = torch.device(device)
+    with _ws_lock:
+        ws = _ws_cache.get(dev)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(max(need, 4096), dtype=torch.uint8, device=dev)
+            _ws_cache[dev] = ws
+    return ws
+
+
+def foak_ce_forward(logits, labels, *, ignore_index: int = -100, denom: float = 0.0, want_lse: bool = True,
+                    want_row_loss: bool = False, workspace_tensor=None, stream=None):
+    """Mean CE loss over non-ignored rows.  Returns dict(loss, lse, row_loss, n_valid, err)."""
+    N, V, ld, dt = _logits_args(logits)
+    dev = logits.device
+    labels = _labels_arg(labels, N, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int32, device=dev)
+    err = torch.empty(1, dtype=torch.int32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
+    row_loss = torch.empty(N, dtype=torch.float32, device=dev) if want_row_loss else None
+    ws = workspace(N, dev) if workspace_tensor is None else workspace_tensor
+    st = lib.foak_ce_forward(_ptr(logits), dt, ld, _ptr(labels), N, V, int(ignore_index), float(denom), _ptr(loss),
+                             _ptr(lse), _ptr(row_loss), _ptr(n_valid), _ptr(err), _ptr(ws), ws.numel(),
+                             _stream(dev, stream))
+    _check(st, "foak_ce_forward")
+    return dict(loss=loss, lse=lse, row_loss=row_loss, n_valid=n_valid, err=err)
+
+
+def foak_ce_backward(logits, labels, lse, grad_out=None, *, dlogits=None, ignore_index: int = -100,
+                     denom: float = 0.0, stream=None):
+    """dlogits = (softmax - onehot) * g / D.  Pass ``dlogits=logits`` to overwrite in place."""
+    N, V, ld, dt = _logits_args(logits)
+    dev = logits.device
+    labels = _labels_arg(labels, N, dev)
+    if dlogits is None:
+        dlogits = torch.empty_strided(logits.shape, logits.stride(), dtype=logits.dtype, device=dev)
+    if dlogits.shape != logits.shape or dlogits.stride() != logits.stride() or dlogits.dtype != logits.dtype:
+        raise ValueError("dlogits must match logits in shape, strides and dtype")
+    if lse.dtype != torch.float32 or lse.numel() != N or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 vector of length N")
+    if grad_out is not None and (grad_out.dtype != torch.float32 or grad_out.numel() != 1):
+        raise ValueError("grad_out must be a float32 scalar tensor")
+    err = torch.empty(1, dtype=torch.int32, device=dev)
+    st = lib.foak_ce_backward(_ptr(dlogits), _ptr(logits), dt, ld, _ptr(labels), N, V, int(ignore_index), _ptr(lse),
+                              _ptr(grad_out), float(denom), _ptr(err), _stream(dev, stream))
+    _check(st, "foak_ce_backward")
+    return dlogits, err
+
+
+def foak_ce_fwd_bwd(logits, labels, *, g: float = 1.0, ignore_index: int = -100, denom: float = 0.0,
+                    want_lse: bool = False, workspace_tensor=None, stream=None):
+    """Fused forward + backward in place: ``logits`` is overwritten by dlogits.
+
+    Returns dict(loss, n_valid, err, lse).
+    """
+    N, V, ld, dt = _logits_args(logits)
+    dev = logits.device
+    labels = _labels_arg(labels, N, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int32, device=dev)
+    err = torch.empty(1, dtype=torch.int32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
+    ws = workspace(N, dev) if workspace_tensor is None else workspace_tensor
+    st = lib.foak_ce_fwd_bwd(_ptr(logits), dt, ld, _ptr(labels), N, V, int(ignore_index), float(g), float(denom),
+                             _ptr(loss), _ptr(lse), _ptr(n_valid), _ptr(err), _ptr(ws), ws.numel(),
+                             _stream(dev, stream))
+    _check(st, "foak_ce_fwd_bwd")
+    return dict(loss=loss, n_valid=n_valid, err=err, lse=lse)

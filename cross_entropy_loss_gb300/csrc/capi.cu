@@ -1,0 +1,178 @@
+// C ABI of the library: argument checks, workspace layout, launches and the
+// optional synchronous error check.  Declarations and their contracts are in
+// include/foak_ce.h.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "foak_ce.h"
+#include "internal.h"
+
+namespace foak {
+
+int device_sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+namespace {
+
+std::atomic<int> g_fail_launches{0};
+
+bool take_injected_failure() {
+    int n = g_fail_launches.load();
+    while (n > 0) {
+        if (g_fail_launches.compare_exchange_weak(n, n - 1)) return true;
+    }
+    return false;
+}
+
+bool sync_check_enabled() {
+    const char* s = std::getenv("FOAK_SYNC_CHECK");
+    return s && s[0] == '1';
+}
+
+int elem_bytes_of(int32_t dtype) {
+    if (dtype == FOAK_BF16) return 2;
+    if (dtype == FOAK_F32) return 4;
+    return 0;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks common to the row calls.
+foak_status check_rows(const void* logits, int32_t dtype, int64_t ld, const int64_t* labels, int64_t N,
+                       int64_t V, int* es) {
+    *es = elem_bytes_of(dtype);
+    if (*es == 0) return FOAK_ERR_UNSUPPORTED;
+    if (N < 0 || V < 1 || ld < V) return FOAK_ERR_INVALID_ARG;
+    if (N > 0x7fffffffLL) return FOAK_ERR_UNSUPPORTED;  // n_valid is int32
+    if (V > ce_rows_max_vocab(*es)) return FOAK_ERR_UNSUPPORTED;
+    if (N > 0 && (!logits || !labels)) return FOAK_ERR_INVALID_ARG;
+    if (logits && !aligned(logits, static_cast<size_t>(*es))) return FOAK_ERR_INVALID_ARG;
+    if (labels && !aligned(labels, 8)) return FOAK_ERR_INVALID_ARG;
+    return FOAK_OK;
+}
+
+foak_status finish(cudaError_t e, int32_t* err, cudaStream_t stream) {
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FOAK_ERR_CUDA;
+    }
+    if (!sync_check_enabled()) return FOAK_OK;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FOAK_ERR_CUDA;
+    if (!err) return FOAK_OK;
+    int32_t h = 0;
+    if (cudaMemcpy(&h, err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FOAK_ERR_CUDA;
+    if (h & FOAK_ERRBIT_TIMEOUT) return FOAK_ERR_TIMEOUT;
+    if (h & FOAK_ERRBIT_LABEL_RANGE) return FOAK_ERR_LABEL_RANGE;
+    return FOAK_OK;
+}
+
+foak_status rows_common(bool grad, const void* logits, int32_t dtype, int64_t ld, const int64_t* labels,
+                        int64_t N, int64_t V, int64_t ignore_index, float g, float denom, float* loss,
+                        float* lse, float* row_loss, int32_t* n_valid, int32_t* err, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    int es = 0;
+    foak_status st = check_rows(logits, dtype, ld, labels, N, V, &es);
+    if (st != FOAK_OK) return st;
+    if (!loss || !aligned(loss, 4)) return FOAK_ERR_INVALID_ARG;
+    if ((lse && !aligned(lse, 4)) || (row_loss && !aligned(row_loss, 4)) || (n_valid && !aligned(n_valid, 4)) ||
+        (err && !aligned(err, 4)))
+        return FOAK_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, kCeWsAlign) || workspace_bytes < ce_workspace_bytes(N))
+        return FOAK_ERR_WORKSPACE;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    CeWsHeader* ws = static_cast<CeWsHeader*>(workspace);
+    float* rl = row_loss ? row_loss : reinterpret_cast<float*>(static_cast<char*>(workspace) + sizeof(CeWsHeader));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_ce_rows(grad, es, logits, grad ? const_cast<void*>(logits) : nullptr, ld, labels, N, V,
+                                   ignore_index, g, denom, loss, lse, rl, n_valid, err, ws, s);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return finish(e, err, s);
+}
+
+}  // namespace
+}  // namespace foak
+
+using namespace foak;
+
+extern "C" {
+
+const char* foak_status_string(int32_t status) {
+    switch (status) {
+        case FOAK_OK: return "FOAK_OK";
+        case FOAK_ERR_INVALID_ARG: return "FOAK_ERR_INVALID_ARG: null, negative, misaligned or inconsistent argument";
+        case FOAK_ERR_UNSUPPORTED: return "FOAK_ERR_UNSUPPORTED: dtype or size outside what the kernels handle";
+        case FOAK_ERR_LABEL_RANGE: return "FOAK_ERR_LABEL_RANGE: a label was outside [0, V) and not ignore_index";
+        case FOAK_ERR_WORKSPACE: return "FOAK_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case FOAK_ERR_CUDA: return "FOAK_ERR_CUDA: a CUDA call or kernel launch failed";
+        case FOAK_ERR_TIMEOUT: return "FOAK_ERR_TIMEOUT: a device-side wait gave up";
+        default: return "unknown foak_status";
+    }
+}
+
+int32_t foak_abi_version(void) { return FOAK_CE_ABI_VERSION; }
+
+int64_t foak_ce_max_vocab(int32_t dtype) {
+    const int es = elem_bytes_of(dtype);
+    return es ? ce_rows_max_vocab(es) : 0;
+}
+
+size_t foak_ce_workspace_size(int64_t N) { return ce_workspace_bytes(N); }
+
+foak_status foak_ce_forward(const void* logits, int32_t dtype, int64_t ld, const int64_t* labels, int64_t N,
+                            int64_t V, int64_t ignore_index, float denom, float* loss, float* lse,
+                            float* row_loss, int32_t* n_valid, int32_t* err, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    return rows_common(false, logits, dtype, ld, labels, N, V, ignore_index, 1.0f, denom, loss, lse, row_loss,
+                       n_valid, err, workspace, workspace_bytes, stream);
+}
+
+foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64_t* labels, int64_t N, int64_t V,
+                            int64_t ignore_index, float g, float denom, float* loss, float* lse,
+                            int32_t* n_valid, int32_t* err, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    return rows_common(true, logits, dtype, ld, labels, N, V, ignore_index, g, denom, loss, lse, nullptr,
+                       n_valid, err, workspace, workspace_bytes, stream);
+}
+
+foak_status foak_ce_backward(void* dlogits, const void* logits, int32_t dtype, int64_t ld, const int64_t* labels,
+                             int64_t N, int64_t V, int64_t ignore_index, const float* lse, const float* grad_out,
+                             float denom, int32_t* err, void* stream) {
+    int es = 0;
+    foak_status st = check_rows(logits, dtype, ld, labels, N, V, &es);
+    if (st != FOAK_OK) return st;
+    if (N > 0 && (!dlogits || !lse)) return FOAK_ERR_INVALID_ARG;
+    if (dlogits && !aligned(dlogits, static_cast<size_t>(es))) return FOAK_ERR_INVALID_ARG;
+    // logits and dlogits share the row geometry: same offset modulo 16 bytes
+    if (dlogits && logits &&
+        (reinterpret_cast<uintptr_t>(dlogits) & 15u) != (reinterpret_cast<uintptr_t>(logits) & 15u))
+        return FOAK_ERR_INVALID_ARG;
+    if ((lse && !aligned(lse, 4)) || (grad_out && !aligned(grad_out, 4)) || (err && !aligned(err, 4)))
+        return FOAK_ERR_INVALID_ARG;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        // nothing to compute; still report a clean error word
+        cudaError_t e = err ? cudaMemsetAsync(err, 0, sizeof(int32_t), s) : cudaSuccess;
+        return finish(e, err, s);
+    }
+    cudaError_t e = launch_ce_backward(es, dlogits, logits, ld, labels, N, V, ignore_index, lse, grad_out, denom,
+                                       err, s);
+    return finish(e, err, s);
+}
+
+void foak_test_fail_next_launches(int32_t count) { g_fail_launches.store(count < 0 ? 0 : count); }
+
+}  // extern "C"

@@ -1,0 +1,548 @@
+// Row-wise cross-entropy: forward, and fused forward+backward in place.
+//
+// One row of the N x V logits matrix is owned by one CTA, or by a cluster of 2,
+// 4 or 8 CTAs when the row is longer than one CTA's 64 KB slice (V = 128256 bf16
+// needs 4, fp32 needs 8).  Each CTA stages its slice of the row in shared memory
+// with one-dimensional bulk copies (TMA engine) completing on an mbarrier, keeps
+// 2-4 rows in flight, and moves the slice into registers (8 x 16 bytes per
+// thread).  From the registers it forms the thread's (max, sum exp(x - max)),
+// merges the pairs across the warp (shuffles), the CTA (shared memory) and the
+// cluster (distributed shared memory) into the row's log-sum-exp, and -- in the
+// fused kernel -- writes (exp(x - lse) - onehot) * g / D straight from registers
+// over the logits with 16-byte streaming stores.  Non-ignored rows are read
+// once; ignored rows are never read (fused: only zero-filled).  That is the
+// one-pass row sweep of the FastCrossEntropyLoss kernel the FOAK pages describe
+// (fms-acceleration PR #79, Description item 4), re-planned for sm_103a.
+//
+// Rows whose address is not 16-byte aligned are split into a scalar head (< 16
+// bytes), a run of 16-byte vectors and a scalar tail; the scalars are handled by
+// one thread each.  n_valid is counted by every CTA from the labels (64 KB at
+// N = 8192, an L2-resident read), and the mean loss is reduced in float64, in
+// row order, by whichever CTA finishes last.
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "common.cuh"
+#include "foak_ce.h"
+#include "internal.h"
+
+namespace foak {
+
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowVpt = 8;                            // 16-byte vectors per thread per slice
+constexpr int kRowSliceVec = kRowThreads * kRowVpt;   // 4096 vectors = 64 KB per CTA
+constexpr int kRowMaxStages = 4;
+constexpr int kRowMaxCluster = 8;
+constexpr int kMaxScalars = 7;                        // head or tail: < 16 bytes of bf16
+constexpr uint32_t kBulkChunk = 32768;
+constexpr size_t kSmemBudget = 227 * 1024 - 2048;     // dynamic smem left after static use
+
+struct CeRowParams {
+    const char* x;
+    char* dx;
+    int64_t ld;
+    const int64_t* labels;
+    int64_t N, V, ignore_index;
+    float g, denom;
+    float* loss;
+    float* lse;
+    float* row_loss;
+    int32_t* n_valid;
+    int32_t* err;
+    CeWsHeader* ws;
+    int k;               // CTAs per row (cluster size)
+    int per;             // vectors per CTA slice
+    int stages;          // rows in flight per CTA
+    uint32_t stage_bytes;
+};
+
+struct RowGeom {
+    int h;       // scalar head elements before the first 16-byte boundary
+    int64_t nb;  // 16-byte vectors
+    int t;       // scalar tail elements
+};
+
+template <int ES>
+__device__ __forceinline__ RowGeom row_geom(const char* rowp, int64_t V) {
+    constexpr int EPV = 16 / ES;
+    RowGeom g;
+    int h = static_cast<int>(((16u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(rowp)) & 15u)) & 15u) / ES);
+    if (h > V) h = static_cast<int>(V);
+    g.h = h;
+    g.nb = (V - h) / EPV;
+    g.t = static_cast<int>(V - h - g.nb * EPV);
+    return g;
+}
+
+template <int ES>
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[16 / ES]) {
+    if constexpr (ES == 2) {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+        f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    } else {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+}
+
+template <int ES>
+__device__ __forceinline__ uint4 pack(const float (&f)[16 / ES]) {
+    uint4 v;
+    if constexpr (ES == 2) {
+        v.x = pack_bf16x2(f[0], f[1]);
+        v.y = pack_bf16x2(f[2], f[3]);
+        v.z = pack_bf16x2(f[4], f[5]);
+        v.w = pack_bf16x2(f[6], f[7]);
+    } else {
+        v.x = __float_as_uint(f[0]); v.y = __float_as_uint(f[1]);
+        v.z = __float_as_uint(f[2]); v.w = __float_as_uint(f[3]);
+    }
+    return v;
+}
+
+template <int ES>
+__device__ __forceinline__ float load_scalar(const char* p) {
+    if constexpr (ES == 2) return bf16_lo(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)));
+    else return *reinterpret_cast<const float*>(p);
+}
+
+template <int ES>
+__device__ __forceinline__ void store_scalar(char* p, float v) {
+    if constexpr (ES == 2) *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+    else *reinterpret_cast<float*>(p) = v;
+}
+
+template <int ES, bool GRAD>
+__global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowParams p) {
+    constexpr int EPV = 16 / ES;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint64_t bars[kRowMaxStages];
+    __shared__ float2 red[kRowWarps];
+    __shared__ float2 cl_slot[2];
+    __shared__ int iscratch[2 * kRowWarps];
+    __shared__ double dred[kRowWarps];
+    __shared__ int s_abort, s_last;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = p.k;
+    const int rank = K > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int64_t cid = K > 1 ? cluster_id_x() : blockIdx.x;
+    const int64_t ncl = K > 1 ? cluster_count_x() : gridDim.x;
+    const int64_t n_it = p.N > cid ? (p.N - 1 - cid) / ncl + 1 : 0;
+    const int64_t row_bytes = p.ld * ES;
+    const int tail_tid = K == 1 ? 32 : 0;
+    const int64_t v0 = static_cast<int64_t>(rank) * p.per;
+
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+        s_abort = 0;
+        s_last = 0;
+    }
+    __syncthreads();
+
+    // Producer state (thread 0): next row iteration to look at, valid rows issued.
+    int64_t p_it = 0;
+    uint32_t p_v = 0;
+    auto issue_next = [&]() {
+        while (p_it < n_it) {
+            const int64_t row = cid + p_it * ncl;
+            ++p_it;
+            const int64_t y = __ldg(p.labels + row);
+            if (y == p.ignore_index || y < 0 || y >= p.V) continue;
+            const char* rowp = p.x + row * row_bytes;
+            const RowGeom gm = row_geom<ES>(rowp, p.V);
+            int64_t nl = gm.nb - v0;
+            nl = nl < 0 ? 0 : (nl > p.per ? p.per : nl);
+            const uint32_t bytes = static_cast<uint32_t>(nl) * 16u;
+            const int st = static_cast<int>(p_v % static_cast<uint32_t>(p.stages));
+            ++p_v;
+            uint64_t* bar = &bars[st];
+            mbar_arrive_expect_tx(bar, bytes);
+            const char* src = rowp + static_cast<int64_t>(gm.h) * ES + v0 * 16;
+            unsigned char* dst = smem + static_cast<size_t>(st) * p.stage_bytes;
+            for (uint32_t off = 0; off < bytes; off += kBulkChunk)
+                bulk_g2s(dst + off, src + off, min(kBulkChunk, bytes - off), bar);
+            return;
+        }
+    };
+    if (tid == 0)
+        for (int s = 0; s < p.stages; ++s) issue_next();
+
+    int n_valid = 0, n_bad = 0;
+    count_labels(p.labels, p.N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
+    const float D = p.denom > 0.f ? p.denom : static_cast<float>(n_valid);
+    const float scale = p.g / D;
+
+    uint32_t c_v = 0;
+    bool aborted = false;
+    for (int64_t it = 0; it < n_it; ++it) {
+        const int64_t row = cid + it * ncl;
+        const int64_t y = __ldg(p.labels + row);
+        const bool valid = y != p.ignore_index && y >= 0 && y < p.V;
+        const char* rowp = p.x + row * row_bytes;
+        const RowGeom gm = row_geom<ES>(rowp, p.V);
+        int nl;
+        {
+            const int64_t t = gm.nb - v0;
+            nl = static_cast<int>(t < 0 ? 0 : (t > p.per ? p.per : t));
+        }
+        const bool has_head = rank == 0 && tid == 0 && gm.h > 0;
+        const bool has_tail = rank == K - 1 && tid == tail_tid && gm.t > 0;
+        const int64_t tail_col = gm.h + gm.nb * EPV;
+
+        if (!valid) {
+            if constexpr (GRAD) {
+                char* drow = p.dx + row * row_bytes;
+                uint4* dv = reinterpret_cast<uint4*>(drow + static_cast<int64_t>(gm.h) * ES + v0 * 16);
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                for (int i = tid; i < nl; i += kRowThreads) st_global_cs_v4(dv + i, z);
+                if (has_head)
+                    for (int s = 0; s < gm.h; ++s) store_scalar<ES>(drow + s * ES, 0.f);
+                if (has_tail)
+                    for (int s = 0; s < gm.t; ++s) store_scalar<ES>(drow + (tail_col + s) * ES, 0.f);
+            }
+            if (rank == 0 && tid == 0) {
+                p.row_loss[row] = 0.f;
+                if (p.lse) p.lse[row] = 0.f;
+            }
+            continue;
+        }
+
+        const int st = static_cast<int>(c_v % static_cast<uint32_t>(p.stages));
+        const uint32_t par = (c_v / static_cast<uint32_t>(p.stages)) & 1u;
+        ++c_v;
+        if (!aborted && !mbar_wait_bounded(&bars[st], par)) s_abort = 1;
+
+        // Slice -> registers; scalars straight from global memory.
+        uint4 v[kRowVpt];
+        const uint4* sb = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(st) * p.stage_bytes);
+#pragma unroll
+        for (int i = 0; i < kRowVpt; ++i) {
+            const int lv = tid + i * kRowThreads;
+            v[i] = lv < nl ? sb[lv] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float xs[kMaxScalars];
+        int ns = 0;
+        int64_t c0 = 0;
+        if (has_head) { ns = gm.h; c0 = 0; }
+        if (has_tail) { ns = gm.t; c0 = tail_col; }
+#pragma unroll
+        for (int s = 0; s < kMaxScalars; ++s) xs[s] = s < ns ? load_scalar<ES>(rowp + (c0 + s) * ES) : kNegInf;
+
+        __syncthreads();  // the stage is consumed; s_abort is settled
+        if (s_abort) aborted = true;
+        if (tid == 0 && !aborted) {
+            fence_proxy_async_smem();
+            issue_next();
+        }
+
+        // Thread (max, sum exp(x - max)).
+        float m = kNegInf;
+#pragma unroll
+        for (int i = 0; i < kRowVpt; ++i) {
+            if (tid + i * kRowThreads < nl) {
+                float f[EPV];
+                unpack<ES>(v[i], f);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) m = fmaxf(m, f[e]);
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < kMaxScalars; ++s) m = fmaxf(m, xs[s]);
+        float sum = 0.f;
+        if (m != kNegInf) {
+            const float mb = m * kLog2e;
+#pragma unroll
+            for (int i = 0; i < kRowVpt; ++i) {
+                if (tid + i * kRowThreads < nl) {
+                    float f[EPV];
+                    unpack<ES>(v[i], f);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) sum += ex2(fmaf(f[e], kLog2e, -mb));
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < kMaxScalars; ++s)
+                if (s < ns) sum += ex2(fmaf(xs[s], kLog2e, -mb));
+        }
+
+        // Merge: warp -> CTA -> cluster.  Every warp merges the CTA's 16 partials
+        // itself (same order, same result), so no second CTA barrier is needed.
+        warp_ms_reduce(m, sum);
+        if (lane == 0) red[warp] = make_float2(m, sum);
+        __syncthreads();
+        float2 r = lane < kRowWarps ? red[lane] : make_float2(kNegInf, 0.f);
+        float M = r.x, S = r.y;
+        warp_ms_reduce(M, S);
+        if (K > 1) {
+            const int slot = c_v & 1u;
+            if (tid == 0) cl_slot[slot] = make_float2(M, S);
+            cluster_sync();
+            const float2 q = lane < K ? ld_dsmem_f2(&cl_slot[slot], static_cast<uint32_t>(lane))
+                                      : make_float2(kNegInf, 0.f);
+            M = q.x;
+            S = q.y;
+            warp_ms_reduce(M, S);
+        }
+        M = __shfl_sync(0xffffffffu, M, 0);
+        S = __shfl_sync(0xffffffffu, S, 0);
+        const float lse = M + logf(S);
+
+        // Which thread holds the label column.
+        int own_slot = -1, own_e = 0, own_sc = -1;
+        if (y < gm.h) {
+            if (rank == 0 && tid == 0) own_sc = static_cast<int>(y);
+        } else if (y < tail_col) {
+            const int64_t ly = y - gm.h;
+            const int64_t vec = ly / EPV;
+            const int r_own = static_cast<int>(vec / p.per);
+            const int lv = static_cast<int>(vec - static_cast<int64_t>(r_own) * p.per);
+            if (r_own == rank && lv % kRowThreads == tid) {
+                own_slot = lv / kRowThreads;
+                own_e = static_cast<int>(ly % EPV);
+            }
+        } else if (rank == K - 1 && tid == tail_tid) {
+            own_sc = static_cast<int>(y - tail_col);
+        }
+
+        float x_y = 0.f;
+        if constexpr (GRAD) {
+            const float c = lse * kLog2e;
+            char* drow = p.dx + row * row_bytes;
+            uint4* dv = reinterpret_cast<uint4*>(drow + static_cast<int64_t>(gm.h) * ES + v0 * 16);
+#pragma unroll
+            for (int i = 0; i < kRowVpt; ++i) {
+                const int lv = tid + i * kRowThreads;
+                if (lv < nl) {
+                    float f[EPV], d[EPV];
+                    unpack<ES>(v[i], f);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) d[e] = ex2(fmaf(f[e], kLog2e, -c)) * scale;
+                    if (i == own_slot) {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e)
+                            if (e == own_e) {
+                                x_y = f[e];
+                                d[e] -= scale;
+                            }
+                    }
+                    if (!aborted) st_global_cs_v4(dv + lv, pack<ES>(d));
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < kMaxScalars; ++s) {
+                if (s < ns) {
+                    float d = ex2(fmaf(xs[s], kLog2e, -c)) * scale;
+                    if (s == own_sc) {
+                        x_y = xs[s];
+                        d -= scale;
+                    }
+                    if (!aborted) store_scalar<ES>(drow + (c0 + s) * ES, d);
+                }
+            }
+        } else {
+            if (own_slot >= 0) {
+#pragma unroll
+                for (int i = 0; i < kRowVpt; ++i) {
+                    if (i == own_slot) {
+                        float f[EPV];
+                        unpack<ES>(v[i], f);
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e)
+                            if (e == own_e) x_y = f[e];
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < kMaxScalars; ++s)
+                if (s == own_sc) x_y = xs[s];
+        }
+        if ((own_slot >= 0 || own_sc >= 0) && !aborted) p.row_loss[row] = lse - x_y;
+        if (rank == 0 && tid == 0 && p.lse && !aborted) p.lse[row] = lse;
+    }
+
+    // Loads still in flight exist only after an abort; let them land first.
+    if (tid == 0) {
+        while (c_v < p_v) {
+            const int st = static_cast<int>(c_v % static_cast<uint32_t>(p.stages));
+            (void)mbar_wait_bounded(&bars[st], (c_v / static_cast<uint32_t>(p.stages)) & 1u);
+            ++c_v;
+        }
+    }
+    if (K > 1) cluster_sync();  // peers may still read this CTA's cl_slot
+
+    __syncthreads();
+    if (tid == 0) {
+        if (aborted) atomicOr(&p.ws->err, static_cast<unsigned>(FOAK_ERRBIT_TIMEOUT));
+        __threadfence();
+        const unsigned t = atomicAdd(&p.ws->done, 1u);
+        s_last = t == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+
+    // Last CTA: loss = (sum of row terms in row order, float64) / D.
+    __threadfence();
+    double acc = 0.0;
+    for (int64_t i = tid; i < p.N; i += kRowThreads) acc += static_cast<double>(__ldcg(p.row_loss + i));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off);
+    if (lane == 0) dred[warp] = acc;
+    __syncthreads();
+    if (tid == 0) {
+        double tot = 0.0;
+        for (int w = 0; w < kRowWarps; ++w) tot += dred[w];
+        const double Dd = p.denom > 0.f ? static_cast<double>(p.denom) : static_cast<double>(n_valid);
+        *p.loss = static_cast<float>(tot / Dd);
+        if (p.n_valid) *p.n_valid = n_valid;
+        unsigned e = atomicExch(&p.ws->err, 0u);
+        if (n_bad > 0) e |= FOAK_ERRBIT_LABEL_RANGE;
+        if (p.err) *p.err = static_cast<int32_t>(e);
+        atomicExch(&p.ws->done, 0u);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+int64_t ce_rows_max_vocab(int elem_bytes) {
+    return static_cast<int64_t>(kRowMaxCluster) * kRowSliceVec * (16 / elem_bytes);
+}
+
+namespace {
+
+struct Plan {
+    int k, per, stages;
+    uint32_t stage_bytes;
+    size_t smem;
+};
+
+bool plan_rows(int ES, int64_t V, Plan* pl) {
+    const int64_t nb_max = V * ES / 16;
+    for (int k = 1; k <= kRowMaxCluster; k *= 2) {
+        const int64_t per = (nb_max + k - 1) / k;
+        if (per <= kRowSliceVec) {
+            pl->k = k;
+            pl->per = static_cast<int>(std::max<int64_t>(per, 1));
+            pl->stage_bytes = static_cast<uint32_t>(((pl->per * 16 + 127) / 128) * 128);
+            pl->stages = static_cast<int>(std::min<size_t>(kRowMaxStages, kSmemBudget / pl->stage_bytes));
+            pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes;
+            return pl->stages >= 2;
+        }
+    }
+    return false;
+}
+
+std::mutex g_mu;
+std::map<std::tuple<int, const void*, int, size_t>, int> g_clusters;  // (device, kernel, k, smem)
+std::map<std::pair<int, const void*>, bool> g_attr_set;                // (device, kernel)
+
+// Co-resident clusters for this kernel configuration (cached per device).  The
+// kernel's dynamic shared-memory limit is raised once per device to the full
+// budget, so every plan's size fits whatever order plans are launched in.
+cudaError_t resident_clusters(const void* kern, int k, size_t smem, int* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto key = std::make_tuple(dev, kern, k, smem);
+    auto it = g_clusters.find(key);
+    if (it != g_clusters.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    auto akey = std::make_pair(dev, kern);
+    if (!g_attr_set[akey]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBudget));
+        if (e != cudaSuccess) return e;
+        g_attr_set[akey] = true;
+    }
+    int n = 0;
+    if (k == 1) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowThreads, smem);
+        if (e != cudaSuccess) return e;
+        n = per_sm * device_sm_count();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(k), 1, 1);
+        cfg.blockDim = dim3(kRowThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(k);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+    }
+    if (n < 1) n = 1;
+    g_clusters[key] = n;
+    *out = n;
+    return cudaSuccess;
+}
+
+template <int ES, bool GRAD>
+cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t stream) {
+    const void* kern = reinterpret_cast<const void*>(&ce_rows_kernel<ES, GRAD>);
+    int ncl = 0;
+    cudaError_t e = resident_clusters(kern, pl.k, pl.smem, &ncl);
+    if (e != cudaSuccess) return e;
+    const int64_t want = std::max<int64_t>(1, std::min<int64_t>(ncl, base.N));
+    CeRowParams prm = base;
+    prm.k = pl.k;
+    prm.per = pl.per;
+    prm.stages = pl.stages;
+    prm.stage_bytes = pl.stage_bytes;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(want * pl.k), 1, 1);
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(pl.k);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ce_rows_kernel<ES, GRAD>, prm);
+}
+
+}  // namespace
+
+cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, int64_t ld,
+                           const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, float g,
+                           float denom, float* loss, float* lse, float* row_loss, int32_t* n_valid,
+                           int32_t* err, CeWsHeader* ws, cudaStream_t stream) {
+    Plan pl;
+    if (!plan_rows(elem_bytes, V, &pl)) return cudaErrorInvalidValue;
+    CeRowParams prm = {};
+    prm.x = static_cast<const char*>(x);
+    prm.dx = static_cast<char*>(dx);
+    prm.ld = ld;
+    prm.labels = labels;
+    prm.N = N;
+    prm.V = V;
+    prm.ignore_index = ignore_index;
+    prm.g = g;
+    prm.denom = denom;
+    prm.loss = loss;
+    prm.lse = lse;
+    prm.row_loss = row_loss;
+    prm.n_valid = n_valid;
+    prm.err = err;
+    prm.ws = ws;
+    if (elem_bytes == 2)
+        return grad ? launch_typed<2, true>(prm, pl, stream) : launch_typed<2, false>(prm, pl, stream);
+    return grad ? launch_typed<4, true>(prm, pl, stream) : launch_typed<4, false>(prm, pl, stream);
+}
+
+}  // namespace foak

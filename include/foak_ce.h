@@ -1,0 +1,155 @@
+/*
+ * foak_ce.h -- C ABI of the GB300 (sm_103a) fused cross-entropy library.
+ *
+ * The operation is the loss the fms-acceleration FOAK plugin swaps into a causal
+ * LM head: "Fast Cross Entropy Triton Kernels" on the fms-acceleration-foak 0.7.4
+ * page (list of fused operations and kernels), called FastCrossEntropyLoss in
+ * fms-acceleration PR #79 "Allow Kernels for Full FT and Non-Quantized PEFT"
+ * (Description, items 4 and 5).  The pages name the kernel but print no formula;
+ * this library computes the textbook softmax cross-entropy over the rows of an
+ * N x V logits matrix with mean reduction over rows whose label is not
+ * ignore_index:
+ *
+ *     lse_i = log sum_j exp(x_ij)          l_i = lse_i - x_{i, y_i}
+ *     loss  = sum_{valid i} l_i / D        D = denom > 0 ? denom : n_valid
+ *     dx_ij = (g / D) * (exp(x_ij - lse_i) - [j == y_i])   (0 on ignored rows)
+ *
+ * The chunked linear + CE call is the fused-linear form the pages name as
+ * LigerFusedLinearCrossEntropy ("Running Liger Kernel Benchmarks", foak page),
+ * "chunked loss" (PR #79, TODO) and FusedCrossEntropyLoss (fms-hf-tuning PR #280,
+ * "Notes on FastKernels").  A caller-supplied denom is the per-token mean across
+ * data-parallel ranks that PR #280 lists under LossAccelerationPlugin
+ * ("--loss_across_gpus mean token"): the caller all-reduces n_valid and passes it.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers marked (device) are device memory owned by the caller; the library
+ *   never allocates or frees.  Host pointers are marked (host).
+ * - Logits are row-major: element (i, j) is at logits[i * ld + j], ld >= V, in
+ *   FOAK_BF16 (bfloat16) or FOAK_F32.  fp16 is not accepted.
+ * - labels (device) are int64[N]; a label equal to ignore_index marks an ignored
+ *   row.  A label outside [0, V) that is not ignore_index is an error found on the
+ *   device: the row is treated as ignored and the error word gets
+ *   FOAK_ERRBIT_LABEL_RANGE.  Nothing traps.
+ * - stream is a cudaStream_t passed as void* (NULL = legacy default stream).  All
+ *   work is enqueued asynchronously on it; nothing synchronises unless the
+ *   environment variable FOAK_SYNC_CHECK=1 is set, in which case the call waits
+ *   for its own work and turns a non-zero error word into FOAK_ERR_LABEL_RANGE or
+ *   FOAK_ERR_TIMEOUT.
+ * - Problems checkable on the host return a status before anything is enqueued.
+ *   A failed launch returns FOAK_ERR_CUDA.  No C++ exception crosses the ABI.
+ * - Scalar outputs (loss, n_valid, err) are single device elements written by the
+ *   last kernel of the call.  With n_valid == 0 and denom <= 0 the loss is 0/0 =
+ *   NaN (as torch's mean reduction gives) and every gradient row is +0.0.
+ * - The result is deterministic for a given input and device: the loss is the
+ *   float64 sum of per-row float32 terms in row order, reduced by a fixed tree.
+ */
+#ifndef FOAK_CE_H
+#define FOAK_CE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FOAK_CE_ABI_VERSION 1
+
+typedef enum foak_status {
+    FOAK_OK = 0,
+    FOAK_ERR_INVALID_ARG = 1,   /* null/negative/misaligned argument, ld < V, ... */
+    FOAK_ERR_UNSUPPORTED = 2,   /* dtype or size outside what the kernels handle */
+    FOAK_ERR_LABEL_RANGE = 3,   /* (FOAK_SYNC_CHECK only) a label was out of range */
+    FOAK_ERR_WORKSPACE = 4,     /* workspace missing, misaligned or too small */
+    FOAK_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    FOAK_ERR_TIMEOUT = 6        /* (FOAK_SYNC_CHECK only) a device wait gave up */
+} foak_status;
+
+typedef enum foak_dtype { FOAK_F32 = 0, FOAK_BF16 = 1 } foak_dtype;
+
+/* Bits of the device error word (int32) that calls write when err != NULL. */
+#define FOAK_ERRBIT_LABEL_RANGE 1
+#define FOAK_ERRBIT_TIMEOUT 2
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* foak_status_string(int32_t status);
+
+/* ABI version of the loaded library (FOAK_CE_ABI_VERSION at build time). */
+int32_t foak_abi_version(void);
+
+/* Largest V the row kernels accept for a dtype (rows up to 8 CTAs x 64 KB). */
+int64_t foak_ce_max_vocab(int32_t dtype);
+
+/*
+ * Bytes of device workspace that foak_ce_forward / foak_ce_fwd_bwd need for N rows
+ * (a 256-byte header plus N float32 per-row loss terms).  The workspace must be
+ * 256-byte aligned and zero-filled before its first use; every call leaves the
+ * header zeroed again when its work completes, so one buffer can serve any number
+ * of stream-ordered calls.  Calls that share a workspace must not overlap on the
+ * GPU (same stream, or ordered by events).
+ */
+size_t foak_ce_workspace_size(int64_t N);
+
+/*
+ * Forward: one read of each non-ignored row (an ignored row is never read).
+ *   logits (device)   N x V, row stride ld (elements)
+ *   dtype             FOAK_BF16 or FOAK_F32
+ *   labels (device)   int64[N]
+ *   ignore_index      label value of ignored rows (usually -100)
+ *   denom             > 0: divide by denom (global valid-token count under data
+ *                     parallelism); <= 0: divide by this call's n_valid
+ *   loss (device)     float[1]: the mean loss
+ *   lse (device)      float[N] or NULL: log-sum-exp per row (0 for ignored rows);
+ *                     foak_ce_backward needs it
+ *   row_loss (device) float[N] or NULL: per-row terms lse_i - x_{i,y_i} (0 for
+ *                     ignored rows), i.e. reduction 'none'
+ *   n_valid (device)  int32[1] or NULL: rows with a label in [0, V)
+ *   err (device)      int32[1] or NULL: FOAK_ERRBIT_* of this call (0 = clean)
+ *   workspace (device) foak_ce_workspace_size(N) bytes, see above
+ */
+foak_status foak_ce_forward(const void* logits, int32_t dtype, int64_t ld, const int64_t* labels,
+                            int64_t N, int64_t V, int64_t ignore_index, float denom, float* loss,
+                            float* lse, float* row_loss, int32_t* n_valid, int32_t* err,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward: dlogits = (exp(logits - lse) - onehot) * g / D, ignored rows +0.0.
+ *   dlogits (device)  N x V with the same ld and dtype; may equal logits (in place)
+ *   logits (device)   as in forward (not read on ignored rows)
+ *   lse (device)      float[N] from foak_ce_forward
+ *   grad_out (device) float[1]: g, the upstream gradient of the loss; NULL = 1.0
+ *   denom             as in forward (<= 0: count n_valid again from labels)
+ *   err (device)      int32[1] or NULL: FOAK_ERRBIT_LABEL_RANGE if a label is bad
+ * Needs no workspace.
+ */
+foak_status foak_ce_backward(void* dlogits, const void* logits, int32_t dtype, int64_t ld,
+                             const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index,
+                             const float* lse, const float* grad_out, float denom, int32_t* err,
+                             void* stream);
+
+/*
+ * Fused forward + backward, in place: each non-ignored row is read once and its
+ * gradient written over it; ignored rows are only written (+0.0).  The logits are
+ * destroyed; a caller that still needs them calls forward + backward instead.
+ *   g (host)          upstream gradient of the loss (1.0 for a plain mean loss,
+ *                     or a loss-scale / accumulation factor)
+ *   lse (device)      float[N] or NULL, as in forward
+ *   other arguments   as in forward
+ */
+foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64_t* labels,
+                            int64_t N, int64_t V, int64_t ignore_index, float g, float denom,
+                            float* loss, float* lse, int32_t* n_valid, int32_t* err,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Test hook: the next `count` launches made by this library fail with
+ * FOAK_ERR_CUDA before anything is enqueued (host-side fault injection).
+ */
+void foak_test_fail_next_launches(int32_t count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FOAK_CE_H */

@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load, export every function include/foak_ce.h declares, and turn
+bad arguments (and an injected launch failure) into status codes before anything
+is enqueued.  The pointers below are never dereferenced: every call here returns
+before the first CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "foak_ce.h")
+
+
+@pytest.fixture(scope="module")
+def so():
+    from cross_entropy_loss_gb300 import _build
+
+    path = _build.build()
+    import cross_entropy_loss_gb300 as ce
+
+    return ce
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(foak_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(so):
+    names = _declared()
+    assert "foak_ce_fwd_bwd" in names and "foak_ce_forward" in names and "foak_ce_backward" in names
+    raw = ctypes.CDLL(so.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in foak_ce.h but not exported"
+    assert set(names) == set(so.SIGNATURES), "binding signatures and header drifted apart"
+
+
+def test_version_vocab_and_workspace(so):
+    assert so.lib.foak_abi_version() == 1
+    assert so.foak_ce_max_vocab(so.FOAK_BF16) >= 128256 * 2
+    assert so.foak_ce_max_vocab(so.FOAK_F32) >= 128256
+    assert so.foak_ce_max_vocab(7) == 0
+    assert so.foak_ce_workspace_size(0) == 256
+    assert so.foak_ce_workspace_size(8192) == 256 + 8192 * 4
+    assert so.foak_ce_workspace_size(3) == 512
+
+
+FAKE = 0x10000  # 64 KB-aligned fake device address (never touched)
+
+
+def _fwd_bwd(so, logits=FAKE, dtype=1, ld=32000, labels=FAKE, N=4, V=32000, loss=FAKE, ws=FAKE,
+             wsb=1 << 20, lse=None, nv=None, err=None):
+    return so.lib.foak_ce_fwd_bwd(logits, dtype, ld, labels, N, V, -100, 1.0, 0.0, loss, lse, nv, err, ws, wsb,
+                                  None)
+
+
+def test_argument_errors_return_before_launch(so):
+    E = so
+    assert _fwd_bwd(so, dtype=2) == E.FOAK_ERR_UNSUPPORTED           # fp16 / unknown dtype
+    assert _fwd_bwd(so, ld=31999) == E.FOAK_ERR_INVALID_ARG          # ld < V
+    assert _fwd_bwd(so, V=0) == E.FOAK_ERR_INVALID_ARG
+    assert _fwd_bwd(so, N=-1) == E.FOAK_ERR_INVALID_ARG
+    assert _fwd_bwd(so, logits=None) == E.FOAK_ERR_INVALID_ARG
+    assert _fwd_bwd(so, labels=None) == E.FOAK_ERR_INVALID_ARG
+    assert _fwd_bwd(so, loss=None) == E.FOAK_ERR_INVALID_ARG
+    assert _fwd_bwd(so, logits=FAKE + 1) == E.FOAK_ERR_INVALID_ARG   # bf16 needs 2-byte alignment
+    assert _fwd_bwd(so, labels=FAKE + 4) == E.FOAK_ERR_INVALID_ARG   # int64 labels
+    assert _fwd_bwd(so, lse=FAKE + 2) == E.FOAK_ERR_INVALID_ARG
+    assert _fwd_bwd(so, V=10 ** 7, ld=10 ** 7) == E.FOAK_ERR_UNSUPPORTED
+    assert _fwd_bwd(so, ws=None) == E.FOAK_ERR_WORKSPACE
+    assert _fwd_bwd(so, ws=FAKE + 16) == E.FOAK_ERR_WORKSPACE        # 256-byte alignment
+    assert _fwd_bwd(so, wsb=256) == E.FOAK_ERR_WORKSPACE             # too small for N rows
+    # backward: dlogits must share logits' 16-byte phase
+    st = so.lib.foak_ce_backward(FAKE + 2, FAKE, 1, 32000, FAKE, 4, 32000, -100, FAKE, None, 0.0, None, None)
+    assert st == E.FOAK_ERR_INVALID_ARG
+    st = so.lib.foak_ce_backward(FAKE, FAKE, 1, 32000, FAKE, 4, 32000, -100, None, None, 0.0, None, None)
+    assert st == E.FOAK_ERR_INVALID_ARG  # lse required
+
+
+def test_injected_launch_failure(so):
+    so.lib.foak_test_fail_next_launches(2)
+    try:
+        assert _fwd_bwd(so) == so.FOAK_ERR_CUDA
+        st = so.lib.foak_ce_forward(FAKE, 0, 64, FAKE, 4, 64, -100, 0.0, FAKE, None, None, None, None, FAKE,
+                                    1 << 20, None)
+        assert st == so.FOAK_ERR_CUDA
+    finally:
+        so.lib.foak_test_fail_next_launches(0)
+    # argument errors still win over the injected failure
+    so.lib.foak_test_fail_next_launches(1)
+    assert _fwd_bwd(so, dtype=5) == so.FOAK_ERR_UNSUPPORTED
+    so.lib.foak_test_fail_next_launches(0)
+
+
+def test_status_strings(so):
+    for code in range(7):
+        assert so.status_string(code).startswith("FOAK_")
+    assert "unknown" in so.status_string(99)
+    err = so.FoakError(so.FOAK_ERR_WORKSPACE, "x")
+    assert "WORKSPACE" in str(err)

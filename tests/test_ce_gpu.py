@@ -1,0 +1,240 @@
+"""GPU parity of the row kernels (forward, backward, fused fwd+bwd) against the oracle.
+
+Every call goes through the C ABI (via the ctypes binding).  Bars: loss within 1e-5
+relative (fp32 logits) or 2e-3 (bf16); dlogits within one bf16 ulp of the oracle or
+1e-6 absolute, whichever is larger; ignored rows bit-exact +0.0 and excluded from
+n_valid; n_valid and the error word exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from ce_helpers import (assert_grad_close, assert_loss_close, bits, sample_rows, to_device, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand(N, V, dtype, seed, ld=None, sigma=2.0, n_ignore=None, spikes=0.0):
+    x = wl.normal_matrix(N, V, seed=seed, sigma=sigma, dtype=dtype, ld=ld, spike_p=spikes, spike_lo=20.0,
+                         spike_hi=30.0)
+    y = wl.uniform_labels(N, V, seed=seed)
+    k = N // 7 if n_ignore is None else n_ignore
+    y[wl.pick_rows(N, min(k, N), seed=seed)] = -100
+    return x, y
+
+
+def _device_logits(x, dtype, V, col_offset=0):
+    """Device N x V view (row stride = x's ld); col_offset shifts the base by whole elements."""
+    t = to_device(x, dtype)
+    return t[:, col_offset:col_offset + V]
+
+
+def _check_fused(ce, x, y, V, dtype, g=1.0, denom=0.0, ii=-100, col_offset=0):
+    xv = x[:, col_offset:col_offset + V] if col_offset else x
+    ref = oracle.ce(np.ascontiguousarray(xv) if col_offset else x, y, V, ignore_index=ii, g=g, denom=denom)
+    t = _device_logits(x, dtype, V, col_offset)
+    out = ce.foak_ce_fwd_bwd(t, torch.from_numpy(y).cuda(), g=g, denom=denom, ignore_index=ii, want_lse=True)
+    torch.cuda.synchronize()
+    assert_loss_close(out["loss"].item(), ref["loss"], dtype)
+    assert out["n_valid"].item() == ref["n_valid"]
+    assert out["err"].item() == (1 if ref["n_bad"] else 0)
+    got = to_f64(t)
+    assert_grad_close(got, ref["grad"])
+    valid = ref["state"] == oracle.VALID
+    np.testing.assert_allclose(to_f64(out["lse"])[valid], ref["lse"][valid], rtol=2e-6, atol=2e-6)
+    assert np.all(bits(t)[~valid] == 0), "ignored rows must be +0.0 bit-exact"
+    return out, ref
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+@pytest.mark.parametrize("N,V", [(1, 1), (3, 2), (5, 7), (9, 8), (17, 9), (64, 1000), (33, 4097),
+                                 (40, 32000), (13, 32003)])
+def test_fused_small_shapes(cuda_lib, dtype, N, V):
+    x, y = _rand(N, V, dtype, seed=100 + N + V)
+    _check_fused(cuda_lib, x, y, V, dtype)
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+@pytest.mark.parametrize("N,V", [(6, 40000), (7, 70001), (5, 128256)])
+def test_fused_cluster_rows(cuda_lib, dtype, N, V):
+    # rows longer than one CTA's 64 KB slice are split over a cluster of 2-8 CTAs
+    x, y = _rand(N, V, dtype, seed=200 + V, sigma=3.0, n_ignore=1, spikes=1e-4)
+    _check_fused(cuda_lib, x, y, V, dtype)
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+@pytest.mark.parametrize("V,ld,off", [(1000, 1024, 0), (1001, 1001, 0), (999, 1008, 1), (5003, 5011, 3),
+                                      (40001, 40001, 0), (70003, 70016, 5)])
+def test_fused_padded_and_unaligned_rows(cuda_lib, dtype, V, ld, off):
+    N = 11
+    x = wl.normal_matrix(N, ld, seed=V + ld, sigma=2.0, dtype=dtype)
+    y = wl.uniform_labels(N, V, seed=V)
+    y[3] = -100
+    y[0] = 0
+    y[1] = V - 1  # label in the scalar head / tail
+    _check_fused(cuda_lib, x, y, V, dtype, col_offset=off)
+    # padding columns untouched by the in-place call? (only the N x V view is written)
+
+
+def test_fused_padding_columns_untouched(cuda_lib):
+    N, V, ld = 8, 3001, 3072
+    x = wl.normal_matrix(N, ld, seed=3, sigma=2.0, dtype=wl.BF16)
+    y = wl.uniform_labels(N, V, seed=3)
+    y[2] = -100
+    full = to_device(x, wl.BF16)
+    before = bits(full)[:, V:].copy()
+    cuda_lib.foak_ce_fwd_bwd(full[:, :V], torch.from_numpy(y).cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(full)[:, V:], before)
+
+
+def test_tiny_config_all_entry_points(cuda_lib):
+    c = wl.tiny()
+    x, y, V = c["logits"], c["labels"], c["V"]
+    ref = oracle.ce(x, y, g=1.0)
+    yd = torch.from_numpy(y).cuda()
+    # fused
+    _check_fused(cuda_lib, x, y, V, wl.F32)
+    # forward
+    t = to_device(x, wl.F32)
+    f = cuda_lib.foak_ce_forward(t, yd, want_lse=True, want_row_loss=True)
+    torch.cuda.synchronize()
+    assert_loss_close(f["loss"].item(), ref["loss"], wl.F32)
+    np.testing.assert_allclose(to_f64(f["row_loss"]), ref["row_loss"], rtol=1e-5, atol=1e-5)
+    np.testing.assert_array_equal(to_f64(t), x.astype(np.float64))  # forward does not write logits
+    # backward (out of place, then in place), g as a device scalar
+    g = torch.tensor([2.5], dtype=torch.float32, device="cuda")
+    d, err = cuda_lib.foak_ce_backward(t, yd, f["lse"], g)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert_grad_close(to_f64(d), 2.5 * ref["grad"])
+    d2, _ = cuda_lib.foak_ce_backward(t, yd, f["lse"], g, dlogits=t)
+    torch.cuda.synchronize()
+    assert_grad_close(to_f64(t), 2.5 * ref["grad"])
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+def test_forward_backward_padded_unaligned(cuda_lib, dtype):
+    N, V, ld, off = 21, 33001, 33013, 1
+    x = wl.normal_matrix(N, ld, seed=9, sigma=2.0, dtype=dtype)
+    y = wl.uniform_labels(N, V, seed=9)
+    y[[4, 5]] = -100
+    xv = np.ascontiguousarray(x[:, off:off + V])
+    ref = oracle.ce(xv, y)
+    t = to_device(x, dtype)[:, off:off + V]
+    yd = torch.from_numpy(y).cuda()
+    f = cuda_lib.foak_ce_forward(t, yd)
+    d, _ = cuda_lib.foak_ce_backward(t, yd, f["lse"])
+    torch.cuda.synchronize()
+    assert_loss_close(f["loss"].item(), ref["loss"], dtype)
+    assert_grad_close(to_f64(d), ref["grad"])
+    assert np.all(bits(d)[[4, 5]] == 0)
+
+
+def test_g_denom_and_ignore_index(cuda_lib):
+    x, y = _rand(50, 3000, wl.BF16, seed=77)
+    y[y == -100] = -1
+    _check_fused(cuda_lib, x, y, 3000, wl.BF16, g=0.37, denom=123.0, ii=-1)
+
+
+def test_all_rows_ignored_and_empty(cuda_lib):
+    x = wl.normal_matrix(4, 500, seed=1, sigma=1.0, dtype=wl.F32)
+    y = np.full(4, -100, dtype=np.int64)
+    t = to_device(x, wl.F32)
+    out = cuda_lib.foak_ce_fwd_bwd(t, torch.from_numpy(y).cuda())
+    torch.cuda.synchronize()
+    assert math.isnan(out["loss"].item()) and out["n_valid"].item() == 0
+    assert np.all(bits(t) == 0)
+    e = torch.empty(0, 500, dtype=torch.float32, device="cuda")
+    out = cuda_lib.foak_ce_fwd_bwd(e, torch.empty(0, dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert math.isnan(out["loss"].item()) and out["n_valid"].item() == 0 and out["err"].item() == 0
+
+
+def test_bad_labels_flagged_and_ignored(cuda_lib):
+    x, y = _rand(30, 777, wl.F32, seed=5)
+    y[2] = 777
+    y[9] = -5
+    out, ref = _check_fused(cuda_lib, x, y, 777, wl.F32)
+    assert ref["n_bad"] == 2 and out["err"].item() == 1
+
+
+def test_data_parallel_shards_compose(cuda_lib):
+    # per-token mean across ranks: each shard divides by the global n_valid
+    x, y = _rand(96, 5000, wl.BF16, seed=31)
+    n_valid = oracle.count(y, 5000)[0]
+    full = to_device(x, wl.BF16)
+    o = cuda_lib.foak_ce_fwd_bwd(full, torch.from_numpy(y).cuda())
+    parts = []
+    tot = 0.0
+    for a, b in [(0, 40), (40, 96)]:
+        s = to_device(np.ascontiguousarray(x[a:b]), wl.BF16)
+        r = cuda_lib.foak_ce_fwd_bwd(s, torch.from_numpy(y[a:b].copy()).cuda(), denom=float(n_valid))
+        tot += r["loss"].item()
+        parts.append(s)
+    torch.cuda.synchronize()
+    assert tot == pytest.approx(o["loss"].item(), rel=1e-6)
+    np.testing.assert_array_equal(bits(torch.cat(parts)), bits(full))
+
+
+def test_deterministic_and_workspace_reuse(cuda_lib):
+    x, y = _rand(300, 2048, wl.BF16, seed=8)
+    losses = set()
+    for n in [300, 17, 300, 1, 300]:
+        t = to_device(np.ascontiguousarray(x[:n]), wl.BF16)
+        o = cuda_lib.foak_ce_fwd_bwd(t, torch.from_numpy(y[:n].copy()).cuda())
+        if n == 300:
+            losses.add(o["loss"].item())
+    torch.cuda.synchronize()
+    assert len(losses) == 1
+    ws = cuda_lib.workspace(300, torch.device("cuda"))
+    assert int(ws[:256].count_nonzero().item()) == 0  # header back to zero
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def _full_size(cuda_lib, cfg, extra_rows=()):
+    x, y, V, dtype = cfg["logits"], cfg["labels"], cfg["V"], cfg["dtype"]
+    N = x.shape[0]
+    n_valid, _ = oracle.count(y, V)
+    scale = oracle.scale_of(1.0, 0.0, n_valid)
+    lse, rl, st, _ = oracle.rows(x, y, V, scale=scale, want_grad=False)
+    ref_loss = oracle.mean(rl, st)
+    t = to_device(x, dtype)
+    out = cuda_lib.foak_ce_fwd_bwd(t, torch.from_numpy(y).cuda(), want_lse=True)
+    torch.cuda.synchronize()
+    assert_loss_close(out["loss"].item(), ref_loss, dtype)
+    assert out["n_valid"].item() == n_valid and out["err"].item() == 0
+    valid = st == oracle.VALID
+    np.testing.assert_allclose(to_f64(out["lse"])[valid], lse[valid], rtol=2e-6, atol=2e-6)
+    rows = sample_rows(N, y, extra=extra_rows)
+    _, _, _, g = oracle.rows(x[rows], y[rows], V, scale=scale)
+    idx = torch.from_numpy(rows).cuda()
+    got = to_f64(t.index_select(0, idx))
+    assert_grad_close(got, g)
+    ign = torch.from_numpy(np.nonzero(~valid)[0]).cuda()
+    assert int(t.index_select(0, ign).view(torch.int16 if dtype == wl.BF16 else torch.int32)
+               .count_nonzero().item()) == 0
+    return out, lse
+
+
+def test_mistral_batch_full_size(cuda_lib):
+    _full_size(cuda_lib, wl.mistral())
+
+
+def test_packed_batch_full_size(cuda_lib):
+    _full_size(cuda_lib, wl.packed())
+
+
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
+def test_llama3_vocab_full_size(cuda_lib, dtype):
+    cfg = wl.llama3(dtype=dtype)
+    out, lse = _full_size(cuda_lib, cfg, extra_rows=(wl.LLAMA3_CONST_ROW,))
+    r = wl.LLAMA3_CONST_ROW
+    # the all-equal row: lse = 3 + ln V exactly in the oracle
+    assert lse[r] == pytest.approx(3.0 + math.log(128256), abs=1e-12)
+    assert to_f64(out["lse"])[r] == pytest.approx(3.0 + math.log(128256), abs=3e-6)
