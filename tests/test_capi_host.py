@@ -17,9 +17,9 @@ HEADER = os.path.join(ROOT, "include", "foak_ce.h")
 
 @pytest.fixture(scope="module")
 def so():
-    from cross_entropy_loss_gb300 import _build
+    import __graft_entry__
 
-    path = _build.build()
+    __graft_entry__._build_module().build()
     import cross_entropy_loss_gb300 as ce
 
     return ce
