@@ -167,7 +167,12 @@ def foak_ce_backward(logits, labels, lse, grad_out=None, *, dlogits=None, ignore
     dev = logits.device
     labels = _labels_arg(labels, N, dev)
     if dlogits is None:
-        dlogits = torch.empty_strided(logits.shape, logits.stride(), dtype=logits.dtype, device=dev)
+        # same row stride and the same offset modulo 16 bytes as logits (the kernels share row geometry)
+        es = logits.element_size()
+        shift = (logits.data_ptr() % 16) // es
+        n = ((N - 1) * ld + V + shift) if N > 0 else 1
+        base = torch.empty(n, dtype=logits.dtype, device=dev)
+        dlogits = base.as_strided((N, V), (ld, 1), storage_offset=shift)
     if dlogits.shape != logits.shape or dlogits.stride() != logits.stride() or dlogits.dtype != logits.dtype:
         raise ValueError("dlogits must match logits in shape, strides and dtype")
     if lse.dtype != torch.float32 or lse.numel() != N or not lse.is_contiguous():
