@@ -238,7 +238,7 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    sampler = ClockSampler(dev.index) if rank == 0 else None
+    sampler = ClockSampler(dev.index) if rank == 0 and not args.profile else None
 
     def upload(a, dtype):
         if dtype == wl.BF16:
@@ -333,6 +333,8 @@ def run_ours(args, rank, world, dist):
         "gpu_launches": args.steps,
     }
 
+    if args.profile:
+        return res
     # end-to-end through the public API: pinned host logits -> device, fused call, loss -> host
     if rank == 0 or dist is not None:
         res["e2e"] = e2e_timing(ce, torch, dev, stream, main, max(3, min(args.steps, 20)), upload, barrier,
@@ -506,6 +508,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="mistral")
     ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--profile", action="store_true",
+                    help="headline timed loop only (no e2e, secondary, clocks or CPU baseline): for ncu captures")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
