@@ -45,6 +45,8 @@ SIGNATURES = {
     "foak_ce_backward": (_i32, [_vp, _vp, _i32, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp]),
     "foak_ce_fwd_bwd": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _sz,
                                _vp]),
+    "foak_ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
+                                       _vp]),
     "foak_test_fail_next_launches": (None, [_i32]),
 }
 
@@ -204,4 +206,31 @@ def foak_ce_fwd_bwd(logits, labels, *, g: float = 1.0, ignore_index: int = -100,
                              _ptr(loss), _ptr(lse), _ptr(n_valid), _ptr(err), _ptr(ws), ws.numel(),
                              _stream(dev, stream))
     _check(st, "foak_ce_fwd_bwd")
+    return dict(loss=loss, n_valid=n_valid, err=err, lse=lse)
+
+
+FOAK_CE_NOALLOC_MAX_ROWS = 262144
+
+
+def foak_ce_fwd_bwd_noalloc(logits, labels, *, g: float = 1.0, ignore_index: int = -100, denom: float = 0.0,
+                            want_lse: bool = False, stream=None):
+    """Fused forward + backward in place, for callers that may not allocate device memory.
+
+    Same result as :func:`foak_ce_fwd_bwd`, but the library takes its scratch from a
+    fixed array in its own device image instead of a workspace, so no workspace
+    buffer is needed (this wrapper still allocates its small output tensors with
+    torch; a C caller passes its own).  N is limited to FOAK_CE_NOALLOC_MAX_ROWS,
+    and calls that overlap on the GPU race on the shared scratch.
+    """
+    N, V, ld, dt = _logits_args(logits)
+    dev = logits.device
+    labels = _labels_arg(labels, N, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int32, device=dev)
+    err = torch.empty(1, dtype=torch.int32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
+    st = lib.foak_ce_fwd_bwd_noalloc(_ptr(logits), dt, ld, _ptr(labels), N, V, int(ignore_index), float(g),
+                                     float(denom), _ptr(loss), _ptr(lse), _ptr(n_valid), _ptr(err),
+                                     _stream(dev, stream))
+    _check(st, "foak_ce_fwd_bwd_noalloc")
     return dict(loss=loss, n_valid=n_valid, err=err, lse=lse)

@@ -143,6 +143,37 @@ foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Largest N that foak_ce_fwd_bwd_noalloc accepts (its fixed scratch holds one
+ * float per row: 1 MiB plus a 256-byte header on every device that loads the
+ * library, kept until the process exits).
+ */
+#define FOAK_CE_NOALLOC_MAX_ROWS 262144
+
+/*
+ * Fused forward + backward without any workspace from the caller.  The pages
+ * have no counterpart to this call; it exists for callers that must not allocate
+ * device memory while they run -- e.g. code on a latency-critical path, where
+ * cudaMalloc/cudaFree can synchronise the whole device, or a plugin inside a
+ * runtime that owns all device memory and forbids allocations during execution.
+ * It computes exactly what foak_ce_fwd_bwd computes, with the same arguments
+ * minus the workspace, and allocates nothing: its scratch is a fixed array in the
+ * library's device image.
+ *   N                 at most FOAK_CE_NOALLOC_MAX_ROWS; larger N returns
+ *                     FOAK_ERR_WORKSPACE before anything is enqueued
+ *   stream            besides the kernel, the call enqueues a 256-byte
+ *                     cudaMemsetAsync that clears the scratch header
+ * The first call on a device looks up the scratch array's device address (once
+ * per device, with that device current); make that first call before any stream
+ * capture begins.  Every call on a device shares the one scratch array, so calls
+ * that overlap on the GPU (different streams without ordering) race and give
+ * wrong results: serialise them.
+ */
+foak_status foak_ce_fwd_bwd_noalloc(void* logits, int32_t dtype, int64_t ld, const int64_t* labels,
+                                    int64_t N, int64_t V, int64_t ignore_index, float g, float denom,
+                                    float* loss, float* lse, int32_t* n_valid, int32_t* err,
+                                    void* stream);
+
+/*
  * Test hook: the next `count` launches made by this library fail with
  * FOAK_ERR_CUDA before anything is enqueued (host-side fault injection).
  */
