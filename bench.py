@@ -250,7 +250,8 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def fused_timing(cfg, steps, warmup, record_clocks, use_dist=True):
+    def fused_timing(cfg, steps, warmup, record_clocks, use_dist=True, call=None):
+        call = call or ce.foak_ce_fwd_bwd
         x = upload(cfg["logits"], cfg["dtype"])
         y = torch.from_numpy(cfg["labels"]).to(dev)
         N = x.shape[0]
@@ -259,7 +260,7 @@ def run_ours(args, rank, world, dist):
         _fill(bufs, x)
         del x
         for i in range(warmup):
-            ce.foak_ce_fwd_bwd(bufs[i % len(bufs)], y, workspace_tensor=ws)
+            call(bufs[i % len(bufs)], y, workspace_tensor=ws)
         if warmup and len(bufs) < steps + warmup:
             _fill(bufs, upload(cfg["logits"], cfg["dtype"]))
         barrier(use_dist)
@@ -269,7 +270,7 @@ def run_ours(args, rank, world, dist):
         e0.record(stream)
         out = None
         for i in range(steps):
-            out = ce.foak_ce_fwd_bwd(bufs[(warmup + i) % len(bufs)], y, workspace_tensor=ws)
+            out = call(bufs[(warmup + i) % len(bufs)], y, workspace_tensor=ws)
         e1.record(stream)
         e1.synchronize()
         t1 = time.perf_counter()
@@ -294,7 +295,10 @@ def run_ours(args, rank, world, dist):
     main = _make(args.workload)
     if sampler:
         sampler.start()
-    ms, loss, err, reused = fused_timing(main, args.steps, args.warmup, True)
+    call = None
+    if args.profile and args.path == "forward":
+        call = lambda b, y, workspace_tensor: ce.foak_ce_forward(b, y, workspace_tensor=workspace_tensor)  # noqa: E731
+    ms, loss, err, reused = fused_timing(main, args.steps, args.warmup, True, call=call)
     ms = max_over_ranks(ms)
     if sampler:
         sampler.stop()
@@ -508,6 +512,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="mistral")
     ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--path", choices=["fused", "forward"], default="fused",
+                    help="with --profile: which entry point the timed loop calls")
     ap.add_argument("--profile", action="store_true",
                     help="headline timed loop only (no e2e, secondary, clocks or CPU baseline): for ncu captures")
     args = ap.parse_args()

@@ -38,7 +38,8 @@ constexpr int kRowMaxStages = 4;
 constexpr int kRowMaxCluster = 8;
 constexpr int kMaxScalars = 7;                        // head or tail: < 16 bytes of bf16
 constexpr uint32_t kBulkChunk = 32768;
-constexpr size_t kSmemBudget = 227 * 1024 - 2048;     // dynamic smem left after static use
+constexpr int kLabCache = 1024;                       // labels of a CTA's first rows kept in smem
+constexpr size_t kSmemBudget = 227 * 1024 - 10 * 1024; // dynamic smem left after static use
 
 struct CeRowParams {
     const char* x;
@@ -117,13 +118,149 @@ __device__ __forceinline__ void store_scalar(char* p, float v) {
     else *reinterpret_cast<float*>(p) = v;
 }
 
+// Per-thread arithmetic on the thread's slice (kRowVpt 16-byte vectors).  Vectors
+// beyond the slice hold -inf, which no max picks and whose exp is 0, so the
+// loops run without predicates.
+template <int ES>
+struct RowMath;
+
+template <>
+struct RowMath<2> {  // bf16: 8 elements per vector, handled as 4 packed pairs
+    static __device__ __forceinline__ uint4 pad() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
+    static __device__ __forceinline__ float vmax(const uint4 (&v)[kRowVpt]) {
+        uint32_t a = v[0].x, b = v[0].y, c = v[0].z, d = v[0].w;
+#pragma unroll
+        for (int i = 1; i < kRowVpt; ++i) {
+            a = bf16x2_max(a, v[i].x);
+            b = bf16x2_max(b, v[i].y);
+            c = bf16x2_max(c, v[i].z);
+            d = bf16x2_max(d, v[i].w);
+        }
+        const uint32_t m = bf16x2_max(bf16x2_max(a, b), bf16x2_max(c, d));
+        return fmaxf(bf16_lo(m), bf16_hi(m));
+    }
+    // sum over the slice of 2^(x*log2e - mb)
+    static __device__ __forceinline__ float vsum(const uint4 (&v)[kRowVpt], float mb) {
+        const f32x2_t L = f2_pack(kLog2e, kLog2e), C = f2_pack(-mb, -mb);
+        f32x2_t a = 0, b = 0, c = 0, d = 0;
+#pragma unroll
+        for (int i = 0; i < kRowVpt; ++i) {
+            a = f2_add(a, f2_ex2(f2_fma(bf16x2_to_f2(v[i].x), L, C)));
+            b = f2_add(b, f2_ex2(f2_fma(bf16x2_to_f2(v[i].y), L, C)));
+            c = f2_add(c, f2_ex2(f2_fma(bf16x2_to_f2(v[i].z), L, C)));
+            d = f2_add(d, f2_ex2(f2_fma(bf16x2_to_f2(v[i].w), L, C)));
+        }
+        float lo, hi;
+        f2_unpack(f2_add(f2_add(a, b), f2_add(c, d)), lo, hi);
+        return lo + hi;
+    }
+    // 2^(x*log2e - c) for every element, optionally times S
+    template <bool MUL>
+    static __device__ __forceinline__ uint4 vexp(const uint4& v, f32x2_t L, f32x2_t C, f32x2_t S) {
+        uint4 o;
+        f32x2_t t0 = f2_ex2(f2_fma(bf16x2_to_f2(v.x), L, C));
+        f32x2_t t1 = f2_ex2(f2_fma(bf16x2_to_f2(v.y), L, C));
+        f32x2_t t2 = f2_ex2(f2_fma(bf16x2_to_f2(v.z), L, C));
+        f32x2_t t3 = f2_ex2(f2_fma(bf16x2_to_f2(v.w), L, C));
+        if (MUL) {
+            t0 = f2_mul(t0, S);
+            t1 = f2_mul(t1, S);
+            t2 = f2_mul(t2, S);
+            t3 = f2_mul(t3, S);
+        }
+        o.x = f2_to_bf16x2(t0);
+        o.y = f2_to_bf16x2(t1);
+        o.z = f2_to_bf16x2(t2);
+        o.w = f2_to_bf16x2(t3);
+        return o;
+    }
+};
+
+template <>
+struct RowMath<4> {  // fp32: 4 elements per vector, 2 packed pairs
+    static __device__ __forceinline__ uint4 pad() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
+    static __device__ __forceinline__ float vmax(const uint4 (&v)[kRowVpt]) {
+        float a = __uint_as_float(v[0].x), b = __uint_as_float(v[0].y);
+        float c = __uint_as_float(v[0].z), d = __uint_as_float(v[0].w);
+#pragma unroll
+        for (int i = 1; i < kRowVpt; ++i) {
+            a = fmaxf(a, __uint_as_float(v[i].x));
+            b = fmaxf(b, __uint_as_float(v[i].y));
+            c = fmaxf(c, __uint_as_float(v[i].z));
+            d = fmaxf(d, __uint_as_float(v[i].w));
+        }
+        return fmaxf(fmaxf(a, b), fmaxf(c, d));
+    }
+    static __device__ __forceinline__ float vsum(const uint4 (&v)[kRowVpt], float mb) {
+        const f32x2_t L = f2_pack(kLog2e, kLog2e), C = f2_pack(-mb, -mb);
+        f32x2_t a = 0, b = 0, c = 0, d = 0;
+#pragma unroll
+        for (int i = 0; i < kRowVpt; i += 2) {
+            a = f2_add(a, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i].x), __uint_as_float(v[i].y)), L, C)));
+            b = f2_add(b, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i].z), __uint_as_float(v[i].w)), L, C)));
+            c = f2_add(c, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i + 1].x), __uint_as_float(v[i + 1].y)), L, C)));
+            d = f2_add(d, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i + 1].z), __uint_as_float(v[i + 1].w)), L, C)));
+        }
+        float lo, hi;
+        f2_unpack(f2_add(f2_add(a, b), f2_add(c, d)), lo, hi);
+        return lo + hi;
+    }
+    template <bool MUL>
+    static __device__ __forceinline__ uint4 vexp(const uint4& v, f32x2_t L, f32x2_t C, f32x2_t S) {
+        f32x2_t t0 = f2_ex2(f2_fma(f2_pack(__uint_as_float(v.x), __uint_as_float(v.y)), L, C));
+        f32x2_t t1 = f2_ex2(f2_fma(f2_pack(__uint_as_float(v.z), __uint_as_float(v.w)), L, C));
+        if (MUL) {
+            t0 = f2_mul(t0, S);
+            t1 = f2_mul(t1, S);
+        }
+        uint4 o;
+        float a, b;
+        f2_unpack(t0, a, b);
+        o.x = __float_as_uint(a);
+        o.y = __float_as_uint(b);
+        f2_unpack(t1, a, b);
+        o.z = __float_as_uint(a);
+        o.w = __float_as_uint(b);
+        return o;
+    }
+};
+
+// Element e (runtime index) of a vector, without dynamic register indexing.
+template <int ES>
+__device__ __forceinline__ float vec_elem(const uint4& v, int e) {
+    float f[16 / ES];
+    unpack<ES>(v, f);
+    float r = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16 / ES; ++k)
+        if (k == e) r = f[k];
+    return r;
+}
+
+// The label's vector: same values as the fast path, minus scale at element e.
+template <int ES>
+__device__ __forceinline__ uint4 vec_grad_label(const uint4& v, int e_own, float c, bool mul, float scale) {
+    constexpr int EPV = 16 / ES;
+    float f[EPV], d[EPV];
+    unpack<ES>(v, f);
+#pragma unroll
+    for (int k = 0; k < EPV; ++k) {
+        float q = ex2(fmaf(f[k], kLog2e, -c));
+        if (mul) q *= scale;
+        d[k] = k == e_own ? q - scale : q;
+    }
+    return pack<ES>(d);
+}
+
 template <int ES, bool GRAD>
 __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowParams p) {
     constexpr int EPV = 16 / ES;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t bars[kRowMaxStages];
-    __shared__ float2 red[kRowWarps];
+    __shared__ float red_m[kRowWarps];
+    __shared__ float red_s[kRowWarps];
     __shared__ float2 cl_slot[2];
+    __shared__ int64_t s_lab[kLabCache];
     __shared__ int iscratch[2 * kRowWarps];
     __shared__ double dred[kRowWarps];
     __shared__ int s_abort, s_last;
@@ -149,11 +286,15 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
     // Producer state (thread 0): next row iteration to look at, valid rows issued.
     int64_t p_it = 0;
     uint32_t p_v = 0;
+    bool lab_cached = false;
+    auto label_of = [&](int64_t it) -> int64_t {
+        return (lab_cached && it < kLabCache) ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
+    };
     auto issue_next = [&]() {
         while (p_it < n_it) {
             const int64_t row = cid + p_it * ncl;
+            const int64_t y = label_of(p_it);
             ++p_it;
-            const int64_t y = __ldg(p.labels + row);
             if (y == p.ignore_index || y < 0 || y >= p.V) continue;
             const char* rowp = p.x + row * row_bytes;
             const RowGeom gm = row_geom<ES>(rowp, p.V);
@@ -178,12 +319,16 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
     count_labels(p.labels, p.N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
     const float D = p.denom > 0.f ? p.denom : static_cast<float>(n_valid);
     const float scale = p.g / D;
+    // Labels of this CTA's first rows, for the row loop and the producer.
+    for (int64_t it = tid; it < n_it && it < kLabCache; it += blockDim.x) s_lab[it] = __ldg(p.labels + cid + it * ncl);
+    __syncthreads();
+    lab_cached = true;
 
     uint32_t c_v = 0;
     bool aborted = false;
     for (int64_t it = 0; it < n_it; ++it) {
         const int64_t row = cid + it * ncl;
-        const int64_t y = __ldg(p.labels + row);
+        const int64_t y = label_of(it);
         const bool valid = y != p.ignore_index && y >= 0 && y < p.V;
         const char* rowp = p.x + row * row_bytes;
         const RowGeom gm = row_geom<ES>(rowp, p.V);
@@ -219,13 +364,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
         ++c_v;
         if (!aborted && !mbar_wait_bounded(&bars[st], par)) s_abort = 1;
 
-        // Slice -> registers; scalars straight from global memory.
+        // Slice -> registers (vectors past the slice hold -inf); scalars from global memory.
         uint4 v[kRowVpt];
         const uint4* sb = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(st) * p.stage_bytes);
+        const uint4 pad = RowMath<ES>::pad();
 #pragma unroll
         for (int i = 0; i < kRowVpt; ++i) {
             const int lv = tid + i * kRowThreads;
-            v[i] = lv < nl ? sb[lv] : make_uint4(0u, 0u, 0u, 0u);
+            v[i] = lv < nl ? sb[lv] : pad;
         }
         float xs[kMaxScalars];
         int ns = 0;
@@ -235,52 +381,33 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
 #pragma unroll
         for (int s = 0; s < kMaxScalars; ++s) xs[s] = s < ns ? load_scalar<ES>(rowp + (c0 + s) * ES) : kNegInf;
 
-        __syncthreads();  // the stage is consumed; s_abort is settled
+        // Row max: thread -> warp -> CTA.  The barrier that publishes the warp
+        // maxima also frees the stage for the producer.
+        float m = RowMath<ES>::vmax(v);
+#pragma unroll
+        for (int s = 0; s < kMaxScalars; ++s) m = fmaxf(m, xs[s]);
+        m = warp_max(m);
+        if (lane == 0) red_m[warp] = m;
+        __syncthreads();
         if (s_abort) aborted = true;
         if (tid == 0 && !aborted) {
             fence_proxy_async_smem();
             issue_next();
         }
+        float M = warp_max(lane < kRowWarps ? red_m[lane] : kNegInf);
 
-        // Thread (max, sum exp(x - max)).
-        float m = kNegInf;
+        // Sum of exp(x - M) relative to the CTA max, so no rescaling is needed in the CTA.
+        const float mb = M == kNegInf ? 0.f : M * kLog2e;
+        float sum = RowMath<ES>::vsum(v, mb);
 #pragma unroll
-        for (int i = 0; i < kRowVpt; ++i) {
-            if (tid + i * kRowThreads < nl) {
-                float f[EPV];
-                unpack<ES>(v[i], f);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) m = fmaxf(m, f[e]);
-            }
-        }
-#pragma unroll
-        for (int s = 0; s < kMaxScalars; ++s) m = fmaxf(m, xs[s]);
-        float sum = 0.f;
-        if (m != kNegInf) {
-            const float mb = m * kLog2e;
-#pragma unroll
-            for (int i = 0; i < kRowVpt; ++i) {
-                if (tid + i * kRowThreads < nl) {
-                    float f[EPV];
-                    unpack<ES>(v[i], f);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) sum += ex2(fmaf(f[e], kLog2e, -mb));
-                }
-            }
-#pragma unroll
-            for (int s = 0; s < kMaxScalars; ++s)
-                if (s < ns) sum += ex2(fmaf(xs[s], kLog2e, -mb));
-        }
-
-        // Merge: warp -> CTA -> cluster.  Every warp merges the CTA's 16 partials
-        // itself (same order, same result), so no second CTA barrier is needed.
-        warp_ms_reduce(m, sum);
-        if (lane == 0) red[warp] = make_float2(m, sum);
+        for (int s = 0; s < kMaxScalars; ++s)
+            if (s < ns) sum += ex2(fmaf(xs[s], kLog2e, -mb));
+        sum = warp_sum(sum);
+        if (lane == 0) red_s[warp] = sum;
         __syncthreads();
-        float2 r = lane < kRowWarps ? red[lane] : make_float2(kNegInf, 0.f);
-        float M = r.x, S = r.y;
-        warp_ms_reduce(M, S);
+        float S = warp_sum(lane < kRowWarps ? red_s[lane] : 0.f);
         if (K > 1) {
+            // cluster: merge the CTAs' (max, sum) pairs read through distributed shared memory
             const int slot = c_v & 1u;
             if (tid == 0) cl_slot[slot] = make_float2(M, S);
             cluster_sync();
@@ -289,79 +416,68 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
             M = q.x;
             S = q.y;
             warp_ms_reduce(M, S);
+            M = __shfl_sync(0xffffffffu, M, 0);
+            S = __shfl_sync(0xffffffffu, S, 0);
         }
-        M = __shfl_sync(0xffffffffu, M, 0);
-        S = __shfl_sync(0xffffffffu, S, 0);
         const float lse = M + logf(S);
 
-        // Which thread holds the label column.
+        // Which thread holds the label column (no division: kRowThreads is a power of 2).
         int own_slot = -1, own_e = 0, own_sc = -1;
         if (y < gm.h) {
             if (rank == 0 && tid == 0) own_sc = static_cast<int>(y);
         } else if (y < tail_col) {
             const int64_t ly = y - gm.h;
-            const int64_t vec = ly / EPV;
-            const int r_own = static_cast<int>(vec / p.per);
-            const int lv = static_cast<int>(vec - static_cast<int64_t>(r_own) * p.per);
-            if (r_own == rank && lv % kRowThreads == tid) {
-                own_slot = lv / kRowThreads;
+            const int64_t lv = ly / EPV - v0;
+            if (lv >= 0 && lv < p.per && (static_cast<int>(lv) & (kRowThreads - 1)) == tid) {
+                own_slot = static_cast<int>(lv) / kRowThreads;
                 own_e = static_cast<int>(ly % EPV);
             }
         } else if (rank == K - 1 && tid == tail_tid) {
             own_sc = static_cast<int>(y - tail_col);
         }
-
         float x_y = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRowVpt; ++i)
+            if (i == own_slot) x_y = vec_elem<ES>(v[i], own_e);
+#pragma unroll
+        for (int s = 0; s < kMaxScalars; ++s)
+            if (s == own_sc) x_y = xs[s];
+
         if constexpr (GRAD) {
-            const float c = lse * kLog2e;
+            // (exp(x - lse) - onehot) * scale; for scale > 0 the scale is folded into the exponent
+            const bool mul = !(scale > 0.f);
+            const float c = mul ? lse * kLog2e : lse * kLog2e - log2f(scale);
+            const f32x2_t L2 = f2_pack(kLog2e, kLog2e), C2 = f2_pack(-c, -c), S2 = f2_pack(scale, scale);
             char* drow = p.dx + row * row_bytes;
             uint4* dv = reinterpret_cast<uint4*>(drow + static_cast<int64_t>(gm.h) * ES + v0 * 16);
+            if (!aborted) {
+                if (!mul) {
 #pragma unroll
-            for (int i = 0; i < kRowVpt; ++i) {
-                const int lv = tid + i * kRowThreads;
-                if (lv < nl) {
-                    float f[EPV], d[EPV];
-                    unpack<ES>(v[i], f);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) d[e] = ex2(fmaf(f[e], kLog2e, -c)) * scale;
-                    if (i == own_slot) {
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e)
-                            if (e == own_e) {
-                                x_y = f[e];
-                                d[e] -= scale;
-                            }
+                    for (int i = 0; i < kRowVpt; ++i) {
+                        const int lv = tid + i * kRowThreads;
+                        uint4 o = RowMath<ES>::template vexp<false>(v[i], L2, C2, S2);
+                        if (i == own_slot) o = vec_grad_label<ES>(v[i], own_e, c, false, scale);
+                        if (lv < nl) st_global_cs_v4(dv + lv, o);
                     }
-                    if (!aborted) st_global_cs_v4(dv + lv, pack<ES>(d));
-                }
-            }
+                } else {
 #pragma unroll
-            for (int s = 0; s < kMaxScalars; ++s) {
-                if (s < ns) {
-                    float d = ex2(fmaf(xs[s], kLog2e, -c)) * scale;
-                    if (s == own_sc) {
-                        x_y = xs[s];
-                        d -= scale;
+                    for (int i = 0; i < kRowVpt; ++i) {
+                        const int lv = tid + i * kRowThreads;
+                        uint4 o = RowMath<ES>::template vexp<true>(v[i], L2, C2, S2);
+                        if (i == own_slot) o = vec_grad_label<ES>(v[i], own_e, c, true, scale);
+                        if (lv < nl) st_global_cs_v4(dv + lv, o);
                     }
-                    if (!aborted) store_scalar<ES>(drow + (c0 + s) * ES, d);
                 }
-            }
-        } else {
-            if (own_slot >= 0) {
 #pragma unroll
-                for (int i = 0; i < kRowVpt; ++i) {
-                    if (i == own_slot) {
-                        float f[EPV];
-                        unpack<ES>(v[i], f);
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e)
-                            if (e == own_e) x_y = f[e];
+                for (int s = 0; s < kMaxScalars; ++s) {
+                    if (s < ns) {
+                        float d = ex2(fmaf(xs[s], kLog2e, -c));
+                        if (mul) d *= scale;
+                        if (s == own_sc) d -= scale;
+                        store_scalar<ES>(drow + (c0 + s) * ES, d);
                     }
                 }
             }
-#pragma unroll
-            for (int s = 0; s < kMaxScalars; ++s)
-                if (s == own_sc) x_y = xs[s];
         }
         if ((own_slot >= 0 || own_sc >= 0) && !aborted) p.row_loss[row] = lse - x_y;
         if (rank == 0 && tid == 0 && p.lse && !aborted) p.lse[row] = lse;
