@@ -20,6 +20,7 @@
 // N = 8192, an L2-resident read), and the mean loss is reduced in float64, in
 // row order, by whichever CTA finishes last.
 #include <algorithm>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -30,10 +31,9 @@
 
 namespace foak {
 
-constexpr int kRowThreads = 512;
-constexpr int kRowWarps = kRowThreads / 32;
-constexpr int kRowVpt = 8;                            // 16-byte vectors per thread per slice
-constexpr int kRowSliceVec = kRowThreads * kRowVpt;   // 4096 vectors = 64 KB per CTA
+// A CTA's slice of a row is at most 4096 16-byte vectors (64 KB), held in
+// registers as 8 vectors per thread (512 threads) or 4 (1024 threads).
+constexpr int kRowSliceVecMax = 4096;
 constexpr int kRowMaxStages = 4;
 constexpr int kRowMaxCluster = 8;
 constexpr int kMaxScalars = 7;                        // head or tail: < 16 bytes of bf16
@@ -118,7 +118,7 @@ __device__ __forceinline__ void store_scalar(char* p, float v) {
     else *reinterpret_cast<float*>(p) = v;
 }
 
-// Per-thread arithmetic on the thread's slice (kRowVpt 16-byte vectors).  Vectors
+// Per-thread arithmetic on the thread's slice (VPT 16-byte vectors).  Vectors
 // beyond the slice hold -inf, which no max picks and whose exp is 0, so the
 // loops run without predicates.
 template <int ES>
@@ -127,10 +127,11 @@ struct RowMath;
 template <>
 struct RowMath<2> {  // bf16: 8 elements per vector, handled as 4 packed pairs
     static __device__ __forceinline__ uint4 pad() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
-    static __device__ __forceinline__ float vmax(const uint4 (&v)[kRowVpt]) {
+    template <int VPT>
+    static __device__ __forceinline__ float vmax(const uint4 (&v)[VPT]) {
         uint32_t a = v[0].x, b = v[0].y, c = v[0].z, d = v[0].w;
 #pragma unroll
-        for (int i = 1; i < kRowVpt; ++i) {
+        for (int i = 1; i < VPT; ++i) {
             a = bf16x2_max(a, v[i].x);
             b = bf16x2_max(b, v[i].y);
             c = bf16x2_max(c, v[i].z);
@@ -140,11 +141,12 @@ struct RowMath<2> {  // bf16: 8 elements per vector, handled as 4 packed pairs
         return fmaxf(bf16_lo(m), bf16_hi(m));
     }
     // sum over the slice of 2^(x*log2e - mb)
-    static __device__ __forceinline__ float vsum(const uint4 (&v)[kRowVpt], float mb) {
+    template <int VPT>
+    static __device__ __forceinline__ float vsum(const uint4 (&v)[VPT], float mb) {
         const f32x2_t L = f2_pack(kLog2e, kLog2e), C = f2_pack(-mb, -mb);
         f32x2_t a = 0, b = 0, c = 0, d = 0;
 #pragma unroll
-        for (int i = 0; i < kRowVpt; ++i) {
+        for (int i = 0; i < VPT; ++i) {
             a = f2_add(a, f2_ex2(f2_fma(bf16x2_to_f2(v[i].x), L, C)));
             b = f2_add(b, f2_ex2(f2_fma(bf16x2_to_f2(v[i].y), L, C)));
             c = f2_add(c, f2_ex2(f2_fma(bf16x2_to_f2(v[i].z), L, C)));
@@ -179,11 +181,12 @@ struct RowMath<2> {  // bf16: 8 elements per vector, handled as 4 packed pairs
 template <>
 struct RowMath<4> {  // fp32: 4 elements per vector, 2 packed pairs
     static __device__ __forceinline__ uint4 pad() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
-    static __device__ __forceinline__ float vmax(const uint4 (&v)[kRowVpt]) {
+    template <int VPT>
+    static __device__ __forceinline__ float vmax(const uint4 (&v)[VPT]) {
         float a = __uint_as_float(v[0].x), b = __uint_as_float(v[0].y);
         float c = __uint_as_float(v[0].z), d = __uint_as_float(v[0].w);
 #pragma unroll
-        for (int i = 1; i < kRowVpt; ++i) {
+        for (int i = 1; i < VPT; ++i) {
             a = fmaxf(a, __uint_as_float(v[i].x));
             b = fmaxf(b, __uint_as_float(v[i].y));
             c = fmaxf(c, __uint_as_float(v[i].z));
@@ -191,11 +194,12 @@ struct RowMath<4> {  // fp32: 4 elements per vector, 2 packed pairs
         }
         return fmaxf(fmaxf(a, b), fmaxf(c, d));
     }
-    static __device__ __forceinline__ float vsum(const uint4 (&v)[kRowVpt], float mb) {
+    template <int VPT>
+    static __device__ __forceinline__ float vsum(const uint4 (&v)[VPT], float mb) {
         const f32x2_t L = f2_pack(kLog2e, kLog2e), C = f2_pack(-mb, -mb);
         f32x2_t a = 0, b = 0, c = 0, d = 0;
 #pragma unroll
-        for (int i = 0; i < kRowVpt; i += 2) {
+        for (int i = 0; i < VPT; i += 2) {
             a = f2_add(a, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i].x), __uint_as_float(v[i].y)), L, C)));
             b = f2_add(b, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i].z), __uint_as_float(v[i].w)), L, C)));
             c = f2_add(c, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i + 1].x), __uint_as_float(v[i + 1].y)), L, C)));
@@ -252,8 +256,11 @@ __device__ __forceinline__ uint4 vec_grad_label(const uint4& v, int e_own, float
     return pack<ES>(d);
 }
 
-template <int ES, bool GRAD>
-__global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowParams p) {
+template <int ES, bool GRAD, int THREADS>
+__global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p) {
+    constexpr int VPT = kRowSliceVecMax / THREADS;  // 64 KB slice: 512 x 8 or 1024 x 4 vectors
+    constexpr int kRowThreads = THREADS;
+    constexpr int kRowWarps = THREADS / 32;
     constexpr int EPV = 16 / ES;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t bars[kRowMaxStages];
@@ -324,7 +331,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
     __syncthreads();
     lab_cached = true;
 
-    uint32_t c_v = 0;
+    // Gradient constants: for scale > 0 the scale is folded into the exponent,
+    // 2^(x*log2e - lse2 + log2(scale)); otherwise the exponential is multiplied by it.
+    const bool mul = !(scale > 0.f);
+    const float log2_scale = mul ? 0.f : log2f(scale);
+
+    int c_st = 0;          // stage of the next valid row
+    uint32_t c_par = 0;    // its phase parity
+    uint32_t c_v = 0;      // valid rows consumed
     bool aborted = false;
     for (int64_t it = 0; it < n_it; ++it) {
         const int64_t row = cid + it * ncl;
@@ -340,6 +354,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
         const bool has_head = rank == 0 && tid == 0 && gm.h > 0;
         const bool has_tail = rank == K - 1 && tid == tail_tid && gm.t > 0;
         const int64_t tail_col = gm.h + gm.nb * EPV;
+        const int ns = has_head ? gm.h : (has_tail ? gm.t : 0);  // this thread's scalars
+        const int64_t c0 = has_head ? 0 : tail_col;
 
         if (!valid) {
             if constexpr (GRAD) {
@@ -347,10 +363,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
                 uint4* dv = reinterpret_cast<uint4*>(drow + static_cast<int64_t>(gm.h) * ES + v0 * 16);
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 for (int i = tid; i < nl; i += kRowThreads) st_global_cs_v4(dv + i, z);
-                if (has_head)
-                    for (int s = 0; s < gm.h; ++s) store_scalar<ES>(drow + s * ES, 0.f);
-                if (has_tail)
-                    for (int s = 0; s < gm.t; ++s) store_scalar<ES>(drow + (tail_col + s) * ES, 0.f);
+                for (int s = 0; s < ns; ++s) store_scalar<ES>(drow + (c0 + s) * ES, 0.f);
             }
             if (rank == 0 && tid == 0) {
                 p.row_loss[row] = 0.f;
@@ -359,33 +372,36 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
             continue;
         }
 
-        const int st = static_cast<int>(c_v % static_cast<uint32_t>(p.stages));
-        const uint32_t par = (c_v / static_cast<uint32_t>(p.stages)) & 1u;
+        const int st = c_st;
+        const uint32_t par = c_par;
+        if (++c_st == p.stages) {
+            c_st = 0;
+            c_par ^= 1u;
+        }
         ++c_v;
         if (!aborted && !mbar_wait_bounded(&bars[st], par)) s_abort = 1;
 
         // Slice -> registers (vectors past the slice hold -inf); scalars from global memory.
-        uint4 v[kRowVpt];
+        uint4 v[VPT];
         const uint4* sb = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(st) * p.stage_bytes);
         const uint4 pad = RowMath<ES>::pad();
 #pragma unroll
-        for (int i = 0; i < kRowVpt; ++i) {
+        for (int i = 0; i < VPT; ++i) {
             const int lv = tid + i * kRowThreads;
             v[i] = lv < nl ? sb[lv] : pad;
         }
         float xs[kMaxScalars];
-        int ns = 0;
-        int64_t c0 = 0;
-        if (has_head) { ns = gm.h; c0 = 0; }
-        if (has_tail) { ns = gm.t; c0 = tail_col; }
+        float m = RowMath<ES>::template vmax<VPT>(v);
+        if (ns > 0) {
 #pragma unroll
-        for (int s = 0; s < kMaxScalars; ++s) xs[s] = s < ns ? load_scalar<ES>(rowp + (c0 + s) * ES) : kNegInf;
+            for (int s = 0; s < kMaxScalars; ++s) {
+                xs[s] = s < ns ? load_scalar<ES>(rowp + (c0 + s) * ES) : kNegInf;
+                m = fmaxf(m, xs[s]);
+            }
+        }
 
         // Row max: thread -> warp -> CTA.  The barrier that publishes the warp
         // maxima also frees the stage for the producer.
-        float m = RowMath<ES>::vmax(v);
-#pragma unroll
-        for (int s = 0; s < kMaxScalars; ++s) m = fmaxf(m, xs[s]);
         m = warp_max(m);
         if (lane == 0) red_m[warp] = m;
         __syncthreads();
@@ -398,10 +414,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
 
         // Sum of exp(x - M) relative to the CTA max, so no rescaling is needed in the CTA.
         const float mb = M == kNegInf ? 0.f : M * kLog2e;
-        float sum = RowMath<ES>::vsum(v, mb);
+        float sum = RowMath<ES>::template vsum<VPT>(v, mb);
+        if (ns > 0) {
 #pragma unroll
-        for (int s = 0; s < kMaxScalars; ++s)
-            if (s < ns) sum += ex2(fmaf(xs[s], kLog2e, -mb));
+            for (int s = 0; s < kMaxScalars; ++s)
+                if (s < ns) sum += ex2(fmaf(xs[s], kLog2e, -mb));
+        }
         sum = warp_sum(sum);
         if (lane == 0) red_s[warp] = sum;
         __syncthreads();
@@ -419,7 +437,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
             M = __shfl_sync(0xffffffffu, M, 0);
             S = __shfl_sync(0xffffffffu, S, 0);
         }
-        const float lse = M + logf(S);
+        const float lse2 = fmaf(M, kLog2e, lg2(S));  // log-sum-exp in base 2
+        const float lse = lse2 * kLn2;
 
         // Which thread holds the label column (no division: kRowThreads is a power of 2).
         int own_slot = -1, own_e = 0, own_sc = -1;
@@ -435,25 +454,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
         } else if (rank == K - 1 && tid == tail_tid) {
             own_sc = static_cast<int>(y - tail_col);
         }
-        float x_y = 0.f;
+        const bool owner = own_slot >= 0 || own_sc >= 0;
+        if (owner) {
+            float x_y = 0.f;
 #pragma unroll
-        for (int i = 0; i < kRowVpt; ++i)
-            if (i == own_slot) x_y = vec_elem<ES>(v[i], own_e);
+            for (int i = 0; i < VPT; ++i)
+                if (i == own_slot) x_y = vec_elem<ES>(v[i], own_e);
 #pragma unroll
-        for (int s = 0; s < kMaxScalars; ++s)
-            if (s == own_sc) x_y = xs[s];
+            for (int s = 0; s < kMaxScalars; ++s)
+                if (s == own_sc) x_y = xs[s];
+            if (!aborted) p.row_loss[row] = lse - x_y;
+        }
 
         if constexpr (GRAD) {
-            // (exp(x - lse) - onehot) * scale; for scale > 0 the scale is folded into the exponent
-            const bool mul = !(scale > 0.f);
-            const float c = mul ? lse * kLog2e : lse * kLog2e - log2f(scale);
+            const float c = lse2 - log2_scale;
             const f32x2_t L2 = f2_pack(kLog2e, kLog2e), C2 = f2_pack(-c, -c), S2 = f2_pack(scale, scale);
             char* drow = p.dx + row * row_bytes;
             uint4* dv = reinterpret_cast<uint4*>(drow + static_cast<int64_t>(gm.h) * ES + v0 * 16);
             if (!aborted) {
                 if (!mul) {
 #pragma unroll
-                    for (int i = 0; i < kRowVpt; ++i) {
+                    for (int i = 0; i < VPT; ++i) {
                         const int lv = tid + i * kRowThreads;
                         uint4 o = RowMath<ES>::template vexp<false>(v[i], L2, C2, S2);
                         if (i == own_slot) o = vec_grad_label<ES>(v[i], own_e, c, false, scale);
@@ -461,25 +482,26 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < kRowVpt; ++i) {
+                    for (int i = 0; i < VPT; ++i) {
                         const int lv = tid + i * kRowThreads;
                         uint4 o = RowMath<ES>::template vexp<true>(v[i], L2, C2, S2);
                         if (i == own_slot) o = vec_grad_label<ES>(v[i], own_e, c, true, scale);
                         if (lv < nl) st_global_cs_v4(dv + lv, o);
                     }
                 }
+                if (ns > 0) {
 #pragma unroll
-                for (int s = 0; s < kMaxScalars; ++s) {
-                    if (s < ns) {
-                        float d = ex2(fmaf(xs[s], kLog2e, -c));
-                        if (mul) d *= scale;
-                        if (s == own_sc) d -= scale;
-                        store_scalar<ES>(drow + (c0 + s) * ES, d);
+                    for (int s = 0; s < kMaxScalars; ++s) {
+                        if (s < ns) {
+                            float d = ex2(fmaf(xs[s], kLog2e, -c));
+                            if (mul) d *= scale;
+                            if (s == own_sc) d -= scale;
+                            store_scalar<ES>(drow + (c0 + s) * ES, d);
+                        }
                     }
                 }
             }
         }
-        if ((own_slot >= 0 || own_sc >= 0) && !aborted) p.row_loss[row] = lse - x_y;
         if (rank == 0 && tid == 0 && p.lse && !aborted) p.lse[row] = lse;
     }
 
@@ -527,22 +549,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) ce_rows_kernel(const CeRowPara
 // ------------------------------------------------------------------ host side
 
 int64_t ce_rows_max_vocab(int elem_bytes) {
-    return static_cast<int64_t>(kRowMaxCluster) * kRowSliceVec * (16 / elem_bytes);
+    return static_cast<int64_t>(kRowMaxCluster) * kRowSliceVecMax * (16 / elem_bytes);
 }
 
 namespace {
 
 struct Plan {
-    int k, per, stages;
+    int threads, k, per, stages;
     uint32_t stage_bytes;
     size_t smem;
 };
 
 bool plan_rows(int ES, int64_t V, Plan* pl) {
+    static const int threads = [] {
+        const char* e = std::getenv("FOAK_ROW_THREADS");  // tuning override: 512 (default) or 1024
+        return (e && std::atoi(e) == 1024) ? 1024 : 512;
+    }();
     const int64_t nb_max = V * ES / 16;
     for (int k = 1; k <= kRowMaxCluster; k *= 2) {
         const int64_t per = (nb_max + k - 1) / k;
-        if (per <= kRowSliceVec) {
+        if (per <= kRowSliceVecMax) {
+            pl->threads = threads;
             pl->k = k;
             pl->per = static_cast<int>(std::max<int64_t>(per, 1));
             pl->stage_bytes = static_cast<uint32_t>(((pl->per * 16 + 127) / 128) * 128);
@@ -561,7 +588,7 @@ std::map<std::pair<int, const void*>, bool> g_attr_set;                // (devic
 // Co-resident clusters for this kernel configuration (cached per device).  The
 // kernel's dynamic shared-memory limit is raised once per device to the full
 // budget, so every plan's size fits whatever order plans are launched in.
-cudaError_t resident_clusters(const void* kern, int k, size_t smem, int* out) {
+cudaError_t resident_clusters(const void* kern, int threads, int k, size_t smem, int* out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -581,13 +608,13 @@ cudaError_t resident_clusters(const void* kern, int k, size_t smem, int* out) {
     int n = 0;
     if (k == 1) {
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
         if (e != cudaSuccess) return e;
         n = per_sm * device_sm_count();
     } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(k), 1, 1);
-        cfg.blockDim = dim3(kRowThreads, 1, 1);
+        cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -605,11 +632,11 @@ cudaError_t resident_clusters(const void* kern, int k, size_t smem, int* out) {
     return cudaSuccess;
 }
 
-template <int ES, bool GRAD>
+template <int ES, bool GRAD, int THREADS>
 cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t stream) {
-    const void* kern = reinterpret_cast<const void*>(&ce_rows_kernel<ES, GRAD>);
+    const void* kern = reinterpret_cast<const void*>(&ce_rows_kernel<ES, GRAD, THREADS>);
     int ncl = 0;
-    cudaError_t e = resident_clusters(kern, pl.k, pl.smem, &ncl);
+    cudaError_t e = resident_clusters(kern, THREADS, pl.k, pl.smem, &ncl);
     if (e != cudaSuccess) return e;
     const int64_t want = std::max<int64_t>(1, std::min<int64_t>(ncl, base.N));
     CeRowParams prm = base;
@@ -619,7 +646,7 @@ cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t s
     prm.stage_bytes = pl.stage_bytes;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(want * pl.k), 1, 1);
-    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
@@ -629,7 +656,13 @@ cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t s
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ce_rows_kernel<ES, GRAD>, prm);
+    return cudaLaunchKernelEx(&cfg, ce_rows_kernel<ES, GRAD, THREADS>, prm);
+}
+
+template <int ES, bool GRAD>
+cudaError_t launch_vpt(const CeRowParams& base, const Plan& pl, cudaStream_t stream) {
+    return pl.threads == 1024 ? launch_typed<ES, GRAD, 1024>(base, pl, stream)
+                              : launch_typed<ES, GRAD, 512>(base, pl, stream);
 }
 
 }  // namespace
@@ -657,8 +690,8 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
     prm.err = err;
     prm.ws = ws;
     if (elem_bytes == 2)
-        return grad ? launch_typed<2, true>(prm, pl, stream) : launch_typed<2, false>(prm, pl, stream);
-    return grad ? launch_typed<4, true>(prm, pl, stream) : launch_typed<4, false>(prm, pl, stream);
+        return grad ? launch_vpt<2, true>(prm, pl, stream) : launch_vpt<2, false>(prm, pl, stream);
+    return grad ? launch_vpt<4, true>(prm, pl, stream) : launch_vpt<4, false>(prm, pl, stream);
 }
 
 }  // namespace foak

@@ -131,6 +131,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// log2(x) on the special-function unit (PTX lg2.approx.ftz.f32).
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void st_global_cs_v4(void* p, uint4 v) {
     asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
