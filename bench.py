@@ -288,9 +288,9 @@ def run_ours(args, rank, world, dist):
     def max_over_ranks(v):
         if dist is None:
             return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        from cross_entropy_loss_gb300 import dp
+
+        return dp.max_over_ranks(v, device=dev)
 
     main = _make(args.workload)
     if sampler:
