@@ -47,6 +47,7 @@ SIGNATURES = {
                                _vp]),
     "foak_ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
                                        _vp]),
+    "foak_gemm_bf16": (_i32, [_vp, _i64, _i32, _vp, _i64, _i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _vp]),
     "foak_test_fail_next_launches": (None, [_i32]),
 }
 
@@ -234,3 +235,27 @@ def foak_ce_fwd_bwd_noalloc(logits, labels, *, g: float = 1.0, ignore_index: int
                                      _stream(dev, stream))
     _check(st, "foak_ce_fwd_bwd_noalloc")
     return dict(loss=loss, n_valid=n_valid, err=err, lse=lse)
+
+
+FOAK_GEMM_BF16, FOAK_GEMM_F32, FOAK_GEMM_F32_ACC = 0, 1, 2
+
+
+def foak_gemm_bf16(a, b, out, *, a_mn_major: bool = False, b_mn_major: bool = False, mode: int = FOAK_GEMM_BF16,
+                   M: int | None = None, N: int | None = None, K: int | None = None, err=None, stream=None):
+    """out (+)= A @ B^T on the tensor cores.  a, b: 2-D bf16 tensors with unit column stride.
+
+    a is [M][K] (or [K][M] with a_mn_major), b is [N][K] (or [K][N] with b_mn_major);
+    out is [M][N] with unit column stride, bf16 for FOAK_GEMM_BF16 else fp32.
+    """
+    for t in (a, b, out):
+        if t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda:
+            raise ValueError("operands must be 2-D CUDA tensors with unit column stride")
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise TypeError("a and b must be bfloat16")
+    M = (a.shape[1] if a_mn_major else a.shape[0]) if M is None else M
+    K = (a.shape[0] if a_mn_major else a.shape[1]) if K is None else K
+    N = (b.shape[1] if b_mn_major else b.shape[0]) if N is None else N
+    st = lib.foak_gemm_bf16(_ptr(a), a.stride(0), int(a_mn_major), _ptr(b), b.stride(0), int(b_mn_major), M, N, K,
+                            _ptr(out), out.stride(0), int(mode), _ptr(err), _stream(out.device, stream))
+    _check(st, "foak_gemm_bf16")
+    return out

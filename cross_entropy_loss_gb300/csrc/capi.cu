@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "foak_ce.h"
+#include "gemm_tc.h"
 #include "internal.h"
 
 namespace foak {
@@ -171,6 +172,44 @@ foak_status foak_ce_backward(void* dlogits, const void* logits, int32_t dtype, i
     cudaError_t e = launch_ce_backward(es, dlogits, logits, ld, labels, N, V, ignore_index, lse, grad_out, denom,
                                        err, s);
     return finish(e, err, s);
+}
+
+foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const void* b, int64_t ldb,
+                           int32_t b_mn_major, int64_t M, int64_t N, int64_t K, void* out, int64_t ldo,
+                           int32_t out_mode, int32_t* err, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL)
+        return FOAK_ERR_INVALID_ARG;
+    if (out_mode != FOAK_GEMM_BF16 && out_mode != FOAK_GEMM_F32 && out_mode != FOAK_GEMM_F32_ACC)
+        return FOAK_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FOAK_OK;
+    const int oes = out_mode == FOAK_GEMM_BF16 ? 2 : 4;
+    if (!a || !b || !out || !aligned(a, 16) || !aligned(b, 16) || !aligned(out, 16)) return FOAK_ERR_INVALID_ARG;
+    if ((lda * 2) % 16 || (ldb * 2) % 16 || (ldo * oes) % 16 || ldo < N) return FOAK_ERR_INVALID_ARG;
+    if (lda < (a_mn_major ? M : K) || ldb < (b_mn_major ? N : K)) return FOAK_ERR_INVALID_ARG;
+    if (err && !aligned(err, 4)) return FOAK_ERR_INVALID_ARG;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {  // empty contraction: C = 0 (or unchanged when accumulating)
+        if (out_mode == FOAK_GEMM_F32_ACC) return FOAK_OK;
+        cudaError_t e = cudaMemset2DAsync(out, static_cast<size_t>(ldo) * oes, 0, static_cast<size_t>(N) * oes,
+                                          static_cast<size_t>(M), s);
+        return finish(e, nullptr, s);
+    }
+    GemmDesc d = {};
+    d.a = a;
+    d.lda = lda;
+    d.a_mn_major = a_mn_major != 0;
+    d.b = b;
+    d.ldb = ldb;
+    d.b_mn_major = b_mn_major != 0;
+    d.M = static_cast<int>(M);
+    d.N = static_cast<int>(N);
+    d.K = static_cast<int>(K);
+    d.out = out;
+    d.ldo = ldo;
+    d.mode = static_cast<GemmOut>(out_mode);
+    d.err = err;
+    return finish(launch_gemm_bf16(d, s), err, s);
 }
 
 void foak_test_fail_next_launches(int32_t count) { g_fail_launches.store(count < 0 ? 0 : count); }

@@ -1,0 +1,314 @@
+// Persistent bf16 GEMM on the fifth-generation tensor cores (tcgen05) for the
+// chunked linear + cross-entropy:  C (+)= A * B^T  with fp32 accumulation.
+//
+// One CTA per SM walks output tiles of 128 x 256 (M fastest, so neighbouring CTAs
+// share the B tile in L2).  Warp roles:
+//   warp 0     TMA producer: 2-D tiled loads (128-byte swizzle) of the A and B
+//              k-blocks (64 deep) into a 4-stage shared-memory ring;
+//   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
+//              one thread issues tcgen05.mma (M=128, N=256, K=16) per 16-deep
+//              slice, committing each stage back to the producer and each
+//              finished accumulator to the epilogue;
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter of the accumulator,
+//              then bf16 store, fp32 store or fp32 read-modify-write.
+// The accumulators are double-buffered, so a tile's epilogue overlaps the next
+// tile's main loop.  Either operand may be K-major (row-major [rows][K]) or
+// MN-major (row-major [K][rows]); the shared-memory descriptors and the
+// instruction descriptor's major bits say which.  All waits are bounded.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "foak_ce.h"
+#include "gemm_tc.h"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace foak {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr uint32_t kABytes = kBM * kBK * 2;            // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;            // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;    // 48 KB
+constexpr uint32_t kMNBlock = 64 * kBK * 2;            // one 64 (MN) x 64 (K) box: 8 KB
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr size_t kGemmSmem = kStages * kStageBytes + 1024;  // + alignment slack
+
+struct GemmParams {
+    CUtensorMap tmA;
+    CUtensorMap tmB;
+    int M, N, K;
+    int a_mn, b_mn;
+    int mode;
+    int tiles_m, tiles_n;
+    uint32_t idesc;
+    void* out;
+    int64_t ldo;
+    int32_t* err;
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        fence_mbar_init();
+        abort_sh = 0;
+        prefetch_tensormap(&p.tmA);
+        prefetch_tensormap(&p.tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_sh;
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    const int nk = (p.K + kBK - 1) / kBK;
+
+    auto give_up = [&]() {
+        abort_sh = 1;
+        if (p.err) atomicOr(p.err, FOAK_ERRBIT_TIMEOUT);
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < num_tiles && !abort_sh; t += gridDim.x) {
+                const int m0 = (t % p.tiles_m) * kBM, n0 = (t / p.tiles_m) * kBN;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) { give_up(); break; }
+                    if (abort_sh) break;
+                    unsigned char* sA = smem + static_cast<size_t>(stage) * kStageBytes;
+                    unsigned char* sB = sA + kABytes;
+                    mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                    const int k0 = kb * kBK;
+                    if (!p.a_mn) {
+                        tma_load_2d(sA, &p.tmA, k0, m0, &full[stage]);
+                    } else {
+                        tma_load_2d(sA, &p.tmA, m0, k0, &full[stage]);
+                        tma_load_2d(sA + kMNBlock, &p.tmA, m0 + 64, k0, &full[stage]);
+                    }
+                    if (!p.b_mn) {
+                        tma_load_2d(sB, &p.tmB, k0, n0, &full[stage]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sB + j * kMNBlock, &p.tmB, n0 + 64 * j, k0, &full[stage]);
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            for (int t = blockIdx.x; t < num_tiles && !abort_sh; t += gridDim.x) {
+                if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u)) { give_up(); break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tbase + static_cast<uint32_t>(acc * kBN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase)) { give_up(); break; }
+                    tc_fence_after();
+                    const uint32_t sA = smem_u32(smem + static_cast<size_t>(stage) * kStageBytes);
+                    const uint32_t sB = sA + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // K-major: advance 32 bytes inside the 128-byte swizzle row;
+                        // MN-major: advance 16 K-rows of 128 bytes.
+                        const uint64_t ad = p.a_mn ? smem_desc_sw128(sA + kk * 2048, kMNBlock, 1024)
+                                                   : smem_desc_sw128(sA + kk * 32, 16, 1024);
+                        const uint64_t bd = p.b_mn ? smem_desc_sw128(sB + kk * 2048, kMNBlock, 1024)
+                                                   : smem_desc_sw128(sB + kk * 32, 16, 1024);
+                        tc_mma_bf16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit(&acc_full[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+    } else {
+        // epilogue warps 2..5: TMEM lane quarter = warp % 4
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            const bool ok = !abort_sh && mbar_wait_bounded(&acc_full[acc], acc_phase);
+            if (!ok) {
+                if (lane == 0) give_up();
+                break;
+            }
+            tc_fence_after();
+            const int m0 = (t % p.tiles_m) * kBM, n0 = (t / p.tiles_m) * kBN;
+            const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t r[32];
+                tc_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN + c * 32), r);
+                tc_wait_ld();
+                const int col0 = n0 + c * 32;
+                if (row >= p.M || col0 >= p.N) continue;
+                const bool full_chunk = col0 + 32 <= p.N;
+                if (p.mode == kGemmOutBf16) {
+                    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo + col0;
+                    if (full_chunk) {
+                        uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                            o4[v] = w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N) o[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                    }
+                } else {
+                    float* o = static_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ldo + col0;
+                    const bool accum = p.mode == kGemmOutF32Acc;
+                    if (full_chunk) {
+                        float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float4 w = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                            if (accum) {
+                                const float4 prev = o4[v];
+                                w.x += prev.x;
+                                w.y += prev.y;
+                                w.z += prev.z;
+                                w.w += prev.w;
+                            }
+                            o4[v] = w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N) o[j] = accum ? o[j] + __uint_as_float(r[j]) : __uint_as_float(r[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// Row-major bf16 [outer][inner] with row stride ld (elements), boxes of 64 inner x
+// box_outer, 128-byte swizzle (the layout the descriptors above expect).
+bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, int64_t ld, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+std::mutex g_gemm_mu;
+bool g_gemm_attr[64] = {false};
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
+    if (d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaSuccess;
+    GemmParams p = {};
+    // K-major [rows][K]: inner K, boxes of 64 x rows-tile; MN-major [K][rows]: inner rows, 64 x 64 boxes.
+    bool ok = d.a_mn_major ? encode_bf16(&p.tmA, d.a, static_cast<uint64_t>(d.M), static_cast<uint64_t>(d.K), d.lda, 64)
+                           : encode_bf16(&p.tmA, d.a, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.M), d.lda, kBM);
+    ok = ok && (d.b_mn_major
+                    ? encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.K), d.ldb, 64)
+                    : encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N), d.ldb, kBN));
+    if (!ok) return cudaErrorInvalidValue;
+    p.M = d.M;
+    p.N = d.N;
+    p.K = d.K;
+    p.a_mn = d.a_mn_major ? 1 : 0;
+    p.b_mn = d.b_mn_major ? 1 : 0;
+    p.mode = d.mode;
+    p.tiles_m = (d.M + kBM - 1) / kBM;
+    p.tiles_n = (d.N + kBN - 1) / kBN;
+    p.idesc = idesc_bf16_f32(kBM, kBN, p.a_mn, p.b_mn);
+    p.out = d.out;
+    p.ldo = d.ldo;
+    p.err = d.err;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_gemm_mu);
+        if (!g_gemm_attr[dev]) {
+            e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kGemmSmem));
+            if (e != cudaSuccess) return e;
+            g_gemm_attr[dev] = true;
+        }
+    }
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int grid = std::min(tiles, device_sm_count());
+    gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace foak

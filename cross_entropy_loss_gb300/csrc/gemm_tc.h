@@ -1,0 +1,35 @@
+// Host interface of the tcgen05 GEMM used by the chunked linear + cross-entropy.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace foak {
+
+enum GemmOut : int {
+    kGemmOutBf16 = 0,    // C = A * B^T, stored as bf16
+    kGemmOutF32 = 1,     // C = A * B^T, stored as fp32
+    kGemmOutF32Acc = 2,  // C += A * B^T in fp32 (read-modify-write)
+};
+
+// C[M x N] (+)= A[M x K] * B[N x K]^T, bf16 operands, fp32 accumulation.
+// An operand is K-major when stored row-major as [rows][K] (row stride ld) and
+// MN-major when stored row-major as [K][rows] (row stride ld).  Pointers and row
+// strides must be 16-byte aligned; C is row-major with row stride ldo.
+struct GemmDesc {
+    const void* a;
+    int64_t lda;
+    bool a_mn_major;
+    const void* b;
+    int64_t ldb;
+    bool b_mn_major;
+    int M, N, K;
+    void* out;
+    int64_t ldo;
+    GemmOut mode;
+    int32_t* err;  // device error word for wait timeouts (may be null)
+};
+
+cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream);
+
+}  // namespace foak

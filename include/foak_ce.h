@@ -143,6 +143,27 @@ foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Building block of the chunked linear + CE: C[M x N] (+)= A[M x K] * B[N x K]^T on
+ * the tcgen05 tensor cores, bf16 operands, fp32 accumulation (exposed so the
+ * three products of the chunked call can be tested and timed alone).
+ *   a, b (device)     bf16.  With *_mn_major = 0 the operand is stored row-major
+ *                     as [rows][K] (K contiguous, row stride lda/ldb elements);
+ *                     with 1 as [K][rows] (rows contiguous).  16-byte aligned
+ *                     pointers and row strides; row strides >= the contiguous extent.
+ *   out (device)      row-major [M][ldo]: bf16 for out_mode FOAK_GEMM_BF16, fp32 for
+ *                     FOAK_GEMM_F32 (overwrite) and FOAK_GEMM_F32_ACC (add into it);
+ *                     16-byte aligned pointer and row stride.
+ *   err (device)      int32[1] or NULL: FOAK_ERRBIT_TIMEOUT is OR-ed in if a
+ *                     device wait gave up (never set on a healthy GPU).
+ */
+#define FOAK_GEMM_BF16 0
+#define FOAK_GEMM_F32 1
+#define FOAK_GEMM_F32_ACC 2
+foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const void* b, int64_t ldb,
+                           int32_t b_mn_major, int64_t M, int64_t N, int64_t K, void* out, int64_t ldo,
+                           int32_t out_mode, int32_t* err, void* stream);
+
+/*
  * Largest N that foak_ce_fwd_bwd_noalloc accepts (its fixed scratch holds one
  * float per row: 1 MiB plus a 256-byte header on every device that loads the
  * library, kept until the process exits).
