@@ -48,6 +48,9 @@ SIGNATURES = {
     "foak_ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
                                        _vp]),
     "foak_gemm_bf16": (_i32, [_vp, _i64, _i32, _vp, _i64, _i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _vp]),
+    "foak_linear_ce_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "foak_linear_ce_chunked": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
+                                      _vp, _vp, _sz, _vp]),
     "foak_test_fail_next_launches": (None, [_i32]),
 }
 
@@ -259,3 +262,45 @@ def foak_gemm_bf16(a, b, out, *, a_mn_major: bool = False, b_mn_major: bool = Fa
                             _ptr(out), out.stride(0), int(mode), _ptr(err), _stream(out.device, stream))
     _check(st, "foak_gemm_bf16")
     return out
+
+
+def foak_linear_ce_workspace_size(N: int, V: int, D: int, chunk: int) -> int:
+    return int(lib.foak_linear_ce_workspace_size(int(N), int(V), int(D), int(chunk)))
+
+
+_lin_ws: dict = {}
+
+
+def foak_linear_ce_chunked(H, W, labels, *, chunk: int = 1024, g: float = 1.0, ignore_index: int = -100,
+                           denom: float = 0.0, dH=None, dW=None, workspace_tensor=None, stream=None):
+    """Loss, dH and dW of CE(H W^T) in chunks of rows on the tensor cores.
+
+    H: bf16 [N][D], W: bf16 [V][D] (contiguous).  Returns dict(loss, dH, dW, n_valid, err);
+    dH is bf16 [N][D], dW fp32 [V][D].
+    """
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or not H.is_contiguous() or not W.is_contiguous():
+        raise ValueError("H and W must be contiguous bfloat16 tensors")
+    N, D = H.shape
+    V, D2 = W.shape
+    if D2 != D:
+        raise ValueError("H and W disagree on the hidden size")
+    dev = H.device
+    labels = _labels_arg(labels, N, dev)
+    dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev) if dH is None else dH
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev) if dW is None else dW
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int32, device=dev)
+    err = torch.empty(1, dtype=torch.int32, device=dev)
+    need = foak_linear_ce_workspace_size(N, V, D, chunk)
+    ws = workspace_tensor
+    if ws is None:
+        with _ws_lock:
+            ws = _lin_ws.get(dev)
+            if ws is None or ws.numel() < need:
+                ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+                _lin_ws[dev] = ws
+    st = lib.foak_linear_ce_chunked(_ptr(H), _ptr(W), _ptr(labels), N, V, D, int(ignore_index), int(chunk), float(g),
+                                    float(denom), _ptr(loss), _ptr(dH), _ptr(dW), _ptr(n_valid), _ptr(err), _ptr(ws),
+                                    ws.numel(), _stream(dev, stream))
+    _check(st, "foak_linear_ce_chunked")
+    return dict(loss=loss, dH=dH, dW=dW, n_valid=n_valid, err=err)

@@ -174,6 +174,33 @@ foak_status foak_ce_backward(void* dlogits, const void* logits, int32_t dtype, i
     return finish(e, err, s);
 }
 
+size_t foak_linear_ce_workspace_size(int64_t N, int64_t V, int64_t D, int64_t chunk) {
+    (void)D;
+    if (N < 0 || V < 1 || chunk < 1) return 0;
+    return linear_ce_workspace_bytes(N, V, chunk);
+}
+
+foak_status foak_linear_ce_chunked(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t V,
+                                   int64_t D, int64_t ignore_index, int64_t chunk, float g, float denom,
+                                   float* loss, void* dH, float* dW, int32_t* n_valid, int32_t* err,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (N < 0 || V < 1 || D < 1 || chunk < 1) return FOAK_ERR_INVALID_ARG;
+    if (N > 0x7fffffffLL || V > 0x7fffffffLL || D > 0x7fffffffLL) return FOAK_ERR_UNSUPPORTED;
+    if (V > ce_rows_max_vocab(2)) return FOAK_ERR_UNSUPPORTED;
+    if (D % 8) return FOAK_ERR_UNSUPPORTED;  // 16-byte rows for the tensor maps
+    if (!W || !dW || !loss || !aligned(W, 16) || !aligned(dW, 16) || !aligned(loss, 4)) return FOAK_ERR_INVALID_ARG;
+    if (N > 0 && (!H || !labels || !dH || !aligned(H, 16) || !aligned(dH, 16) || !aligned(labels, 8)))
+        return FOAK_ERR_INVALID_ARG;
+    if ((n_valid && !aligned(n_valid, 4)) || (err && !aligned(err, 4))) return FOAK_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, kCeWsAlign) || workspace_bytes < linear_ce_workspace_bytes(N, V, chunk))
+        return FOAK_ERR_WORKSPACE;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(launch_linear_ce(H, W, labels, N, V, D, ignore_index, chunk, g, denom, loss, dH, dW, n_valid, err,
+                                   workspace, s),
+                  err, s);
+}
+
 foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const void* b, int64_t ldb,
                            int32_t b_mn_major, int64_t M, int64_t N, int64_t K, void* out, int64_t ldo,
                            int32_t out_mode, int32_t* err, void* stream) {

@@ -54,6 +54,8 @@ struct CeRowParams {
     int32_t* n_valid;
     int32_t* err;
     CeWsHeader* ws;
+    const int64_t* count_labels;  // labels whose valid count is the denominator (the batch's)
+    int64_t count_N;
     int k;               // CTAs per row (cluster size)
     int per;             // vectors per CTA slice
     int stages;          // rows in flight per CTA
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p
         for (int s = 0; s < p.stages; ++s) issue_next();
 
     int n_valid = 0, n_bad = 0;
-    count_labels(p.labels, p.N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
+    count_labels(p.count_labels, p.count_N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
     const float D = p.denom > 0.f ? p.denom : static_cast<float>(n_valid);
     const float scale = p.g / D;
     // Labels of this CTA's first rows, for the row loop and the producer.
@@ -670,7 +672,8 @@ cudaError_t launch_vpt(const CeRowParams& base, const Plan& pl, cudaStream_t str
 cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, int64_t ld,
                            const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, float g,
                            float denom, float* loss, float* lse, float* row_loss, int32_t* n_valid,
-                           int32_t* err, CeWsHeader* ws, cudaStream_t stream) {
+                           int32_t* err, CeWsHeader* ws, cudaStream_t stream, const int64_t* count_labels,
+                           int64_t count_N) {
     Plan pl;
     if (!plan_rows(elem_bytes, V, &pl)) return cudaErrorInvalidValue;
     CeRowParams prm = {};
@@ -689,6 +692,8 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
     prm.n_valid = n_valid;
     prm.err = err;
     prm.ws = ws;
+    prm.count_labels = count_labels ? count_labels : labels;
+    prm.count_N = count_labels ? count_N : N;
     if (elem_bytes == 2)
         return grad ? launch_vpt<2, true>(prm, pl, stream) : launch_vpt<2, false>(prm, pl, stream);
     return grad ? launch_vpt<4, true>(prm, pl, stream) : launch_vpt<4, false>(prm, pl, stream);

@@ -27,16 +27,28 @@ inline size_t ce_workspace_bytes(int64_t N) {
 int64_t ce_rows_max_vocab(int elem_bytes);
 
 // Forward (grad == false) or fused forward+backward in place (grad == true).
-// row_loss must be non-null (caller buffer or the workspace's row area).
+// row_loss must be non-null (caller buffer or the workspace's row area).  The
+// denominator (when denom <= 0) and the error word's label check use
+// count_labels[0, count_N) -- by default the rows' own labels; the chunked
+// linear + CE passes the whole batch's labels so every chunk divides by the
+// batch's n_valid.  The loss and n_valid outputs then describe this call's rows
+// over that denominator.
 cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, int64_t ld,
                            const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, float g,
                            float denom, float* loss, float* lse, float* row_loss, int32_t* n_valid,
-                           int32_t* err, CeWsHeader* ws, cudaStream_t stream);
+                           int32_t* err, CeWsHeader* ws, cudaStream_t stream,
+                           const int64_t* count_labels = nullptr, int64_t count_N = 0);
 
 cudaError_t launch_ce_backward(int elem_bytes, void* dx, const void* x, int64_t ld,
                                const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index,
                                const float* lse, const float* g_ptr, float denom, int32_t* err,
                                cudaStream_t stream);
+
+// Chunked linear + CE (linear_ce.cu): workspace bytes and the launch sequence.
+size_t linear_ce_workspace_bytes(int64_t N, int64_t V, int64_t chunk);
+cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t V, int64_t D,
+                             int64_t ignore_index, int64_t chunk, float g, float denom, float* loss, void* dH,
+                             float* dW, int32_t* n_valid, int32_t* err, void* workspace, cudaStream_t stream);
 
 // Streaming multiprocessor count of the current device (cached per device).
 int device_sm_count();

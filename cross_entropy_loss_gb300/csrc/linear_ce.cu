@@ -1,0 +1,175 @@
+// Chunked linear + cross-entropy: loss, dH and dW of CE(H W^T) without the full
+// N x V logits -- the fused-linear / "chunked loss" form the FOAK pages name
+// (LigerFusedLinearCrossEntropy, "Running Liger Kernel Benchmarks" on the
+// fms-acceleration-foak 0.7.4 page; "add chunked loss" in the TODO of
+// fms-acceleration PR #79).
+//
+// For each chunk of rows [r0, r0 + C):
+//   1. Z  = H_c W^T            tcgen05 GEMM, bf16 out (C x V scratch)
+//   2. dZ = CE fwd+bwd on Z    the fused row kernel, in place, dividing by the
+//                              batch's n_valid (counted over all N labels), so
+//                              the result does not depend on the chunk size
+//   3. dH_c = dZ W             tcgen05 GEMM, bf16 out into dH
+//   4. dW (+)= dZ^T H_c        tcgen05 GEMM, fp32 out (stored by the first
+//                              chunk, accumulated by the others)
+// and finally one CTA sums the per-row loss terms of all N rows in float64, in
+// row order, over the denominator.  Only one chunk's Z lives at a time.
+#include <algorithm>
+
+#include "common.cuh"
+#include "foak_ce.h"
+#include "gemm_tc.h"
+#include "internal.h"
+
+namespace foak {
+
+namespace {
+
+constexpr int kFinThreads = 512;
+
+inline size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+struct LinWs {
+    CeWsHeader* hdr;
+    float* row_loss;   // N
+    int32_t* chunk_err;  // one word per chunk's CE call, then one word for the GEMMs
+    float* chunk_loss;   // scratch loss output of the chunk CE calls
+    void* z;           // chunk x ldz bf16
+    size_t bytes;
+};
+
+LinWs lin_layout(void* base, int64_t N, int64_t V, int64_t chunk) {
+    const int64_t nchunks = N > 0 ? (N + chunk - 1) / chunk : 0;
+    const int64_t ldz = (V + 63) / 64 * 64;
+    LinWs w = {};
+    size_t off = 0;
+    char* b = static_cast<char*>(base);
+    w.hdr = reinterpret_cast<CeWsHeader*>(b + off);
+    off += sizeof(CeWsHeader);
+    w.row_loss = reinterpret_cast<float*>(b + off);
+    off += round256(static_cast<size_t>(N) * 4);
+    w.chunk_err = reinterpret_cast<int32_t*>(b + off);
+    off += round256(static_cast<size_t>(nchunks + 1) * 4);
+    w.chunk_loss = reinterpret_cast<float*>(b + off);
+    off += 256;
+    w.z = b + off;
+    off += round256(static_cast<size_t>(std::min(chunk, std::max<int64_t>(N, 1))) * static_cast<size_t>(ldz) * 2);
+    w.bytes = off;
+    return w;
+}
+
+// loss = (sum of row terms, float64, row order) / D; n_valid; error word.
+__global__ void __launch_bounds__(kFinThreads) linear_ce_finalize(const float* __restrict__ row_loss,
+                                                                  const int64_t* __restrict__ labels, int64_t N,
+                                                                  int64_t V, int64_t ignore_index, float denom,
+                                                                  const int32_t* chunk_err, int64_t nchunks,
+                                                                  float* loss, int32_t* n_valid_out,
+                                                                  int32_t* err_out) {
+    __shared__ int iscratch[2 * (kFinThreads / 32)];
+    __shared__ double dred[kFinThreads / 32];
+    int n_valid = 0, n_bad = 0;
+    count_labels(labels, N, V, ignore_index, iscratch, n_valid, n_bad);
+    double acc = 0.0;
+    for (int64_t i = threadIdx.x; i < N; i += kFinThreads) acc += static_cast<double>(row_loss[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off);
+    if ((threadIdx.x & 31) == 0) dred[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+        for (int w = 0; w < kFinThreads / 32; ++w) tot += dred[w];
+        const double D = denom > 0.f ? static_cast<double>(denom) : static_cast<double>(n_valid);
+        *loss = static_cast<float>(tot / D);
+        if (n_valid_out) *n_valid_out = n_valid;
+        int32_t e = n_bad > 0 ? FOAK_ERRBIT_LABEL_RANGE : 0;
+        for (int64_t c = 0; c < nchunks; ++c) e |= chunk_err[c];
+        if (err_out) *err_out = e;
+    }
+}
+
+}  // namespace
+
+size_t linear_ce_workspace_bytes(int64_t N, int64_t V, int64_t chunk) {
+    return lin_layout(nullptr, N, V, chunk).bytes;
+}
+
+cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t V, int64_t D,
+                             int64_t ignore_index, int64_t chunk, float g, float denom, float* loss, void* dH,
+                             float* dW, int32_t* n_valid, int32_t* err, void* workspace, cudaStream_t stream) {
+    const LinWs ws = lin_layout(workspace, N, V, chunk);
+    const int64_t ldz = (V + 63) / 64 * 64;
+    const int64_t nchunks = N > 0 ? (N + chunk - 1) / chunk : 0;
+    int32_t* gemm_err = ws.chunk_err + nchunks;  // GEMM timeouts are OR-ed in here
+    cudaError_t e = cudaMemsetAsync(gemm_err, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    if (nchunks == 0) {
+        e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * static_cast<size_t>(D) * 4, stream);
+        if (e != cudaSuccess) return e;
+    }
+    const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
+    __nv_bfloat16* dHb = static_cast<__nv_bfloat16*>(dH);
+    for (int64_t c = 0; c < nchunks; ++c) {
+        const int64_t r0 = c * chunk;
+        const int rows = static_cast<int>(std::min(chunk, N - r0));
+        // 1. Z = H_c W^T
+        GemmDesc g1 = {};
+        g1.a = Hb + r0 * D;
+        g1.lda = D;
+        g1.a_mn_major = false;
+        g1.b = W;
+        g1.ldb = D;
+        g1.b_mn_major = false;
+        g1.M = rows;
+        g1.N = static_cast<int>(V);
+        g1.K = static_cast<int>(D);
+        g1.out = ws.z;
+        g1.ldo = ldz;
+        g1.mode = kGemmOutBf16;
+        g1.err = gemm_err;
+        e = launch_gemm_bf16(g1, stream);
+        if (e != cudaSuccess) return e;
+        // 2. dZ = (softmax(Z) - onehot) * g / D in place; row terms into the batch's row_loss
+        e = launch_ce_rows(true, 2, ws.z, ws.z, ldz, labels + r0, rows, V, ignore_index, g, denom, ws.chunk_loss,
+                           nullptr, ws.row_loss + r0, nullptr, ws.chunk_err + c, ws.hdr, stream, labels, N);
+        if (e != cudaSuccess) return e;
+        // 3. dH_c = dZ W     (W is [V][D]: MN-major as the [K][N] operand)
+        GemmDesc g2 = {};
+        g2.a = ws.z;
+        g2.lda = ldz;
+        g2.a_mn_major = false;
+        g2.b = W;
+        g2.ldb = D;
+        g2.b_mn_major = true;
+        g2.M = rows;
+        g2.N = static_cast<int>(D);
+        g2.K = static_cast<int>(V);
+        g2.out = dHb + r0 * D;
+        g2.ldo = D;
+        g2.mode = kGemmOutBf16;
+        g2.err = gemm_err;
+        e = launch_gemm_bf16(g2, stream);
+        if (e != cudaSuccess) return e;
+        // 4. dW (+)= dZ^T H_c  (dZ is [rows][V] = [K][M], H_c is [rows][D] = [K][N])
+        GemmDesc g3 = {};
+        g3.a = ws.z;
+        g3.lda = ldz;
+        g3.a_mn_major = true;
+        g3.b = Hb + r0 * D;
+        g3.ldb = D;
+        g3.b_mn_major = true;
+        g3.M = static_cast<int>(V);
+        g3.N = static_cast<int>(D);
+        g3.K = rows;
+        g3.out = dW;
+        g3.ldo = D;
+        g3.mode = c == 0 ? kGemmOutF32 : kGemmOutF32Acc;
+        g3.err = gemm_err;
+        e = launch_gemm_bf16(g3, stream);
+        if (e != cudaSuccess) return e;
+    }
+    linear_ce_finalize<<<1, kFinThreads, 0, stream>>>(ws.row_loss, labels, N, V, ignore_index, denom, ws.chunk_err,
+                                                      nchunks + 1, loss, n_valid, err);
+    return cudaGetLastError();
+}
+
+}  // namespace foak

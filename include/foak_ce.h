@@ -143,6 +143,36 @@ foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of device workspace foak_linear_ce_chunked needs: a 256-byte header, N
+ * float32 per-row loss terms, a few error words and one chunk of bf16 logits
+ * (min(chunk, N) x V, rows padded to 64 elements).  Same rules as the CE workspace:
+ * 256-byte aligned, zero-filled before first use, left reusable by every call.
+ */
+size_t foak_linear_ce_workspace_size(int64_t N, int64_t V, int64_t D, int64_t chunk);
+
+/*
+ * Chunked linear + cross-entropy: loss, dH and dW of CE(H W^T) computed chunk by
+ * chunk (Z = H_c W^T, dZ = (softmax(Z) - onehot) g / D, dH_c = dZ W,
+ * dW += dZ^T H_c) without materialising the N x V logits; the products run on the
+ * tcgen05 tensor cores with fp32 accumulation, Z/dZ are kept in bf16.
+ *   H (device)        bf16 [N][D] row-major (hidden states), D % 8 == 0
+ *   W (device)        bf16 [V][D] row-major (LM-head weight, no bias)
+ *   labels (device)   int64[N]; ignore_index as for the CE calls
+ *   chunk             rows per chunk (e.g. 1024), >= 1
+ *   g (host), denom   as for foak_ce_fwd_bwd; D = denom > 0 ? denom : n_valid of
+ *                     all N rows, the same for every chunk
+ *   loss (device)     float[1]
+ *   dH (device)       bf16 [N][D], overwritten
+ *   dW (device)       float32 [V][D], overwritten (not accumulated into)
+ *   n_valid, err      as for foak_ce_forward (err also reports GEMM wait timeouts)
+ * All pointers 16-byte aligned.
+ */
+foak_status foak_linear_ce_chunked(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t V,
+                                   int64_t D, int64_t ignore_index, int64_t chunk, float g, float denom,
+                                   float* loss, void* dH, float* dW, int32_t* n_valid, int32_t* err,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Building block of the chunked linear + CE: C[M x N] (+)= A[M x K] * B[N x K]^T on
  * the tcgen05 tensor cores, bf16 operands, fp32 accumulation (exposed so the
  * three products of the chunked call can be tested and timed alone).
