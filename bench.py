@@ -295,6 +295,8 @@ def run_ours(args, rank, world, dist):
     main = _make(args.workload)
     if sampler:
         sampler.start()
+    if args.profile and args.path == "chunked":
+        return {"metric": "chunked linear+CE (profiling run)", "chunked": chunked_timing(ce, torch, dev, stream)}
     call = None
     if args.profile and args.path == "forward":
         call = lambda b, y, workspace_tensor: ce.foak_ce_forward(b, y, workspace_tensor=workspace_tensor)  # noqa: E731
@@ -443,7 +445,67 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
                 "ms_per_step": fms + bms, "tokens_per_s": N / ((fms + bms) * 1e-3)})
     del bufs, dl
     torch.cuda.empty_cache()
+    out.extend(chunked_timing(ce, torch, dev, stream))
     return out
+
+
+CHUNKED_DESC = ("chunked linear+CE: H 8192x4096 bf16 ~N(0,1), W 32000x4096 bf16 ~N(0,0.02^2), 10% rows -100, "
+                "chunks of 1024 rows")
+
+
+def chunked_timing(ce, torch, dev, stream, steps=5, warmup=2):
+    """foak_linear_ce_chunked on the chunked workload, and its three GEMM shapes alone."""
+    c = wl.chunked()
+    N, V, D, chunk = c["N"], c["V"], c["D"], c["chunk"]
+    H = torch.from_numpy(c["H"].view(np.int16)).to(dev).view(torch.bfloat16)
+    W = torch.from_numpy(c["W"].view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.from_numpy(c["labels"]).to(dev)
+    dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    peak, src = _peak_bf16(sustained=False)
+    res = []
+
+    def timed(fn, k, w):
+        for _ in range(w):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / k
+
+    ms = timed(lambda: ce.foak_linear_ce_chunked(H, W, y, chunk=chunk, dH=dH, dW=dW), steps, warmup)
+    out = ce.foak_linear_ce_chunked(H, W, y, chunk=chunk, dH=dH, dW=dW)
+    flops = 6.0 * N * V * D
+    tf = flops / (ms * 1e-3) / 1e12
+    res.append({"path": "foak_linear_ce_chunked", "workload": CHUNKED_DESC, "steps": steps, "ms_per_step": ms,
+                "tokens_per_s": N / (ms * 1e-3), "TFLOPs": tf, "frac": tf / peak, "peak": peak,
+                "peak_unit": "TFLOP/s bf16", "peak_source": src, "loss": float(out["loss"].item()),
+                "err": int(out["err"].item()), "gpu_launches_per_step": 4 * ((N + chunk - 1) // chunk) + 1})
+    # the three products of one chunk, alone
+    Z = torch.empty(chunk, V, dtype=torch.bfloat16, device=dev)
+    Zs = torch.randn(chunk, V, device=dev).to(torch.bfloat16)
+    Hc = H[:chunk]
+    dHc = torch.empty(chunk, D, dtype=torch.bfloat16, device=dev)
+    shapes = [
+        ("Z = H_c W^T (M=1024, N=32000, K=4096, K/K-major)",
+         lambda: ce.foak_gemm_bf16(Hc, W, Z, mode=ce.FOAK_GEMM_BF16)),
+        ("dH_c = dZ W (M=1024, N=4096, K=32000, K/MN-major)",
+         lambda: ce.foak_gemm_bf16(Zs, W, dHc, b_mn_major=True, mode=ce.FOAK_GEMM_BF16)),
+        ("dW += dZ^T H_c (M=32000, N=4096, K=1024, MN/MN-major, fp32 RMW)",
+         lambda: ce.foak_gemm_bf16(Zs, Hc, dW, a_mn_major=True, b_mn_major=True, mode=ce.FOAK_GEMM_F32_ACC)),
+    ]
+    for name, fn in shapes:
+        gms = timed(fn, 10, 3)
+        gtf = 2.0 * chunk * V * D / (gms * 1e-3) / 1e12
+        res.append({"path": "foak_gemm_bf16", "workload": name, "steps": 10, "ms_per_step": gms, "TFLOPs": gtf,
+                    "frac": gtf / peak, "peak_source": src})
+    del H, W, dH, dW, Z, Zs
+    torch.cuda.empty_cache()
+    return res
 
 
 # ----------------------------------------------------------------------------- oracle legs
@@ -512,7 +574,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="mistral")
     ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
-    ap.add_argument("--path", choices=["fused", "forward"], default="fused",
+    ap.add_argument("--path", choices=["fused", "forward", "chunked"], default="fused",
                     help="with --profile: which entry point the timed loop calls")
     ap.add_argument("--profile", action="store_true",
                     help="headline timed loop only (no e2e, secondary, clocks or CPU baseline): for ncu captures")
