@@ -34,11 +34,15 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;    // 48 KB
 constexpr uint32_t kMNBlock = 64 * kBK * 2;            // one 64 (MN) x 64 (K) box: 8 KB
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 2 * kBN;
-constexpr size_t kGemmSmem = kStages * kStageBytes + 1024;  // + alignment slack
+// fp32 outputs leave through shared memory: per epilogue warp two 32 x 32 fp32
+// staging boxes (4 KB each, 128-byte swizzle) written back by TMA store or reduce-add.
+constexpr uint32_t kStageOutBytes = 32 * 32 * 4;
+constexpr size_t kGemmSmem = kStages * kStageBytes + 4 * 2 * kStageOutBytes + 1024;  // + alignment slack
 
 struct GemmParams {
     CUtensorMap tmA;
     CUtensorMap tmB;
+    CUtensorMap tmC;  // fp32 output (modes kGemmOutF32 / kGemmOutF32Acc)
     int M, N, K;
     int a_mn, b_mn;
     int mode;
@@ -156,6 +160,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     } else {
         // epilogue warps 2..5: TMEM lane quarter = warp % 4
         const int q = warp & 3;
+        float* out_stage = reinterpret_cast<float*>(smem + kStages * kStageBytes) + q * 2 * (kStageOutBytes / 4);
+        uint32_t out_it = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -166,16 +172,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
             }
             tc_fence_after();
             const int m0 = (t % p.tiles_m) * kBM, n0 = (t / p.tiles_m) * kBN;
-            const int row = m0 + q * 32 + lane;
+            const int row_blk = m0 + q * 32;  // first row of this warp's 32
+            const int row = row_blk + lane;
 #pragma unroll 1
             for (int c = 0; c < kBN / 32; ++c) {
                 uint32_t r[32];
                 tc_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN + c * 32), r);
                 tc_wait_ld();
                 const int col0 = n0 + c * 32;
-                if (row >= p.M || col0 >= p.N) continue;
+                if (col0 >= p.N) continue;
                 const bool full_chunk = col0 + 32 <= p.N;
                 if (p.mode == kGemmOutBf16) {
+                    if (row >= p.M) continue;
                     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo + col0;
                     if (full_chunk) {
                         uint4* o4 = reinterpret_cast<uint4*>(o);
@@ -193,28 +201,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                         for (int j = 0; j < 32; ++j)
                             if (col0 + j < p.N) o[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
                     }
-                } else {
-                    float* o = static_cast<float*>(p.out) + static_cast<int64_t>(row) * p.ldo + col0;
-                    const bool accum = p.mode == kGemmOutF32Acc;
-                    if (full_chunk) {
-                        float4* o4 = reinterpret_cast<float4*>(o);
+                } else if (row_blk < p.M) {
+                    // stage the 32 x 32 box (row = lane) with the 128-byte swizzle, then one
+                    // TMA store or reduce-add writes it back; two boxes alternate per warp
+                    float* sbuf = out_stage + (out_it & 1) * (kStageOutBytes / 4);
+                    ++out_it;
+                    if (lane == 0) bulk_wait_group_read_1();
+                    __syncwarp();
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            float4 w = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
-                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                            if (accum) {
-                                const float4 prev = o4[v];
-                                w.x += prev.x;
-                                w.y += prev.y;
-                                w.z += prev.z;
-                                w.w += prev.w;
-                            }
-                            o4[v] = w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < p.N) o[j] = accum ? o[j] + __uint_as_float(r[j]) : __uint_as_float(r[j]);
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4*>(sbuf + lane * 32 + ((j ^ (lane & 7)) * 4)) =
+                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (p.mode == kGemmOutF32Acc) tma_reduce_add_2d(&p.tmC, sbuf, col0, row_blk);
+                        else tma_store_2d(&p.tmC, sbuf, col0, row_blk);
+                        bulk_commit_group();
                     }
                 }
             }
@@ -226,6 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         }
     }
 
+    if (warp >= 2 && lane == 0) bulk_wait_group_0();  // staged fp32 boxes fully written
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -265,6 +270,21 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer
     return r == CUDA_SUCCESS;
 }
 
+// Row-major fp32 [rows][cols] output with row stride ld: 32 x 32 boxes, 128-byte
+// swizzle (the staging layout of the epilogue).
+bool encode_f32_out(CUtensorMap* m, void* ptr, uint64_t cols, uint64_t rows, int64_t ld) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 std::mutex g_gemm_mu;
 bool g_gemm_attr[64] = {false};
 
@@ -279,6 +299,8 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     ok = ok && (d.b_mn_major
                     ? encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.K), d.ldb, 64)
                     : encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N), d.ldb, kBN));
+    if (ok && d.mode != kGemmOutBf16)
+        ok = encode_f32_out(&p.tmC, d.out, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.M), d.ldo);
     if (!ok) return cudaErrorInvalidValue;
     p.M = d.M;
     p.N = d.N;
