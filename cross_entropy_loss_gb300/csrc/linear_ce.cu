@@ -10,10 +10,11 @@
 //                              batch's n_valid (counted over all N labels), so
 //                              the result does not depend on the chunk size
 //   3. dH_c = dZ W             tcgen05 GEMM, bf16 out into dH
-//   4. dW (+)= dZ^T H_c        tcgen05 GEMM, fp32 out (stored by the first
-//                              chunk, accumulated by the others)
+//   4. dW (+)= dZ^T H          tcgen05 GEMM, fp32 out, once per group of
+//                              kDeferChunks chunks (stored by the first group,
+//                              added by TMA reduce for the others)
 // and finally one CTA sums the per-row loss terms of all N rows in float64, in
-// row order, over the denominator.  Only one chunk's Z lives at a time.
+// row order, over the denominator.  Only one group's Z lives at a time.
 #include <algorithm>
 
 #include "common.cuh"
@@ -26,6 +27,10 @@ namespace foak {
 namespace {
 
 constexpr int kFinThreads = 512;
+// dW is updated once per group of this many chunks (one product with K = the
+// group's rows), halving its fp32 read-modify-write traffic; only the group's
+// logits are ever resident.
+constexpr int64_t kDeferChunks = 2;
 
 inline size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
@@ -34,7 +39,7 @@ struct LinWs {
     float* row_loss;   // N
     int32_t* chunk_err;  // one word per chunk's CE call, then one word for the GEMMs
     float* chunk_loss;   // scratch loss output of the chunk CE calls
-    void* z;           // chunk x ldz bf16
+    void* z;           // kDeferChunks chunks x ldz bf16
     size_t bytes;
 };
 
@@ -53,7 +58,8 @@ LinWs lin_layout(void* base, int64_t N, int64_t V, int64_t chunk) {
     w.chunk_loss = reinterpret_cast<float*>(b + off);
     off += 256;
     w.z = b + off;
-    off += round256(static_cast<size_t>(std::min(chunk, std::max<int64_t>(N, 1))) * static_cast<size_t>(ldz) * 2);
+    off += round256(static_cast<size_t>(std::min(kDeferChunks * chunk, std::max<int64_t>(N, 1))) *
+                    static_cast<size_t>(ldz) * 2);
     w.bytes = off;
     return w;
 }
@@ -108,9 +114,12 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
     }
     const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
     __nv_bfloat16* dHb = static_cast<__nv_bfloat16*>(dH);
+    __nv_bfloat16* zbuf = static_cast<__nv_bfloat16*>(ws.z);
     for (int64_t c = 0; c < nchunks; ++c) {
         const int64_t r0 = c * chunk;
         const int rows = static_cast<int>(std::min(chunk, N - r0));
+        const int64_t slot = c % kDeferChunks;  // this chunk's place in the group's Z buffer
+        __nv_bfloat16* z = zbuf + slot * chunk * ldz;
         // 1. Z = H_c W^T
         GemmDesc g1 = {};
         g1.a = Hb + r0 * D;
@@ -122,19 +131,19 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
         g1.M = rows;
         g1.N = static_cast<int>(V);
         g1.K = static_cast<int>(D);
-        g1.out = ws.z;
+        g1.out = z;
         g1.ldo = ldz;
         g1.mode = kGemmOutBf16;
         g1.err = gemm_err;
         e = launch_gemm_bf16(g1, stream);
         if (e != cudaSuccess) return e;
         // 2. dZ = (softmax(Z) - onehot) * g / D in place; row terms into the batch's row_loss
-        e = launch_ce_rows(true, 2, ws.z, ws.z, ldz, labels + r0, rows, V, ignore_index, g, denom, ws.chunk_loss,
+        e = launch_ce_rows(true, 2, z, z, ldz, labels + r0, rows, V, ignore_index, g, denom, ws.chunk_loss,
                            nullptr, ws.row_loss + r0, nullptr, ws.chunk_err + c, ws.hdr, stream, labels, N);
         if (e != cudaSuccess) return e;
         // 3. dH_c = dZ W     (W is [V][D]: MN-major as the [K][N] operand)
         GemmDesc g2 = {};
-        g2.a = ws.z;
+        g2.a = z;
         g2.lda = ldz;
         g2.a_mn_major = false;
         g2.b = W;
@@ -149,23 +158,28 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
         g2.err = gemm_err;
         e = launch_gemm_bf16(g2, stream);
         if (e != cudaSuccess) return e;
-        // 4. dW (+)= dZ^T H_c  (dZ is [rows][V] = [K][M], H_c is [rows][D] = [K][N])
-        GemmDesc g3 = {};
-        g3.a = ws.z;
-        g3.lda = ldz;
-        g3.a_mn_major = true;
-        g3.b = Hb + r0 * D;
-        g3.ldb = D;
-        g3.b_mn_major = true;
-        g3.M = static_cast<int>(V);
-        g3.N = static_cast<int>(D);
-        g3.K = rows;
-        g3.out = dW;
-        g3.ldo = D;
-        g3.mode = c == 0 ? kGemmOutF32 : kGemmOutF32Acc;
-        g3.err = gemm_err;
-        e = launch_gemm_bf16(g3, stream);
-        if (e != cudaSuccess) return e;
+        // 4. once the group is complete: dW (+)= dZ_g^T H_g over the group's rows
+        //    (dZ_g is [rows_g][V] = [K][M], H_g is [rows_g][D] = [K][N])
+        if (slot == kDeferChunks - 1 || c == nchunks - 1) {
+            const int64_t g0 = (c - slot) * chunk;
+            const int rows_g = static_cast<int>(r0 + rows - g0);
+            GemmDesc g3 = {};
+            g3.a = zbuf;
+            g3.lda = ldz;
+            g3.a_mn_major = true;
+            g3.b = Hb + g0 * D;
+            g3.ldb = D;
+            g3.b_mn_major = true;
+            g3.M = static_cast<int>(V);
+            g3.N = static_cast<int>(D);
+            g3.K = rows_g;
+            g3.out = dW;
+            g3.ldo = D;
+            g3.mode = g0 == 0 ? kGemmOutF32 : kGemmOutF32Acc;
+            g3.err = gemm_err;
+            e = launch_gemm_bf16(g3, stream);
+            if (e != cudaSuccess) return e;
+        }
     }
     linear_ce_finalize<<<1, kFinThreads, 0, stream>>>(ws.row_loss, labels, N, V, ignore_index, denom, ws.chunk_err,
                                                       nchunks + 1, loss, n_valid, err);

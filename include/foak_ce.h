@@ -144,8 +144,9 @@ foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64
 
 /*
  * Bytes of device workspace foak_linear_ce_chunked needs: a 256-byte header, N
- * float32 per-row loss terms, a few error words and one chunk of bf16 logits
- * (min(chunk, N) x V, rows padded to 64 elements).  Same rules as the CE workspace:
+ * float32 per-row loss terms, a few error words and two chunks of bf16 logits
+ * (min(2 chunk, N) x V, rows padded to 64 elements: dW is updated once per pair
+ * of chunks).  Same rules as the CE workspace:
  * 256-byte aligned, zero-filled before first use, left reusable by every call.
  */
 size_t foak_linear_ce_workspace_size(int64_t N, int64_t V, int64_t D, int64_t chunk);
