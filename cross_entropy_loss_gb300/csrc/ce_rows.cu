@@ -266,8 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p
     constexpr int EPV = 16 / ES;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t bars[kRowMaxStages];
-    __shared__ float red_m[kRowWarps];
-    __shared__ float red_s[kRowWarps];
+    __shared__ float2 red_ms[2][kRowWarps];
     __shared__ float2 cl_slot[2];
     __shared__ int64_t s_lab[kLabCache];
     __shared__ int iscratch[2 * kRowWarps];
@@ -402,20 +401,11 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p
             }
         }
 
-        // Row max: thread -> warp -> CTA.  The barrier that publishes the warp
-        // maxima also frees the stage for the producer.
+        // Row (max, sum): the thread's sum is taken relative to its warp's max, the
+        // warp's pair is published, and one barrier per row (which also frees the
+        // stage for the producer) lets every warp merge the CTA's pairs.
         m = warp_max(m);
-        if (lane == 0) red_m[warp] = m;
-        __syncthreads();
-        if (s_abort) aborted = true;
-        if (tid == 0 && !aborted) {
-            fence_proxy_async_smem();
-            issue_next();
-        }
-        float M = warp_max(lane < kRowWarps ? red_m[lane] : kNegInf);
-
-        // Sum of exp(x - M) relative to the CTA max, so no rescaling is needed in the CTA.
-        const float mb = M == kNegInf ? 0.f : M * kLog2e;
+        const float mb = m == kNegInf ? 0.f : m * kLog2e;
         float sum = RowMath<ES>::template vsum<VPT>(v, mb);
         if (ns > 0) {
 #pragma unroll
@@ -423,9 +413,17 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p
                 if (s < ns) sum += ex2(fmaf(xs[s], kLog2e, -mb));
         }
         sum = warp_sum(sum);
-        if (lane == 0) red_s[warp] = sum;
+        const int rb = c_v & 1;  // red[] is double-buffered by row parity
+        if (lane == 0) red_ms[rb][warp] = make_float2(m, sum);
         __syncthreads();
-        float S = warp_sum(lane < kRowWarps ? red_s[lane] : 0.f);
+        if (s_abort) aborted = true;
+        if (tid == 0 && !aborted) {
+            fence_proxy_async_smem();
+            issue_next();
+        }
+        const float2 pr = lane < kRowWarps ? red_ms[rb][lane] : make_float2(kNegInf, 0.f);
+        float M = warp_max(pr.x);
+        float S = warp_sum(pr.x == kNegInf ? 0.f : pr.y * ex2((pr.x - M) * kLog2e));
         if (K > 1) {
             // cluster: merge the CTAs' (max, sum) pairs read through distributed shared memory
             const int slot = c_v & 1u;
