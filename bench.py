@@ -293,6 +293,8 @@ def run_ours(args, rank, world, dist):
         return dp.max_over_ranks(v, device=dev)
 
     main = _make(args.workload)
+    if args.profile and args.rows > 0:
+        main = dict(main, logits=main["logits"][:args.rows], labels=main["labels"][:args.rows])
     if sampler:
         sampler.start()
     if args.profile and args.path == "chunked":
@@ -574,6 +576,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="mistral")
     ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="with --profile: keep only the first ROWS rows of the workload (smaller ncu captures)")
     ap.add_argument("--path", choices=["fused", "forward", "chunked"], default="fused",
                     help="with --profile: which entry point the timed loop calls")
     ap.add_argument("--profile", action="store_true",
