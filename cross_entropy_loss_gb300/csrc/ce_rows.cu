@@ -267,7 +267,8 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t bars[kRowMaxStages];
     __shared__ float2 red_ms[2][kRowWarps];
-    __shared__ float2 cl_slot[2];
+    __shared__ float2 xslot[2][kRowMaxCluster];  // [row parity][source CTA] (max, sum) pairs
+    __shared__ uint64_t xbar[2];                  // completes when all K pairs of a row arrived
     __shared__ int64_t s_lab[kLabCache];
     __shared__ int iscratch[2 * kRowWarps];
     __shared__ double dred[kRowWarps];
@@ -285,11 +286,14 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p
 
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) mbar_init(&bars[s], 1);
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
         fence_mbar_init();
         s_abort = 0;
         s_last = 0;
     }
     __syncthreads();
+    if (K > 1) cluster_sync();  // every CTA's exchange barriers exist before the first st.async
 
     // Producer state (thread 0): next row iteration to look at, valid rows issued.
     int64_t p_it = 0;
@@ -425,12 +429,19 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p
         float M = warp_max(pr.x);
         float S = warp_sum(pr.x == kNegInf ? 0.f : pr.y * ex2((pr.x - M) * kLog2e));
         if (K > 1) {
-            // cluster: merge the CTAs' (max, sum) pairs read through distributed shared memory
-            const int slot = c_v & 1u;
-            if (tid == 0) cl_slot[slot] = make_float2(M, S);
-            cluster_sync();
-            const float2 q = lane < K ? ld_dsmem_f2(&cl_slot[slot], static_cast<uint32_t>(lane))
-                                      : make_float2(kNegInf, 0.f);
+            // cluster: thread 0 sends this CTA's pair to every CTA of the cluster with
+            // st.async (no fence, so the row's gradient stores never have to drain
+            // first); each CTA waits on its own barrier for the K pairs and merges them
+            const uint32_t j = c_v - 1;
+            const int xb = j & 1;
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&xbar[xb], 8u * static_cast<uint32_t>(K));
+                for (int r = 0; r < K; ++r)
+                    st_async_f2(mapa_u32(&xslot[xb][rank], static_cast<uint32_t>(r)), M, S,
+                                mapa_u32(&xbar[xb], static_cast<uint32_t>(r)));
+            }
+            if (!aborted && !mbar_wait_bounded(&xbar[xb], (j >> 1) & 1u)) s_abort = 1;
+            const float2 q = lane < K ? xslot[xb][lane] : make_float2(kNegInf, 0.f);
             M = q.x;
             S = q.y;
             warp_ms_reduce(M, S);
@@ -513,7 +524,7 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p
             ++c_v;
         }
     }
-    if (K > 1) cluster_sync();  // peers may still read this CTA's cl_slot
+    if (K > 1) cluster_sync();  // no CTA leaves while a peer may still send it a pair
 
     __syncthreads();
     if (tid == 0) {

@@ -123,6 +123,21 @@ __device__ __forceinline__ float2 ld_dsmem_f2(const void* local, uint32_t rank) 
     return v;
 }
 
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_u32(const void* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    return remote;
+}
+
+// Asynchronous store of two floats into (possibly another CTA's) shared memory,
+// completing 8 bytes of transaction on that CTA's mbarrier; no fence is implied.
+__device__ __forceinline__ void st_async_f2(uint32_t remote_addr, float a, float b, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(remote_addr),
+                 "f"(a), "f"(b), "r"(remote_bar)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- math / memory
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32).
 __device__ __forceinline__ float ex2(float x) {
