@@ -259,8 +259,9 @@ __device__ __forceinline__ uint4 vec_grad_label(const uint4& v, int e_own, float
 }
 
 template <int ES, bool GRAD, int THREADS>
-__global__ void __launch_bounds__(THREADS, 1) ce_rows_kernel(const CeRowParams p) {
-    constexpr int VPT = kRowSliceVecMax / THREADS;  // 64 KB slice: 512 x 8 or 1024 x 4 vectors
+__global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kernel(const CeRowParams p) {
+    // slice: 512 x 8 or 1024 x 4 vectors (64 KB, one CTA per SM) or 256 x 8 (32 KB, two CTAs per SM)
+    constexpr int VPT = THREADS == 256 ? 8 : kRowSliceVecMax / THREADS;
     constexpr int kRowThreads = THREADS;
     constexpr int kRowWarps = THREADS / 32;
     constexpr int EPV = 16 / ES;
@@ -571,25 +572,42 @@ struct Plan {
     size_t smem;
 };
 
-bool plan_rows(int ES, int64_t V, Plan* pl) {
-    static const int threads = [] {
-        const char* e = std::getenv("FOAK_ROW_THREADS");  // tuning override: 512 (default) or 1024
-        return (e && std::atoi(e) == 1024) ? 1024 : 512;
-    }();
+constexpr size_t kSmemBudgetHalf = 100 * 1024;  // per CTA when two CTAs share an SM
+
+// Smallest cluster whose per-CTA slices fit `slice_max` vectors.
+bool plan_with(int ES, int64_t V, int threads, int64_t slice_max, size_t budget, Plan* pl) {
     const int64_t nb_max = V * ES / 16;
     for (int k = 1; k <= kRowMaxCluster; k *= 2) {
         const int64_t per = (nb_max + k - 1) / k;
-        if (per <= kRowSliceVecMax) {
+        if (per <= slice_max) {
             pl->threads = threads;
             pl->k = k;
             pl->per = static_cast<int>(std::max<int64_t>(per, 1));
             pl->stage_bytes = static_cast<uint32_t>(((pl->per * 16 + 127) / 128) * 128);
-            pl->stages = static_cast<int>(std::min<size_t>(kRowMaxStages, kSmemBudget / pl->stage_bytes));
+            pl->stages = static_cast<int>(std::min<size_t>(kRowMaxStages, budget / pl->stage_bytes));
             pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes;
             return pl->stages >= 2;
         }
     }
     return false;
+}
+
+// Rows that fit one 64 KB slice: one 512-thread CTA per row and SM.  Longer rows
+// need a cluster anyway; there 32 KB slices on 256-thread CTAs, two per SM, hide
+// each other's per-row latency better (when eight of them cover the row).
+bool plan_rows(int ES, int64_t V, Plan* pl) {
+    static const int forced = [] {
+        const char* e = std::getenv("FOAK_ROW_THREADS");  // tuning override: 256, 512 or 1024
+        return e ? std::atoi(e) : 0;
+    }();
+    if (forced == 1024 && plan_with(ES, V, 1024, kRowSliceVecMax, kSmemBudget, pl)) return true;
+    if (forced == 256 && plan_with(ES, V, 256, 2048, kSmemBudgetHalf, pl)) return true;
+    if (!plan_with(ES, V, 512, kRowSliceVecMax, kSmemBudget, pl)) return false;
+    if (forced == 0 && pl->k > 1) {
+        Plan half;
+        if (plan_with(ES, V, 256, 2048, kSmemBudgetHalf, &half)) *pl = half;
+    }
+    return true;
 }
 
 std::mutex g_mu;
@@ -672,6 +690,7 @@ cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t s
 
 template <int ES, bool GRAD>
 cudaError_t launch_vpt(const CeRowParams& base, const Plan& pl, cudaStream_t stream) {
+    if (pl.threads == 256) return launch_typed<ES, GRAD, 256>(base, pl, stream);
     return pl.threads == 1024 ? launch_typed<ES, GRAD, 1024>(base, pl, stream)
                               : launch_typed<ES, GRAD, 512>(base, pl, stream);
 }
