@@ -302,6 +302,15 @@ def run_ours(args, rank, world, dist):
     call = None
     if args.profile and args.path == "forward":
         call = lambda b, y, workspace_tensor: ce.foak_ce_forward(b, y, workspace_tensor=workspace_tensor)  # noqa: E731
+    if args.profile and args.path == "backward":
+        x0 = upload(main["logits"], main["dtype"])
+        y0 = torch.from_numpy(main["labels"]).to(dev)
+        lse0 = ce.foak_ce_forward(x0, y0)["lse"]
+        dl = torch.empty_like(x0)
+
+        def call(b, y, workspace_tensor):
+            ce.foak_ce_backward(b, y, lse0, dlogits=dl)
+            return {"loss": torch.zeros(1, device=dev), "err": torch.zeros(1, dtype=torch.int32, device=dev)}
     ms, loss, err, reused = fused_timing(main, args.steps, args.warmup, True, call=call)
     ms = max_over_ranks(ms)
     if sampler:
@@ -578,7 +587,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--rows", type=int, default=0,
                     help="with --profile: keep only the first ROWS rows of the workload (smaller ncu captures)")
-    ap.add_argument("--path", choices=["fused", "forward", "chunked"], default="fused",
+    ap.add_argument("--path", choices=["fused", "forward", "backward", "chunked"], default="fused",
                     help="with --profile: which entry point the timed loop calls")
     ap.add_argument("--profile", action="store_true",
                     help="headline timed loop only (no e2e, secondary, clocks or CPU baseline): for ncu captures")
