@@ -52,6 +52,8 @@ SIGNATURES = {
     "foak_linear_ce_chunked": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _sz, _vp]),
     "foak_test_fail_next_launches": (None, [_i32]),
+    "foak_test_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "foak_test_skip_row_load": (None, [_i64]),
 }
 
 

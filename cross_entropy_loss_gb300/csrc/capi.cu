@@ -27,6 +27,14 @@ int device_sm_count() {
 }
 
 namespace {
+std::atomic<uint64_t> g_wait_limit_ns{4000000000ull};
+std::atomic<int64_t> g_skip_load_row{-1};
+}  // namespace
+
+uint64_t test_wait_limit_ns() { return g_wait_limit_ns.load(); }
+int64_t test_skip_load_row() { return g_skip_load_row.load(); }
+
+namespace {
 
 std::atomic<int> g_fail_launches{0};
 
@@ -240,5 +248,9 @@ foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const
 }
 
 void foak_test_fail_next_launches(int32_t count) { g_fail_launches.store(count < 0 ? 0 : count); }
+
+void foak_test_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns == 0 ? 4000000000ull : ns); }
+
+void foak_test_skip_row_load(int64_t row) { g_skip_load_row.store(row < 0 ? -1 : row); }
 
 }  // extern "C"

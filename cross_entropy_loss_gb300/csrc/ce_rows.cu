@@ -56,6 +56,8 @@ struct CeRowParams {
     CeWsHeader* ws;
     const int64_t* count_labels;  // labels whose valid count is the denominator (the batch's)
     int64_t count_N;
+    uint64_t wait_ns;        // limit of every shared-memory barrier wait
+    int64_t skip_load_row;   // test hook: this row's slice is never loaded (-1: none)
     int k;               // CTAs per row (cluster size)
     int per;             // vectors per CTA slice
     int stages;          // rows in flight per CTA
@@ -309,6 +311,10 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
             const int64_t y = label_of(p_it);
             ++p_it;
             if (y == p.ignore_index || y < 0 || y >= p.V) continue;
+            if (row == p.skip_load_row) {  // test hook: the stage's barrier is never completed
+                ++p_v;
+                return;
+            }
             const char* rowp = p.x + row * row_bytes;
             const RowGeom gm = row_geom<ES>(rowp, p.V);
             int64_t nl = gm.nb - v0;
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
             c_par ^= 1u;
         }
         ++c_v;
-        if (!aborted && !mbar_wait_bounded(&bars[st], par)) s_abort = 1;
+        if (!aborted && !mbar_wait_bounded(&bars[st], par, p.wait_ns)) s_abort = 1;
 
         // Slice -> registers (vectors past the slice hold -inf); scalars from global memory.
         uint4 v[VPT];
@@ -441,7 +447,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
                     st_async_f2(mapa_u32(&xslot[xb][rank], static_cast<uint32_t>(r)), M, S,
                                 mapa_u32(&xbar[xb], static_cast<uint32_t>(r)));
             }
-            if (!aborted && !mbar_wait_bounded(&xbar[xb], (j >> 1) & 1u)) s_abort = 1;
+            if (!aborted && !mbar_wait_bounded(&xbar[xb], (j >> 1) & 1u, p.wait_ns)) s_abort = 1;
             const float2 q = lane < K ? xslot[xb][lane] : make_float2(kNegInf, 0.f);
             M = q.x;
             S = q.y;
@@ -521,7 +527,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     if (tid == 0) {
         while (c_v < p_v) {
             const int st = static_cast<int>(c_v % static_cast<uint32_t>(p.stages));
-            (void)mbar_wait_bounded(&bars[st], (c_v / static_cast<uint32_t>(p.stages)) & 1u);
+            (void)mbar_wait_bounded(&bars[st], (c_v / static_cast<uint32_t>(p.stages)) & 1u, p.wait_ns);
             ++c_v;
         }
     }
@@ -722,6 +728,8 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
     prm.ws = ws;
     prm.count_labels = count_labels ? count_labels : labels;
     prm.count_N = count_labels ? count_N : N;
+    prm.wait_ns = test_wait_limit_ns();
+    prm.skip_load_row = test_skip_load_row();
     if (elem_bytes == 2)
         return grad ? launch_vpt<2, true>(prm, pl, stream) : launch_vpt<2, false>(prm, pl, stream);
     return grad ? launch_vpt<4, true>(prm, pl, stream) : launch_vpt<4, false>(prm, pl, stream);

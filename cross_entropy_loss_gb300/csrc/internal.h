@@ -50,6 +50,11 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
                              int64_t ignore_index, int64_t chunk, float g, float denom, float* loss, void* dH,
                              float* dW, int32_t* n_valid, int32_t* err, void* workspace, cudaStream_t stream);
 
+// Test hooks (capi.cu): the barrier-wait limit given to the row kernel, and a row
+// whose slice the row kernel's producer skips (so a wait is sure to run out).
+uint64_t test_wait_limit_ns();
+int64_t test_skip_load_row();
+
 // Streaming multiprocessor count of the current device (cached per device).
 int device_sm_count();
 

@@ -231,6 +231,18 @@ foak_status foak_ce_fwd_bwd_noalloc(void* logits, int32_t dtype, int64_t ld, con
  */
 void foak_test_fail_next_launches(int32_t count);
 
+/*
+ * Test hooks for the device-side failure path (no fault is involved): the row
+ * kernels' shared-memory barrier waits give up after `ns` nanoseconds (0 restores
+ * the default of 4 s), and the row kernels' producers never load row `row`'s data
+ * (-1 disables), so the wait for that row is sure to run out.  A call that hits a
+ * run-out wait stops loading, finishes its barriers, leaves the workspace reusable
+ * and reports FOAK_ERRBIT_TIMEOUT in its error word (FOAK_ERR_TIMEOUT under
+ * FOAK_SYNC_CHECK=1); its loss and gradient are then undefined.
+ */
+void foak_test_set_wait_limit_ns(uint64_t ns);
+void foak_test_skip_row_load(int64_t row);
+
 #ifdef __cplusplus
 }
 #endif

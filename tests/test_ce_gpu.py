@@ -238,3 +238,49 @@ def test_llama3_vocab_full_size(cuda_lib, dtype):
     # the all-equal row: lse = 3 + ln V exactly in the oracle
     assert lse[r] == pytest.approx(3.0 + math.log(128256), abs=1e-12)
     assert to_f64(out["lse"])[r] == pytest.approx(3.0 + math.log(128256), abs=3e-6)
+
+
+# ------------------------------------------------------------ failure detection
+
+def test_wait_timeout_is_reported_and_recovers(cuda_lib, monkeypatch):
+    """A barrier wait that nothing completes runs out its short limit: the call
+    reports FOAK_ERRBIT_TIMEOUT (FOAK_ERR_TIMEOUT under FOAK_SYNC_CHECK=1), nothing
+    faults, and the next call on the same workspace is correct."""
+    ce = cuda_lib
+    cases = [_rand(300, 5000, wl.BF16, seed=4), _rand(6, 128256, wl.BF16, seed=5, n_ignore=1)]
+    try:
+        ce.lib.foak_test_set_wait_limit_ns(100_000_000)
+        for x, y in cases:
+            row = int(np.nonzero(y != -100)[0][2])
+            ce.lib.foak_test_skip_row_load(row)
+            t = to_device(x, wl.BF16)
+            out = ce.foak_ce_fwd_bwd(t, torch.from_numpy(y).cuda())
+            torch.cuda.synchronize()
+            assert out["err"].item() & ce.FOAK_ERRBIT_TIMEOUT
+            monkeypatch.setenv("FOAK_SYNC_CHECK", "1")
+            with pytest.raises(ce.FoakError) as ei:
+                ce.foak_ce_fwd_bwd(to_device(x, wl.BF16), torch.from_numpy(y).cuda())
+            assert ei.value.status == ce.FOAK_ERR_TIMEOUT
+            monkeypatch.delenv("FOAK_SYNC_CHECK")
+    finally:
+        ce.lib.foak_test_skip_row_load(-1)
+        ce.lib.foak_test_set_wait_limit_ns(0)
+    for x, y in cases:
+        _check_fused(cuda_lib, x, y, x.shape[1], wl.BF16)
+
+
+def test_sync_check_reports_bad_labels(cuda_lib, monkeypatch):
+    ce = cuda_lib
+    x, y = _rand(20, 300, wl.F32, seed=6)
+    y[4] = 300
+    monkeypatch.setenv("FOAK_SYNC_CHECK", "1")
+    with pytest.raises(ce.FoakError) as ei:
+        ce.foak_ce_fwd_bwd(to_device(x, wl.F32), torch.from_numpy(y).cuda())
+    assert ei.value.status == ce.FOAK_ERR_LABEL_RANGE
+
+
+def test_many_rows_per_cta(cuda_lib):
+    # more than 1024 rows per CTA: labels past the shared-memory cache are read from global memory
+    N, V = 160_000, 64
+    x, y = _rand(N, V, wl.F32, seed=12, n_ignore=N // 10)
+    _check_fused(cuda_lib, x, y, V, wl.F32)
