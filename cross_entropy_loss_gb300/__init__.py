@@ -54,6 +54,7 @@ SIGNATURES = {
     "foak_test_fail_next_launches": (None, [_i32]),
     "foak_test_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "foak_test_skip_row_load": (None, [_i64]),
+    "foak_test_set_row_path": (None, [_i32]),
 }
 
 

@@ -29,10 +29,12 @@ int device_sm_count() {
 namespace {
 std::atomic<uint64_t> g_wait_limit_ns{4000000000ull};
 std::atomic<int64_t> g_skip_load_row{-1};
+std::atomic<int32_t> g_row_path{0};
 }  // namespace
 
 uint64_t test_wait_limit_ns() { return g_wait_limit_ns.load(); }
 int64_t test_skip_load_row() { return g_skip_load_row.load(); }
+int32_t test_row_path() { return g_row_path.load(); }
 
 namespace {
 
@@ -252,5 +254,7 @@ void foak_test_fail_next_launches(int32_t count) { g_fail_launches.store(count <
 void foak_test_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns == 0 ? 4000000000ull : ns); }
 
 void foak_test_skip_row_load(int64_t row) { g_skip_load_row.store(row < 0 ? -1 : row); }
+
+void foak_test_set_row_path(int32_t path) { g_row_path.store(path == 1 || path == 2 ? path : 0); }
 
 }  // extern "C"

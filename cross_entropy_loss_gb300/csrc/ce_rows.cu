@@ -25,240 +25,9 @@
 #include <mutex>
 #include <tuple>
 
-#include "common.cuh"
-#include "foak_ce.h"
-#include "internal.h"
+#include "row_common.cuh"
 
 namespace foak {
-
-// A CTA's slice of a row is at most 4096 16-byte vectors (64 KB), held in
-// registers as 8 vectors per thread (512 threads) or 4 (1024 threads).
-constexpr int kRowSliceVecMax = 4096;
-constexpr int kRowMaxStages = 4;
-constexpr int kRowMaxCluster = 8;
-constexpr int kMaxScalars = 7;                        // head or tail: < 16 bytes of bf16
-constexpr uint32_t kBulkChunk = 32768;
-constexpr int kLabCache = 1024;                       // labels of a CTA's first rows kept in smem
-constexpr size_t kSmemBudget = 227 * 1024 - 10 * 1024; // dynamic smem left after static use
-
-struct CeRowParams {
-    const char* x;
-    char* dx;
-    int64_t ld;
-    const int64_t* labels;
-    int64_t N, V, ignore_index;
-    float g, denom;
-    float* loss;
-    float* lse;
-    float* row_loss;
-    int32_t* n_valid;
-    int32_t* err;
-    CeWsHeader* ws;
-    const int64_t* count_labels;  // labels whose valid count is the denominator (the batch's)
-    int64_t count_N;
-    uint64_t wait_ns;        // limit of every shared-memory barrier wait
-    int64_t skip_load_row;   // test hook: this row's slice is never loaded (-1: none)
-    int k;               // CTAs per row (cluster size)
-    int per;             // vectors per CTA slice
-    int stages;          // rows in flight per CTA
-    uint32_t stage_bytes;
-};
-
-struct RowGeom {
-    int h;       // scalar head elements before the first 16-byte boundary
-    int64_t nb;  // 16-byte vectors
-    int t;       // scalar tail elements
-};
-
-template <int ES>
-__device__ __forceinline__ RowGeom row_geom(const char* rowp, int64_t V) {
-    constexpr int EPV = 16 / ES;
-    RowGeom g;
-    int h = static_cast<int>(((16u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(rowp)) & 15u)) & 15u) / ES);
-    if (h > V) h = static_cast<int>(V);
-    g.h = h;
-    g.nb = (V - h) / EPV;
-    g.t = static_cast<int>(V - h - g.nb * EPV);
-    return g;
-}
-
-template <int ES>
-__device__ __forceinline__ void unpack(const uint4& v, float (&f)[16 / ES]) {
-    if constexpr (ES == 2) {
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-        f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-    } else {
-        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
-        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
-    }
-}
-
-template <int ES>
-__device__ __forceinline__ uint4 pack(const float (&f)[16 / ES]) {
-    uint4 v;
-    if constexpr (ES == 2) {
-        v.x = pack_bf16x2(f[0], f[1]);
-        v.y = pack_bf16x2(f[2], f[3]);
-        v.z = pack_bf16x2(f[4], f[5]);
-        v.w = pack_bf16x2(f[6], f[7]);
-    } else {
-        v.x = __float_as_uint(f[0]); v.y = __float_as_uint(f[1]);
-        v.z = __float_as_uint(f[2]); v.w = __float_as_uint(f[3]);
-    }
-    return v;
-}
-
-template <int ES>
-__device__ __forceinline__ float load_scalar(const char* p) {
-    if constexpr (ES == 2) return bf16_lo(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)));
-    else return *reinterpret_cast<const float*>(p);
-}
-
-template <int ES>
-__device__ __forceinline__ void store_scalar(char* p, float v) {
-    if constexpr (ES == 2) *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
-    else *reinterpret_cast<float*>(p) = v;
-}
-
-// Per-thread arithmetic on the thread's slice (VPT 16-byte vectors).  Vectors
-// beyond the slice hold -inf, which no max picks and whose exp is 0, so the
-// loops run without predicates.
-template <int ES>
-struct RowMath;
-
-template <>
-struct RowMath<2> {  // bf16: 8 elements per vector, handled as 4 packed pairs
-    static __device__ __forceinline__ uint4 pad() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
-    template <int VPT>
-    static __device__ __forceinline__ float vmax(const uint4 (&v)[VPT]) {
-        uint32_t a = v[0].x, b = v[0].y, c = v[0].z, d = v[0].w;
-#pragma unroll
-        for (int i = 1; i < VPT; ++i) {
-            a = bf16x2_max(a, v[i].x);
-            b = bf16x2_max(b, v[i].y);
-            c = bf16x2_max(c, v[i].z);
-            d = bf16x2_max(d, v[i].w);
-        }
-        const uint32_t m = bf16x2_max(bf16x2_max(a, b), bf16x2_max(c, d));
-        return fmaxf(bf16_lo(m), bf16_hi(m));
-    }
-    // sum over the slice of 2^(x*log2e - mb)
-    template <int VPT>
-    static __device__ __forceinline__ float vsum(const uint4 (&v)[VPT], float mb) {
-        const f32x2_t L = f2_pack(kLog2e, kLog2e), C = f2_pack(-mb, -mb);
-        f32x2_t a = 0, b = 0, c = 0, d = 0;
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            a = f2_add(a, f2_ex2(f2_fma(bf16x2_to_f2(v[i].x), L, C)));
-            b = f2_add(b, f2_ex2(f2_fma(bf16x2_to_f2(v[i].y), L, C)));
-            c = f2_add(c, f2_ex2(f2_fma(bf16x2_to_f2(v[i].z), L, C)));
-            d = f2_add(d, f2_ex2(f2_fma(bf16x2_to_f2(v[i].w), L, C)));
-        }
-        float lo, hi;
-        f2_unpack(f2_add(f2_add(a, b), f2_add(c, d)), lo, hi);
-        return lo + hi;
-    }
-    // 2^(x*log2e - c) for every element, optionally times S
-    template <bool MUL>
-    static __device__ __forceinline__ uint4 vexp(const uint4& v, f32x2_t L, f32x2_t C, f32x2_t S) {
-        uint4 o;
-        f32x2_t t0 = f2_ex2(f2_fma(bf16x2_to_f2(v.x), L, C));
-        f32x2_t t1 = f2_ex2(f2_fma(bf16x2_to_f2(v.y), L, C));
-        f32x2_t t2 = f2_ex2(f2_fma(bf16x2_to_f2(v.z), L, C));
-        f32x2_t t3 = f2_ex2(f2_fma(bf16x2_to_f2(v.w), L, C));
-        if (MUL) {
-            t0 = f2_mul(t0, S);
-            t1 = f2_mul(t1, S);
-            t2 = f2_mul(t2, S);
-            t3 = f2_mul(t3, S);
-        }
-        o.x = f2_to_bf16x2(t0);
-        o.y = f2_to_bf16x2(t1);
-        o.z = f2_to_bf16x2(t2);
-        o.w = f2_to_bf16x2(t3);
-        return o;
-    }
-};
-
-template <>
-struct RowMath<4> {  // fp32: 4 elements per vector, 2 packed pairs
-    static __device__ __forceinline__ uint4 pad() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
-    template <int VPT>
-    static __device__ __forceinline__ float vmax(const uint4 (&v)[VPT]) {
-        float a = __uint_as_float(v[0].x), b = __uint_as_float(v[0].y);
-        float c = __uint_as_float(v[0].z), d = __uint_as_float(v[0].w);
-#pragma unroll
-        for (int i = 1; i < VPT; ++i) {
-            a = fmaxf(a, __uint_as_float(v[i].x));
-            b = fmaxf(b, __uint_as_float(v[i].y));
-            c = fmaxf(c, __uint_as_float(v[i].z));
-            d = fmaxf(d, __uint_as_float(v[i].w));
-        }
-        return fmaxf(fmaxf(a, b), fmaxf(c, d));
-    }
-    template <int VPT>
-    static __device__ __forceinline__ float vsum(const uint4 (&v)[VPT], float mb) {
-        const f32x2_t L = f2_pack(kLog2e, kLog2e), C = f2_pack(-mb, -mb);
-        f32x2_t a = 0, b = 0, c = 0, d = 0;
-#pragma unroll
-        for (int i = 0; i < VPT; i += 2) {
-            a = f2_add(a, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i].x), __uint_as_float(v[i].y)), L, C)));
-            b = f2_add(b, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i].z), __uint_as_float(v[i].w)), L, C)));
-            c = f2_add(c, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i + 1].x), __uint_as_float(v[i + 1].y)), L, C)));
-            d = f2_add(d, f2_ex2(f2_fma(f2_pack(__uint_as_float(v[i + 1].z), __uint_as_float(v[i + 1].w)), L, C)));
-        }
-        float lo, hi;
-        f2_unpack(f2_add(f2_add(a, b), f2_add(c, d)), lo, hi);
-        return lo + hi;
-    }
-    template <bool MUL>
-    static __device__ __forceinline__ uint4 vexp(const uint4& v, f32x2_t L, f32x2_t C, f32x2_t S) {
-        f32x2_t t0 = f2_ex2(f2_fma(f2_pack(__uint_as_float(v.x), __uint_as_float(v.y)), L, C));
-        f32x2_t t1 = f2_ex2(f2_fma(f2_pack(__uint_as_float(v.z), __uint_as_float(v.w)), L, C));
-        if (MUL) {
-            t0 = f2_mul(t0, S);
-            t1 = f2_mul(t1, S);
-        }
-        uint4 o;
-        float a, b;
-        f2_unpack(t0, a, b);
-        o.x = __float_as_uint(a);
-        o.y = __float_as_uint(b);
-        f2_unpack(t1, a, b);
-        o.z = __float_as_uint(a);
-        o.w = __float_as_uint(b);
-        return o;
-    }
-};
-
-// Element e (runtime index) of a vector, without dynamic register indexing.
-template <int ES>
-__device__ __forceinline__ float vec_elem(const uint4& v, int e) {
-    float f[16 / ES];
-    unpack<ES>(v, f);
-    float r = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16 / ES; ++k)
-        if (k == e) r = f[k];
-    return r;
-}
-
-// The label's vector: same values as the fast path, minus scale at element e.
-template <int ES>
-__device__ __forceinline__ uint4 vec_grad_label(const uint4& v, int e_own, float c, bool mul, float scale) {
-    constexpr int EPV = 16 / ES;
-    float f[EPV], d[EPV];
-    unpack<ES>(v, f);
-#pragma unroll
-    for (int k = 0; k < EPV; ++k) {
-        float q = ex2(fmaf(f[k], kLog2e, -c));
-        if (mul) q *= scale;
-        d[k] = k == e_own ? q - scale : q;
-    }
-    return pack<ES>(d);
-}
 
 template <int ES, bool GRAD, int THREADS>
 __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kernel(const CeRowParams p) {
@@ -351,6 +120,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     int c_st = 0;          // stage of the next valid row
     uint32_t c_par = 0;    // its phase parity
     uint32_t c_v = 0;      // valid rows consumed
+    uint32_t c_ok = 0;     // valid rows whose load was seen complete (a prefix)
     bool aborted = false;
     for (int64_t it = 0; it < n_it; ++it) {
         const int64_t row = cid + it * ncl;
@@ -391,7 +161,10 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
             c_par ^= 1u;
         }
         ++c_v;
-        if (!aborted && !mbar_wait_bounded(&bars[st], par, p.wait_ns)) s_abort = 1;
+        if (!aborted) {
+            if (mbar_wait_bounded(&bars[st], par, p.wait_ns)) c_ok = c_v;
+            else s_abort = 1;
+        }
 
         // Slice -> registers (vectors past the slice hold -inf); scalars from global memory.
         uint4 v[VPT];
@@ -523,45 +296,15 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
         if (rank == 0 && tid == 0 && p.lse && !aborted) p.lse[row] = lse;
     }
 
-    // Loads still in flight exist only after an abort; let them land first.
+    // Loads still in flight exist only after an abort: those issued past the
+    // last one seen complete may still be landing; let them land first.
     if (tid == 0) {
-        while (c_v < p_v) {
-            const int st = static_cast<int>(c_v % static_cast<uint32_t>(p.stages));
-            (void)mbar_wait_bounded(&bars[st], (c_v / static_cast<uint32_t>(p.stages)) & 1u, p.wait_ns);
-            ++c_v;
-        }
+        const uint32_t S = static_cast<uint32_t>(p.stages);
+        for (uint32_t k = c_ok; k < p_v; ++k) (void)mbar_wait_bounded(&bars[k % S], (k / S) & 1u, p.wait_ns);
     }
     if (K > 1) cluster_sync();  // no CTA leaves while a peer may still send it a pair
 
-    __syncthreads();
-    if (tid == 0) {
-        if (aborted) atomicOr(&p.ws->err, static_cast<unsigned>(FOAK_ERRBIT_TIMEOUT));
-        __threadfence();
-        const unsigned t = atomicAdd(&p.ws->done, 1u);
-        s_last = t == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!s_last) return;
-
-    // Last CTA: loss = (sum of row terms in row order, float64) / D.
-    __threadfence();
-    double acc = 0.0;
-    for (int64_t i = tid; i < p.N; i += kRowThreads) acc += static_cast<double>(__ldcg(p.row_loss + i));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off);
-    if (lane == 0) dred[warp] = acc;
-    __syncthreads();
-    if (tid == 0) {
-        double tot = 0.0;
-        for (int w = 0; w < kRowWarps; ++w) tot += dred[w];
-        const double Dd = p.denom > 0.f ? static_cast<double>(p.denom) : static_cast<double>(n_valid);
-        *p.loss = static_cast<float>(tot / Dd);
-        if (p.n_valid) *p.n_valid = n_valid;
-        unsigned e = atomicExch(&p.ws->err, 0u);
-        if (n_bad > 0) e |= FOAK_ERRBIT_LABEL_RANGE;
-        if (p.err) *p.err = static_cast<int32_t>(e);
-        atomicExch(&p.ws->done, 0u);
-    }
+    rows_finish<THREADS>(p, aborted, n_valid, n_bad, &s_last, dred);
 }
 
 // ------------------------------------------------------------------ host side
@@ -614,6 +357,11 @@ bool plan_rows(int ES, int64_t V, Plan* pl) {
         if (plan_with(ES, V, 256, 2048, kSmemBudgetHalf, &half)) *pl = half;
     }
     return true;
+}
+
+bool plan_needs_cluster(int ES, int64_t V) {
+    Plan one;
+    return !plan_with(ES, V, 512, kRowSliceVecMax, kSmemBudget, &one) || one.k > 1;
 }
 
 std::mutex g_mu;
@@ -730,6 +478,10 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
     prm.count_N = count_labels ? count_N : N;
     prm.wait_ns = test_wait_limit_ns();
     prm.skip_load_row = test_skip_load_row();
+    // Rows longer than one 512-thread CTA's slice are streamed twice by one CTA
+    // (every SM busy, no cluster exchange) unless the one-pass cluster kernel is asked for.
+    const int path = test_row_path();
+    if (path == 2 || (path == 0 && plan_needs_cluster(elem_bytes, V))) return launch_ce_rows_long(grad, elem_bytes, prm, stream);
     if (elem_bytes == 2)
         return grad ? launch_vpt<2, true>(prm, pl, stream) : launch_vpt<2, false>(prm, pl, stream);
     return grad ? launch_vpt<4, true>(prm, pl, stream) : launch_vpt<4, false>(prm, pl, stream);

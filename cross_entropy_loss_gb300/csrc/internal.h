@@ -54,6 +54,7 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
 // whose slice the row kernel's producer skips (so a wait is sure to run out).
 uint64_t test_wait_limit_ns();
 int64_t test_skip_load_row();
+int32_t test_row_path();  // 0 automatic, 1 one pass (clusters), 2 two-pass streaming
 
 // Streaming multiprocessor count of the current device (cached per device).
 int device_sm_count();

@@ -61,7 +61,7 @@ def test_fused_small_shapes(cuda_lib, dtype, N, V):
 @pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
 @pytest.mark.parametrize("N,V", [(6, 40000), (7, 70001), (5, 128256)])
 def test_fused_cluster_rows(cuda_lib, dtype, N, V):
-    # rows longer than one CTA's 64 KB slice are split over a cluster of 2-8 CTAs
+    # rows longer than one CTA's 64 KB slice: by default one CTA streams the row twice
     x, y = _rand(N, V, dtype, seed=200 + V, sigma=3.0, n_ignore=1, spikes=1e-4)
     _check_fused(cuda_lib, x, y, V, dtype)
 
