@@ -82,6 +82,15 @@ def _source_sha(*names):
     return h.hexdigest()[:16]
 
 
+def _row_kernel(cfg):
+    """The fused row kernel the library picks for this workload, and its source files:
+    rows of at most one 64 KB slice are swept once, longer rows streamed twice."""
+    es = 2 if cfg["dtype"] == wl.BF16 else 4
+    if cfg["V"] * es <= 65536:
+        return f"ce_rows_kernel<{es},true,512>", ("ce_rows.cu", "row_common.cuh", "common.cuh")
+    return f"ce_rows_long_kernel<{es},true>", ("ce_rows_long.cu", "row_common.cuh", "common.cuh")
+
+
 def _traffic(profile_name, sha):
     """Per-launch DRAM bytes from a committed ncu summary, if taken on this kernel source."""
     p = os.path.join(ROOT, "profiles", profile_name)
@@ -320,7 +329,8 @@ def run_ours(args, rank, world, dist):
     stated = _stated_bytes(main)
     peak, peak_src = _peak_hbm()
     achieved = algo / (ms * 1e-3) / 1e9
-    sha = _source_sha("ce_rows.cu", "common.cuh")
+    kernel, srcs = _row_kernel(main)
+    sha = _source_sha(*srcs)
     prof_name = f"ce_fused_{args.workload}.txt"
     res = {
         "metric": METRIC,
@@ -345,7 +355,7 @@ def run_ours(args, rank, world, dist):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": _traffic(prof_name, sha),
-                     "algorithmic_bytes_per_launch": algo, "kernel": "ce_rows_kernel<2,true>",
+                     "algorithmic_bytes_per_launch": algo, "kernel": kernel,
                      "kernel_source_sha": sha},
         "gpu_launches": args.steps,
     }
@@ -409,7 +419,8 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
         ms, loss, err, _ = fused_timing(cfg, k, w, False, use_dist=False)
         algo = _algo_bytes(cfg)
         gbs = algo / (ms * 1e-3) / 1e9
-        out.append({"path": "foak_ce_fwd_bwd", "workload": WORKLOAD_DESC[name], "steps": k, "ms_per_step": ms,
+        out.append({"path": "foak_ce_fwd_bwd", "kernel": _row_kernel(cfg)[0], "workload": WORKLOAD_DESC[name],
+                    "steps": k, "ms_per_step": ms,
                     "tokens_per_s": cfg["logits"].shape[0] / (ms * 1e-3), "GBps_algorithmic": gbs,
                     "GBps_stated_2NVs": _stated_bytes(cfg) / (ms * 1e-3) / 1e9, "frac": gbs / peak,
                     "peak": peak, "peak_source": peak_src, "loss": loss, "err": err})

@@ -1,7 +1,7 @@
 // Row-wise cross-entropy for rows longer than one CTA's 64 KB slice, without
-// clusters: one 512-thread CTA owns a whole row and streams it through a ring
-// of 64 KB shared-memory stages (one-dimensional bulk copies completing on
-// mbarriers) twice.
+// clusters: one CTA owns a whole row and streams it through a ring of
+// shared-memory stages (one-dimensional bulk copies completing on mbarriers)
+// twice.
 //
 //   pass 1  every thread folds its share of each chunk into a running
 //           (max, sum exp(x - max)) -- the max is kept per warp, so a chunk
@@ -10,6 +10,10 @@
 //   pass 2  (fused forward+backward) the same chunks are loaded again and
 //           (exp(x - lse) - onehot) * g / D is written over them with 16-byte
 //           streaming stores.
+//
+// Stages are handed back per warp: the last warp to take a chunk into its
+// registers refills the stage, so warps only meet at the one CTA barrier per
+// row that merges the (max, sum) pairs.
 //
 // A row is 250 KB (bf16) or 501 KB (fp32) at V = 128256; 152 CTAs hold about
 // 40 or 80 MB of rows between the two passes, well inside the 129 MB L2, so the
@@ -22,8 +26,9 @@
 // Description item 4: log-sum-exp first, then the gradient in place), with
 // the row split into chunks where the original holds it in one block.
 #include <algorithm>
-#include <mutex>
+#include <cstdlib>
 #include <map>
+#include <mutex>
 
 #include "row_common.cuh"
 
@@ -31,23 +36,22 @@ namespace foak {
 
 namespace {
 
-constexpr int kLongThreads = 512;
-constexpr int kLongWarps = kLongThreads / 32;
-constexpr int kLongVpt = 8;
-constexpr int kLongChunkVec = kLongThreads * kLongVpt;  // 4096 vectors = 64 KB
-constexpr int kLongChunkShift = 12;
-static_assert(kLongChunkVec == 1 << kLongChunkShift, "chunk is a power of two");
+constexpr int kLongMaxStages = 4;
 
 __device__ __forceinline__ bool label_valid(int64_t y, const CeRowParams& p) {
     return y != p.ignore_index && y >= 0 && y < p.V;
 }
 
-template <int ES, bool GRAD>
-__global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeRowParams p) {
-    constexpr int THREADS = kLongThreads, VPT = kLongVpt, WARPS = kLongWarps, EPV = 16 / ES;
+// THREADS threads x VPT 16-byte vectors per thread = one chunk (48 or 64 KB).
+template <int ES, bool GRAD, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowParams p) {
+    constexpr int WARPS = THREADS / 32, EPV = 16 / ES;
+    constexpr int CHUNK = THREADS * VPT;  // vectors per chunk
     constexpr int PASSES = GRAD ? 2 : 1;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t bars[kRowMaxStages];
+    __shared__ uint64_t full[kLongMaxStages];   // chunk landed (producer's expect_tx + bytes)
+    __shared__ unsigned s_rel[kLongMaxStages];  // warps that released each stage, cumulative
+    __shared__ unsigned s_iss[kLongMaxStages];  // loads issued into each stage
     __shared__ float2 red_ms[2][WARPS];
     __shared__ int64_t s_lab[kLabCache];
     __shared__ int iscratch[2 * WARPS];
@@ -58,10 +62,14 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
     const int64_t cid = blockIdx.x, ncl = gridDim.x;
     const int64_t n_it = p.N > cid ? (p.N - 1 - cid) / ncl + 1 : 0;
     const int64_t row_bytes = p.ld * ES;
-    const int S = p.stages;
+    const uint32_t S = static_cast<uint32_t>(p.stages);
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        for (uint32_t s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            s_rel[s] = 0;
+            s_iss[s] = 0;
+        }
         fence_mbar_init();
         s_abort = 0;
         s_last = 0;
@@ -72,55 +80,70 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
     auto label_of = [&](int64_t it) -> int64_t {
         return (lab_cached && it < kLabCache) ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
     };
+    bool aborted = false;
+    auto check_abort = [&]() {
+        if (!aborted && *reinterpret_cast<volatile int*>(&s_abort)) aborted = true;
+    };
 
-    // Producer (thread 0).  The load sequence is: for every valid row, its
-    // chunks for pass 1, then (fused) the same chunks again for pass 2.
-    int64_t p_it = -1;      // row iteration being loaded
+    // ---- producers.  The chunk sequence is: for every valid row, its chunks
+    // for pass 1, then (fused) the same chunks again for pass 2; chunk k goes to
+    // stage k % S.  Lane 0 of every warp walks this sequence S chunks ahead of
+    // its own consumption, and the warp that releases chunk k last (a shared
+    // counter per stage) issues chunk k + S into the freed stage: a stage is
+    // refilled as soon as the slowest warp holds its chunk, and no thread ever
+    // waits to issue.  Warp 0 issues the first S chunks.
+    int64_t p_it = -1;          // row iteration of the cursor's chunk
     int p_pass = 0, p_chunk = 0, p_nchunk = 0;
     const char* p_src = nullptr;
     int64_t p_nb = 0;
-    uint32_t p_v = 0;       // chunk loads issued (one stage each)
-    auto issue_next = [&]() {
-        while (true) {
-            const bool row_done = p_it < 0 || p_nchunk == 0 || (p_pass == PASSES - 1 && p_chunk == p_nchunk - 1);
-            if (row_done) {
-                int64_t it = p_it + 1;
-                while (it < n_it && !label_valid(label_of(it), p)) ++it;
-                p_it = it;
-                p_nchunk = 0;
-                if (it >= n_it) return;
-                const char* rowp = p.x + (cid + it * ncl) * row_bytes;
-                const RowGeom gm = row_geom<ES>(rowp, p.V);
-                p_src = rowp + static_cast<int64_t>(gm.h) * ES;
-                p_nb = gm.nb;
-                p_nchunk = static_cast<int>((gm.nb + kLongChunkVec - 1) >> kLongChunkShift);
-                p_pass = 0;
-                p_chunk = 0;
-                if (p_nchunk == 0) continue;  // scalars only: nothing to stream
-                if (p.skip_load_row == cid + it * ncl) {  // test hook: this stage never completes
-                    ++p_v;
-                    return;
-                }
-            } else if (p_chunk == p_nchunk - 1) {
+    bool p_has = false;         // the cursor is on a chunk
+    auto advance = [&]() {      // move the cursor to the next chunk
+        if (p_has && !(p_pass == PASSES - 1 && p_chunk == p_nchunk - 1)) {
+            if (p_chunk == p_nchunk - 1) {
                 ++p_pass;
                 p_chunk = 0;
             } else {
                 ++p_chunk;
             }
-            const int64_t c0 = static_cast<int64_t>(p_chunk) << kLongChunkShift;
-            const int64_t nl = std::min<int64_t>(kLongChunkVec, p_nb - c0);
-            const uint32_t bytes = static_cast<uint32_t>(nl) * 16u;
-            const int st = static_cast<int>(p_v % static_cast<uint32_t>(S));
-            ++p_v;
-            mbar_arrive_expect_tx(&bars[st], bytes);
-            unsigned char* dst = smem + static_cast<size_t>(st) * p.stage_bytes;
-            for (uint32_t off = 0; off < bytes; off += kBulkChunk)
-                bulk_g2s(dst + off, p_src + c0 * 16 + off, min(kBulkChunk, bytes - off), &bars[st]);
             return;
         }
+        p_has = false;
+        for (int64_t it = p_it + 1; it < n_it; ++it) {
+            if (!label_valid(label_of(it), p)) continue;
+            const char* rowp = p.x + (cid + it * ncl) * row_bytes;
+            const RowGeom gm = row_geom<ES>(rowp, p.V);
+            const int nch = static_cast<int>((gm.nb + CHUNK - 1) / CHUNK);
+            if (nch == 0) continue;  // scalars only: nothing to stream
+            p_it = it;
+            p_src = rowp + static_cast<int64_t>(gm.h) * ES;
+            p_nb = gm.nb;
+            p_nchunk = nch;
+            p_pass = 0;
+            p_chunk = 0;
+            p_has = true;
+            return;
+        }
+        p_it = n_it;
     };
-    if (tid == 0)
-        for (int s = 0; s < S; ++s) issue_next();
+    auto issue = [&](uint32_t st) {  // the cursor's chunk into stage st
+        // test hook: the first load of one row is never made, so its stage never completes
+        if (p_chunk == 0 && p_pass == 0 && p.skip_load_row == cid + p_it * ncl) return;
+        const int64_t c0 = static_cast<int64_t>(p_chunk) * CHUNK;
+        const uint32_t bytes = static_cast<uint32_t>(std::min<int64_t>(CHUNK, p_nb - c0)) * 16u;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&full[st], bytes);
+        unsigned char* dst = smem + static_cast<size_t>(st) * p.stage_bytes;
+        for (uint32_t off = 0; off < bytes; off += kBulkChunk)
+            bulk_g2s(dst + off, p_src + c0 * 16 + off, min(kBulkChunk, bytes - off), &full[st]);
+        ++s_iss[st];  // one issuer per stage at a time: the release protocol orders them
+    };
+    if (lane == 0) {
+        advance();
+        for (uint32_t k = 0; k < S && p_has; ++k) {
+            if (warp == 0) issue(k);
+            advance();
+        }
+    }
 
     int n_valid = 0, n_bad = 0;
     count_labels(p.count_labels, p.count_N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
@@ -134,20 +157,19 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
     const bool mul = !(scale > 0.f);
     const float log2_scale = mul ? 0.f : log2f(scale);
 
-    uint32_t c_v = 0;   // chunks consumed
-    uint32_t c_ok = 0;  // chunks whose load was seen complete (a prefix of the loads)
+    uint32_t c_v = 0;  // chunks consumed
     uint32_t n_rows = 0;
-    bool aborted = false;
     const uint4 pad = RowMath<ES>::pad();
 
-    // Wait for the next chunk and move it into registers (-inf past its end).
+    // Wait for the next chunk, move it into registers (-inf past its end) and
+    // release its stage; the last warp to release it refills it.
     auto take_chunk = [&](int nl, uint4 (&v)[VPT]) {
-        const int st = static_cast<int>(c_v % static_cast<uint32_t>(S));
-        const uint32_t par = (c_v / static_cast<uint32_t>(S)) & 1u;
+        const uint32_t n = c_v, st = n % S;
         ++c_v;
-        if (!aborted) {
-            if (mbar_wait_bounded(&bars[st], par, p.wait_ns)) c_ok = c_v;
-            else s_abort = 1;
+        check_abort();
+        if (!aborted && !mbar_wait_bounded(&full[st], (n / S) & 1u, p.wait_ns)) {
+            s_abort = 1;
+            aborted = true;
         }
         const uint4* sb = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(st) * p.stage_bytes);
 #pragma unroll
@@ -155,13 +177,16 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
             const int lv = tid + i * THREADS;
             v[i] = lv < nl ? sb[lv] : pad;
         }
-    };
-    // After every thread has its copy: pick up an abort, refill the freed stage.
-    auto release = [&]() {
-        if (s_abort) aborted = true;
-        if (tid == 0 && !aborted) {
-            fence_proxy_async_smem();
-            issue_next();
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();  // this warp's reads of the stage come before its release
+            const unsigned prior = atomicAdd(&s_rel[st], 1u);
+            if (prior % WARPS == WARPS - 1) {  // the last warp: every read is done
+                __threadfence_block();
+                check_abort();
+                if (p_has && !aborted) issue(st);
+            }
+            advance();  // the cursor stays S chunks ahead of consumption
         }
     };
 
@@ -170,7 +195,7 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
         const int64_t y = label_of(it);
         const char* rowp = p.x + row * row_bytes;
         const RowGeom gm = row_geom<ES>(rowp, p.V);
-        const int nchunk = static_cast<int>((gm.nb + kLongChunkVec - 1) >> kLongChunkShift);
+        const int nchunk = static_cast<int>((gm.nb + CHUNK - 1) / CHUNK);
         const bool has_head = tid == 0 && gm.h > 0;
         const bool has_tail = tid == 32 && gm.t > 0;  // another warp than the head's
         const int64_t tail_col = gm.h + gm.nb * EPV;
@@ -202,9 +227,9 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
         } else if (y < tail_col) {
             const int64_t ly = y - gm.h;
             const int64_t lvec = ly / EPV;
-            const int lv = static_cast<int>(lvec & (kLongChunkVec - 1));
-            if ((lv & (THREADS - 1)) == tid) {
-                own_chunk = static_cast<int>(lvec >> kLongChunkShift);
+            const int lv = static_cast<int>(lvec % CHUNK);
+            if (lv % THREADS == tid) {
+                own_chunk = static_cast<int>(lvec / CHUNK);
                 own_slot = lv / THREADS;
                 own_e = static_cast<int>(ly % EPV);
             }
@@ -235,14 +260,9 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
             }
         }
         for (int j = 0; j < nchunk; ++j) {
-            const int nl = static_cast<int>(std::min<int64_t>(kLongChunkVec, gm.nb - (static_cast<int64_t>(j) << kLongChunkShift)));
+            const int nl = static_cast<int>(std::min<int64_t>(CHUNK, gm.nb - static_cast<int64_t>(j) * CHUNK));
             uint4 v[VPT];
             take_chunk(nl, v);
-            const bool last = j == nchunk - 1;
-            if (!last) {
-                __syncthreads();
-                release();
-            }
             const float Mn = fmaxf(M, warp_max(RowMath<ES>::template vmax<VPT>(v)));
             if (Mn != M) s *= ex2((M - Mn) * kLog2e);
             M = Mn;
@@ -252,19 +272,13 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
                 for (int i = 0; i < VPT; ++i)
                     if (i == own_slot) x_y = vec_elem<ES>(v[i], own_e);
             }
-            if (last) {
-                const float sw = warp_sum(s);
-                if (lane == 0) red_ms[rb][warp] = make_float2(M, sw);
-                __syncthreads();
-                release();
-            }
         }
-        if (nchunk == 0) {
+        {
             const float sw = warp_sum(s);
             if (lane == 0) red_ms[rb][warp] = make_float2(M, sw);
-            __syncthreads();
-            if (s_abort) aborted = true;
         }
+        __syncthreads();
+        check_abort();
         const float2 pr = lane < WARPS ? red_ms[rb][lane] : make_float2(kNegInf, 0.f);
         const float Mr = warp_max(pr.x);
         const float Sr = warp_sum(pr.x == kNegInf ? 0.f : pr.y * ex2((pr.x - Mr) * kLog2e));
@@ -280,12 +294,10 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
             char* drow = p.dx + row * row_bytes;
             uint4* dv = reinterpret_cast<uint4*>(drow + static_cast<int64_t>(gm.h) * ES);
             for (int j = 0; j < nchunk; ++j) {
-                const int64_t cv0 = static_cast<int64_t>(j) << kLongChunkShift;
-                const int nl = static_cast<int>(std::min<int64_t>(kLongChunkVec, gm.nb - cv0));
+                const int64_t cv0 = static_cast<int64_t>(j) * CHUNK;
+                const int nl = static_cast<int>(std::min<int64_t>(CHUNK, gm.nb - cv0));
                 uint4 v[VPT];
                 take_chunk(nl, v);
-                __syncthreads();
-                release();
                 if (aborted) continue;
                 const int slot = j == own_chunk ? own_slot : -1;
                 uint4* dvc = dv + cv0;
@@ -323,10 +335,10 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
 
     // After an abort, loads issued past the last one seen complete may still be
     // landing in shared memory: wait for them (bounded) before the CTA exits.
+    __syncthreads();  // no warp issues any more
     if (tid == 0) {
-        for (uint32_t k = c_ok; k < p_v; ++k)
-            (void)mbar_wait_bounded(&bars[k % static_cast<uint32_t>(S)], (k / static_cast<uint32_t>(S)) & 1u,
-                                    p.wait_ns);
+        for (uint32_t st = 0; st < S; ++st)
+            if (s_iss[st] > 0) (void)mbar_wait_bounded(&full[st], (s_iss[st] - 1u) & 1u, p.wait_ns);
     }
     rows_finish<THREADS>(p, aborted, n_valid, n_bad, &s_last, dred);
 }
@@ -334,9 +346,9 @@ __global__ void __launch_bounds__(kLongThreads, 1) ce_rows_long_kernel(const CeR
 std::mutex g_long_mu;
 std::map<std::pair<int, const void*>, bool> g_long_attr;  // (device, kernel): smem limit raised
 
-template <int ES, bool GRAD>
+template <int ES, bool GRAD, int THREADS, int VPT>
 cudaError_t launch_long_typed(const CeRowParams& base, cudaStream_t stream) {
-    const void* kern = reinterpret_cast<const void*>(&ce_rows_long_kernel<ES, GRAD>);
+    const void* kern = reinterpret_cast<const void*>(&ce_rows_long_kernel<ES, GRAD, THREADS, VPT>);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -351,20 +363,31 @@ cudaError_t launch_long_typed(const CeRowParams& base, cudaStream_t stream) {
     }
     CeRowParams prm = base;
     prm.k = 1;
-    prm.per = kLongChunkVec;
-    prm.stage_bytes = kLongChunkVec * 16;
-    prm.stages = static_cast<int>(std::min<size_t>(kRowMaxStages, kSmemBudget / prm.stage_bytes));
+    prm.per = THREADS * VPT;
+    prm.stage_bytes = static_cast<uint32_t>(THREADS * VPT * 16);
+    prm.stages = static_cast<int>(std::min<size_t>(kLongMaxStages, kSmemBudget / prm.stage_bytes));
     const size_t smem = static_cast<size_t>(prm.stages) * prm.stage_bytes;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), base.N));
-    ce_rows_long_kernel<ES, GRAD><<<static_cast<unsigned>(grid), kLongThreads, smem, stream>>>(prm);
+    ce_rows_long_kernel<ES, GRAD, THREADS, VPT><<<static_cast<unsigned>(grid), THREADS, smem, stream>>>(prm);
     return cudaGetLastError();
+}
+
+template <int ES, bool GRAD>
+cudaError_t launch_long_shape(const CeRowParams& base, cudaStream_t stream) {
+    static const int threads = [] {
+        const char* e = std::getenv("FOAK_LONG_THREADS");  // tuning override: 512, 768 or 1024
+        return e ? std::atoi(e) : 0;
+    }();
+    if (threads == 768) return launch_long_typed<ES, GRAD, 768, 4>(base, stream);
+    if (threads == 1024) return launch_long_typed<ES, GRAD, 1024, 4>(base, stream);
+    return launch_long_typed<ES, GRAD, 512, 8>(base, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_ce_rows_long(bool grad, int elem_bytes, const CeRowParams& base, cudaStream_t stream) {
-    if (elem_bytes == 2) return grad ? launch_long_typed<2, true>(base, stream) : launch_long_typed<2, false>(base, stream);
-    return grad ? launch_long_typed<4, true>(base, stream) : launch_long_typed<4, false>(base, stream);
+    if (elem_bytes == 2) return grad ? launch_long_shape<2, true>(base, stream) : launch_long_shape<2, false>(base, stream);
+    return grad ? launch_long_shape<4, true>(base, stream) : launch_long_shape<4, false>(base, stream);
 }
 
 }  // namespace foak
