@@ -133,8 +133,16 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&full[st], bytes);
         unsigned char* dst = smem + static_cast<size_t>(st) * p.stage_bytes;
-        for (uint32_t off = 0; off < bytes; off += kBulkChunk)
-            bulk_g2s(dst + off, p_src + c0 * 16 + off, min(kBulkChunk, bytes - off), &full[st]);
+        const int hint = p.l2_hint;
+        if (hint == 0 || (hint == 2 && p_pass == 0)) {
+            for (uint32_t off = 0; off < bytes; off += kBulkChunk)
+                bulk_g2s(dst + off, p_src + c0 * 16 + off, min(kBulkChunk, bytes - off), &full[st]);
+        } else {
+            // pass 1 keeps the row in L2 for pass 2; pass 2 lets it go
+            const uint64_t pol = p_pass == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
+            for (uint32_t off = 0; off < bytes; off += kBulkChunk)
+                bulk_g2s_hint(dst + off, p_src + c0 * 16 + off, min(kBulkChunk, bytes - off), &full[st], pol);
+        }
         ++s_iss[st];  // one issuer per stage at a time: the release protocol orders them
     };
     if (lane == 0) {
@@ -219,26 +227,25 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
         const int rb = n_rows & 1u;  // red_ms is double-buffered by row parity
         ++n_rows;
 
-        // Where the label column lives: a scalar of the head or tail, or element
-        // own_e of vector own_slot of chunk own_chunk in this thread's registers.
-        int own_chunk = -1, own_slot = -1, own_e = 0, own_sc = -1;
+        // Who owns the label column: the thread holding the head or tail scalar it
+        // falls in, or the thread whose vector of chunk own_chunk contains it.  The
+        // owner reads x_y straight from memory (one 32-byte sector per row) and,
+        // after storing its vector, overwrites the label's gradient element.
+        int own_chunk = -1, own_sc = -1;
         if (y < gm.h) {
             if (tid == 0) own_sc = static_cast<int>(y);
         } else if (y < tail_col) {
             const int64_t ly = y - gm.h;
             const int64_t lvec = ly / EPV;
             const int lv = static_cast<int>(lvec % CHUNK);
-            if (lv % THREADS == tid) {
-                own_chunk = static_cast<int>(lvec / CHUNK);
-                own_slot = lv / THREADS;
-                own_e = static_cast<int>(ly % EPV);
-            }
+            if (lv % THREADS == tid) own_chunk = static_cast<int>(lvec / CHUNK);
         } else if (tid == 32) {
             own_sc = static_cast<int>(y - tail_col);
         }
 
         // ---- pass 1: running (max, sum) per thread, max shared by the warp
         float M = kNegInf, s = 0.f, x_y = 0.f;
+        if (own_chunk >= 0) x_y = load_scalar<ES>(rowp + y * ES);
         float xs[kMaxScalars];
         if (gm.h > 0 || gm.t > 0) {  // CTA-uniform
             float xm = kNegInf;
@@ -267,11 +274,6 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
             if (Mn != M) s *= ex2((M - Mn) * kLog2e);
             M = Mn;
             s += RowMath<ES>::template vsum<VPT>(v, M == kNegInf ? 0.f : M * kLog2e);
-            if (j == own_chunk) {
-#pragma unroll
-                for (int i = 0; i < VPT; ++i)
-                    if (i == own_slot) x_y = vec_elem<ES>(v[i], own_e);
-            }
         }
         {
             const float sw = warp_sum(s);
@@ -299,24 +301,26 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
                 uint4 v[VPT];
                 take_chunk(nl, v);
                 if (aborted) continue;
-                const int slot = j == own_chunk ? own_slot : -1;
                 uint4* dvc = dv + cv0;
                 if (!mul) {
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         const int lv = tid + i * THREADS;
-                        uint4 o = RowMath<ES>::template vexp<false>(v[i], L2, C2, S2);
-                        if (i == slot) o = vec_grad_label<ES>(v[i], own_e, c, false, scale);
+                        const uint4 o = RowMath<ES>::template vexp<false>(v[i], L2, C2, S2);
                         if (lv < nl) st_global_cs_v4(dvc + lv, o);
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         const int lv = tid + i * THREADS;
-                        uint4 o = RowMath<ES>::template vexp<true>(v[i], L2, C2, S2);
-                        if (i == slot) o = vec_grad_label<ES>(v[i], own_e, c, true, scale);
+                        const uint4 o = RowMath<ES>::template vexp<true>(v[i], L2, C2, S2);
                         if (lv < nl) st_global_cs_v4(dvc + lv, o);
                     }
+                }
+                if (j == own_chunk) {  // after this thread's own store of that vector
+                    float d = ex2(fmaf(x_y, kLog2e, -c));
+                    if (mul) d *= scale;
+                    store_scalar<ES>(drow + y * ES, d - scale);
                 }
             }
             if (ns > 0 && !aborted) {
@@ -361,13 +365,21 @@ cudaError_t launch_long_typed(const CeRowParams& base, cudaStream_t stream) {
             set = true;
         }
     }
+    static const int forced_hint = [] {
+        const char* e = std::getenv("FOAK_LONG_L2HINT");  // tuning override: 0, 1 or 2
+        return e ? std::atoi(e) : -1;
+    }();
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), base.N));
+    // Rows held between the two passes: one per CTA.  Past half the 129 MB L2 the
+    // second pass reads with evict_first, so the rows still waiting for it stay.
+    const double in_flight = static_cast<double>(grid) * static_cast<double>(base.V) * ES;
     CeRowParams prm = base;
+    prm.l2_hint = forced_hint >= 0 ? forced_hint : (in_flight > 64.0 * (1 << 20) ? 2 : 0);
     prm.k = 1;
     prm.per = THREADS * VPT;
     prm.stage_bytes = static_cast<uint32_t>(THREADS * VPT * 16);
     prm.stages = static_cast<int>(std::min<size_t>(kLongMaxStages, kSmemBudget / prm.stage_bytes));
     const size_t smem = static_cast<size_t>(prm.stages) * prm.stage_bytes;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), base.N));
     ce_rows_long_kernel<ES, GRAD, THREADS, VPT><<<static_cast<unsigned>(grid), THREADS, smem, stream>>>(prm);
     return cudaGetLastError();
 }

@@ -36,6 +36,7 @@ struct CeRowParams {
     int64_t count_N;
     uint64_t wait_ns;        // limit of every shared-memory barrier wait
     int64_t skip_load_row;   // test hook: this row's slice is never loaded (-1: none)
+    int l2_hint;             // two-pass kernel: 0 none, 1 pass 1 evict_last + pass 2 evict_first, 2 pass 2 evict_first
     int k;               // CTAs per row (cluster size)
     int per;             // vectors per CTA slice
     int stages;          // rows in flight per CTA
