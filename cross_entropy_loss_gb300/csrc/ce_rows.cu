@@ -29,7 +29,10 @@
 
 namespace foak {
 
-template <int ES, bool GRAD, int THREADS>
+// AL: every row starts on a 16-byte boundary and V * ES is a multiple of 16, so
+// rows have no scalar head or tail and every row's slice has the same length;
+// the stage slots past it are filled with -inf once and loaded unconditionally.
+template <int ES, bool GRAD, int THREADS, bool AL>
 __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kernel(const CeRowParams p) {
     // slice: 512 x 8 or 1024 x 4 vectors (64 KB, one CTA per SM) or 256 x 8 (32 KB, two CTAs per SM)
     constexpr int VPT = THREADS == 256 ? 8 : kRowSliceVecMax / THREADS;
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
                 return;
             }
             const char* rowp = p.x + row * row_bytes;
-            const RowGeom gm = row_geom<ES>(rowp, p.V);
+            const RowGeom gm = AL ? RowGeom{0, p.V / EPV, 0} : row_geom<ES>(rowp, p.V);
             int64_t nl = gm.nb - v0;
             nl = nl < 0 ? 0 : (nl > p.per ? p.per : nl);
             const uint32_t bytes = static_cast<uint32_t>(nl) * 16u;
@@ -109,6 +112,16 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     const float scale = p.g / D;
     // Labels of this CTA's first rows, for the row loop and the producer.
     for (int64_t it = tid; it < n_it && it < kLabCache; it += blockDim.x) s_lab[it] = __ldg(p.labels + cid + it * ncl);
+    if constexpr (AL) {
+        // -inf in every stage slot past this CTA's slice (the copies never write there)
+        int64_t nl0 = p.V / EPV - v0;
+        nl0 = nl0 < 0 ? 0 : (nl0 > p.per ? p.per : nl0);
+        const uint4 pad = RowMath<ES>::pad();
+        for (int s = 0; s < p.stages; ++s) {
+            uint4* sb = reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
+            for (int i = static_cast<int>(nl0) + tid; i < VPT * kRowThreads; i += kRowThreads) sb[i] = pad;
+        }
+    }
     __syncthreads();
     lab_cached = true;
 
@@ -127,7 +140,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
         const int64_t y = label_of(it);
         const bool valid = y != p.ignore_index && y >= 0 && y < p.V;
         const char* rowp = p.x + row * row_bytes;
-        const RowGeom gm = row_geom<ES>(rowp, p.V);
+        const RowGeom gm = AL ? RowGeom{0, p.V / EPV, 0} : row_geom<ES>(rowp, p.V);
         int nl;
         {
             const int64_t t = gm.nb - v0;
@@ -154,6 +167,24 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
             continue;
         }
 
+        // Who owns the label column: the thread holding the head or tail scalar it
+        // falls in, or the thread whose vector contains it (no division: kRowThreads
+        // is a power of 2).  A vector owner reads x_y from memory now, so the load
+        // overlaps the row's wait and arithmetic, and later patches the label's
+        // gradient element with a scalar store: no per-vector label work.
+        bool own_vec = false;
+        int own_sc = -1;
+        if (y < gm.h) {
+            if (rank == 0 && tid == 0) own_sc = static_cast<int>(y);
+        } else if (y < tail_col) {
+            const int64_t lv = (y - gm.h) / EPV - v0;
+            own_vec = lv >= 0 && lv < p.per && (static_cast<int>(lv) & (kRowThreads - 1)) == tid;
+        } else if (rank == K - 1 && tid == tail_tid) {
+            own_sc = static_cast<int>(y - tail_col);
+        }
+        float x_y = 0.f;
+        if (own_vec) x_y = load_scalar<ES>(rowp + y * ES);
+
         const int st = c_st;
         const uint32_t par = c_par;
         if (++c_st == p.stages) {
@@ -173,7 +204,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int lv = tid + i * kRowThreads;
-            v[i] = lv < nl ? sb[lv] : pad;
+            v[i] = (AL || lv < nl) ? sb[lv] : pad;
         }
         float xs[kMaxScalars];
         float m = RowMath<ES>::template vmax<VPT>(v);
@@ -231,31 +262,12 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
         const float lse2 = fmaf(M, kLog2e, lg2(S));  // log-sum-exp in base 2
         const float lse = lse2 * kLn2;
 
-        // Which thread holds the label column (no division: kRowThreads is a power of 2).
-        int own_slot = -1, own_e = 0, own_sc = -1;
-        if (y < gm.h) {
-            if (rank == 0 && tid == 0) own_sc = static_cast<int>(y);
-        } else if (y < tail_col) {
-            const int64_t ly = y - gm.h;
-            const int64_t lv = ly / EPV - v0;
-            if (lv >= 0 && lv < p.per && (static_cast<int>(lv) & (kRowThreads - 1)) == tid) {
-                own_slot = static_cast<int>(lv) / kRowThreads;
-                own_e = static_cast<int>(ly % EPV);
-            }
-        } else if (rank == K - 1 && tid == tail_tid) {
-            own_sc = static_cast<int>(y - tail_col);
-        }
-        const bool owner = own_slot >= 0 || own_sc >= 0;
-        if (owner) {
-            float x_y = 0.f;
-#pragma unroll
-            for (int i = 0; i < VPT; ++i)
-                if (i == own_slot) x_y = vec_elem<ES>(v[i], own_e);
+        if (own_sc >= 0) {
 #pragma unroll
             for (int s = 0; s < kMaxScalars; ++s)
                 if (s == own_sc) x_y = xs[s];
-            if (!aborted) p.row_loss[row] = lse - x_y;
         }
+        if ((own_vec || own_sc >= 0) && !aborted) p.row_loss[row] = lse - x_y;
 
         if constexpr (GRAD) {
             const float c = lse2 - log2_scale;
@@ -267,18 +279,21 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         const int lv = tid + i * kRowThreads;
-                        uint4 o = RowMath<ES>::template vexp<false>(v[i], L2, C2, S2);
-                        if (i == own_slot) o = vec_grad_label<ES>(v[i], own_e, c, false, scale);
+                        const uint4 o = RowMath<ES>::template vexp<false>(v[i], L2, C2, S2);
                         if (lv < nl) st_global_cs_v4(dv + lv, o);
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         const int lv = tid + i * kRowThreads;
-                        uint4 o = RowMath<ES>::template vexp<true>(v[i], L2, C2, S2);
-                        if (i == own_slot) o = vec_grad_label<ES>(v[i], own_e, c, true, scale);
+                        const uint4 o = RowMath<ES>::template vexp<true>(v[i], L2, C2, S2);
                         if (lv < nl) st_global_cs_v4(dv + lv, o);
                     }
+                }
+                if (own_vec) {  // the label's element, after this thread's store of its vector
+                    float d = ex2(fmaf(x_y, kLog2e, -c));
+                    if (mul) d *= scale;
+                    store_scalar<ES>(drow + y * ES, d - scale);
                 }
                 if (ns > 0) {
 #pragma unroll
@@ -415,9 +430,9 @@ cudaError_t resident_clusters(const void* kern, int threads, int k, size_t smem,
     return cudaSuccess;
 }
 
-template <int ES, bool GRAD, int THREADS>
+template <int ES, bool GRAD, int THREADS, bool AL>
 cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t stream) {
-    const void* kern = reinterpret_cast<const void*>(&ce_rows_kernel<ES, GRAD, THREADS>);
+    const void* kern = reinterpret_cast<const void*>(&ce_rows_kernel<ES, GRAD, THREADS, AL>);
     int ncl = 0;
     cudaError_t e = resident_clusters(kern, THREADS, pl.k, pl.smem, &ncl);
     if (e != cudaSuccess) return e;
@@ -439,14 +454,30 @@ cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t s
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ce_rows_kernel<ES, GRAD, THREADS>, prm);
+    return cudaLaunchKernelEx(&cfg, ce_rows_kernel<ES, GRAD, THREADS, AL>, prm);
 }
 
+// Aligned rows on one CTA each take the AL kernel, whose stages hold a full
+// slice (THREADS x VPT vectors) so the pad slots exist.
 template <int ES, bool GRAD>
-cudaError_t launch_vpt(const CeRowParams& base, const Plan& pl, cudaStream_t stream) {
-    if (pl.threads == 256) return launch_typed<ES, GRAD, 256>(base, pl, stream);
-    return pl.threads == 1024 ? launch_typed<ES, GRAD, 1024>(base, pl, stream)
-                              : launch_typed<ES, GRAD, 512>(base, pl, stream);
+cudaError_t launch_vpt(const CeRowParams& base, const Plan& pl, cudaStream_t stream, bool aligned) {
+    if (pl.threads == 256) return launch_typed<ES, GRAD, 256, false>(base, pl, stream);
+    if (aligned && pl.k == 1) {
+        // 512 x 8 by default; 1024 x 4 (64 registers) as a tuning override
+        static const int forced = [] {
+            const char* e = std::getenv("FOAK_ROW_THREADS");
+            return e ? std::atoi(e) : 0;
+        }();
+        const int threads = forced == 1024 ? 1024 : 512;
+        Plan full = pl;
+        full.stage_bytes = kRowSliceVecMax * 16;
+        full.stages = static_cast<int>(std::min<size_t>(kRowMaxStages, kSmemBudget / full.stage_bytes));
+        full.smem = static_cast<size_t>(full.stages) * full.stage_bytes;
+        return threads == 1024 ? launch_typed<ES, GRAD, 1024, true>(base, full, stream)
+                               : launch_typed<ES, GRAD, 512, true>(base, full, stream);
+    }
+    return pl.threads == 1024 ? launch_typed<ES, GRAD, 1024, false>(base, pl, stream)
+                              : launch_typed<ES, GRAD, 512, false>(base, pl, stream);
 }
 
 }  // namespace
@@ -482,9 +513,12 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
     // (every SM busy, no cluster exchange) unless the one-pass cluster kernel is asked for.
     const int path = test_row_path();
     if (path == 2 || (path == 0 && plan_needs_cluster(elem_bytes, V))) return launch_ce_rows_long(grad, elem_bytes, prm, stream);
+    // Aligned: every row (base + i * ld elements) starts on 16 bytes and ends on a vector.
+    const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld * elem_bytes) % 16 == 0 &&
+                         (V * elem_bytes) % 16 == 0 && (dx == x || dx == nullptr || !grad);
     if (elem_bytes == 2)
-        return grad ? launch_vpt<2, true>(prm, pl, stream) : launch_vpt<2, false>(prm, pl, stream);
-    return grad ? launch_vpt<4, true>(prm, pl, stream) : launch_vpt<4, false>(prm, pl, stream);
+        return grad ? launch_vpt<2, true>(prm, pl, stream, aligned) : launch_vpt<2, false>(prm, pl, stream, aligned);
+    return grad ? launch_vpt<4, true>(prm, pl, stream, aligned) : launch_vpt<4, false>(prm, pl, stream, aligned);
 }
 
 }  // namespace foak
