@@ -87,8 +87,9 @@ def _row_kernel(cfg):
     rows of at most one 64 KB slice are swept once, longer rows streamed twice."""
     es = 2 if cfg["dtype"] == wl.BF16 else 4
     if cfg["V"] * es <= 65536:
-        return f"ce_rows_kernel<{es},true,512>", ("ce_rows.cu", "row_common.cuh", "common.cuh")
-    return f"ce_rows_long_kernel<{es},true>", ("ce_rows_long.cu", "row_common.cuh", "common.cuh")
+        aligned = "true" if cfg["V"] * es % 16 == 0 else "false"  # dense rows, 256-byte aligned base
+        return f"ce_rows_kernel<{es},true,512,{aligned}>", ("ce_rows.cu", "row_common.cuh", "common.cuh")
+    return f"ce_rows_long_kernel<{es},true,512,8>", ("ce_rows_long.cu", "row_common.cuh", "common.cuh")
 
 
 def _traffic(profile_name, sha):
