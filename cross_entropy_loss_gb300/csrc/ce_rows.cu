@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
         // Row (max, sum): the thread's sum is taken relative to its warp's max, the
         // warp's pair is published, and one barrier per row (which also frees the
         // stage for the producer) lets every warp merge the CTA's pairs.
-        m = warp_max(m);
+        m = GRAD ? warp_max(m) : warp_max_redux(m);  // measured: shuffles for the fused kernel
         const float mb = m == kNegInf ? 0.f : m * kLog2e;
         float sum = RowMath<ES>::template vsum<VPT>(v, mb);
         if (ns > 0) {
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
             issue_next();
         }
         const float2 pr = lane < kRowWarps ? red_ms[rb][lane] : make_float2(kNegInf, 0.f);
-        float M = warp_max(pr.x);
+        float M = GRAD ? warp_max(pr.x) : warp_max_redux(pr.x);
         float S = warp_sum(pr.x == kNegInf ? 0.f : pr.y * ex2((pr.x - M) * kLog2e));
         if (K > 1) {
             // cluster: thread 0 sends this CTA's pair to every CTA of the cluster with

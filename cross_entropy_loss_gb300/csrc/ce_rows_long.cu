@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
                     xm = fmaxf(xm, xs[q]);
                 }
             }
-            M = warp_max(xm);
+            M = warp_max_redux(xm);
             if (ns > 0) {
                 const float mb = M == kNegInf ? 0.f : M * kLog2e;
 #pragma unroll
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
             const int nl = static_cast<int>(std::min<int64_t>(CHUNK, gm.nb - static_cast<int64_t>(j) * CHUNK));
             uint4 v[VPT];
             take_chunk(nl, v);
-            const float Mn = fmaxf(M, warp_max(RowMath<ES>::template vmax<VPT>(v)));
+            const float Mn = fmaxf(M, warp_max_redux(RowMath<ES>::template vmax<VPT>(v)));
             if (Mn != M) s *= ex2((M - Mn) * kLog2e);
             M = Mn;
             s += RowMath<ES>::template vsum<VPT>(v, M == kNegInf ? 0.f : M * kLog2e);
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
         __syncthreads();
         check_abort();
         const float2 pr = lane < WARPS ? red_ms[rb][lane] : make_float2(kNegInf, 0.f);
-        const float Mr = warp_max(pr.x);
+        const float Mr = warp_max_redux(pr.x);
         const float Sr = warp_sum(pr.x == kNegInf ? 0.f : pr.y * ex2((pr.x - Mr) * kLog2e));
         const float lse2 = fmaf(Mr, kLog2e, lg2(Sr));  // log-sum-exp in base 2
         const float lse = lse2 * kLn2;

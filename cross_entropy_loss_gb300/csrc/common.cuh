@@ -265,6 +265,15 @@ __device__ __forceinline__ float warp_max(float v) {
     for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
 }
+// The same max in one warp-wide reduction instruction (redux.sync on f32, an
+// sm_100-family feature) instead of five dependent shuffles: shorter latency,
+// which pays off where the row's reduction chain is the critical path (the
+// forward sweep, the two-pass kernel); all 32 lanes must be converged.
+__device__ __forceinline__ float warp_max_redux(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
