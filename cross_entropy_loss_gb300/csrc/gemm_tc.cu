@@ -1,8 +1,12 @@
 // Persistent bf16 GEMM on the fifth-generation tensor cores (tcgen05) for the
 // chunked linear + cross-entropy:  C (+)= A * B^T  with fp32 accumulation.
 //
-// One CTA per SM walks output tiles of 128 x 256 (M fastest, so neighbouring CTAs
-// share the B tile in L2).  Warp roles:
+// One CTA per SM walks output tiles of 128 x 256.  The walk runs along the
+// shorter tile dimension first (M fastest when there are fewer M tiles than N
+// tiles, else N fastest), so the CTAs working at once share a few tiles of the
+// operand with many tiles and every operand tile is fetched from HBM about once:
+// for dW (250 x 16 tiles) an M-fastest walk re-read the 131 MB dZ operand once
+// per N tile.  Warp roles:
 //   warp 0     TMA producer: 2-D tiled loads (128-byte swizzle) of the A and B
 //              k-blocks (64 deep) into a 4-stage shared-memory ring;
 //   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
@@ -47,11 +51,15 @@ struct GemmParams {
     int a_mn, b_mn;
     int mode;
     int tiles_m, tiles_n;
+    int n_fast;  // tile walk: N index fastest (else M)
     uint32_t idesc;
     void* out;
     int64_t ldo;
     int32_t* err;
 };
+
+__device__ __forceinline__ int tile_m(const GemmParams& p, int t) { return p.n_fast ? t / p.tiles_n : t % p.tiles_m; }
+__device__ __forceinline__ int tile_n(const GemmParams& p, int t) { return p.n_fast ? t % p.tiles_n : t / p.tiles_m; }
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -96,7 +104,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
             int stage = 0;
             uint32_t phase = 0;
             for (int t = blockIdx.x; t < num_tiles && !abort_sh; t += gridDim.x) {
-                const int m0 = (t % p.tiles_m) * kBM, n0 = (t / p.tiles_m) * kBN;
+                const int m0 = tile_m(p, t) * kBM, n0 = tile_n(p, t) * kBN;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) { give_up(); break; }
                     if (abort_sh) break;
@@ -171,7 +179,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 break;
             }
             tc_fence_after();
-            const int m0 = (t % p.tiles_m) * kBM, n0 = (t / p.tiles_m) * kBN;
+            const int m0 = tile_m(p, t) * kBM, n0 = tile_n(p, t) * kBN;
             const int row_blk = m0 + q * 32;  // first row of this warp's 32
             const int row = row_blk + lane;
 #pragma unroll 1
@@ -310,6 +318,7 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     p.mode = d.mode;
     p.tiles_m = (d.M + kBM - 1) / kBM;
     p.tiles_n = (d.N + kBN - 1) / kBN;
+    p.n_fast = p.tiles_m > p.tiles_n ? 1 : 0;
     p.idesc = idesc_bf16_f32(kBM, kBN, p.a_mn, p.b_mn);
     p.out = d.out;
     p.ldo = d.ldo;
