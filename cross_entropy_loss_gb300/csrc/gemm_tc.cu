@@ -182,11 +182,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
             const int m0 = tile_m(p, t) * kBM, n0 = tile_n(p, t) * kBN;
             const int row_blk = m0 + q * 32;  // first row of this warp's 32
             const int row = row_blk + lane;
-#pragma unroll 1
+            // TMEM -> registers one 32-column chunk ahead: chunk c + 1 is loading while
+            // chunk c is converted and stored (two register sets, loop unrolled)
+            const uint32_t taddr = tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+            uint32_t ra[32], rb[32];
+            tc_ld32(taddr, ra);
+#pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t r[32];
-                tc_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN + c * 32), r);
-                tc_wait_ld();
+                uint32_t(&r)[32] = (c & 1) ? rb : ra;
+                uint32_t(&rn)[32] = (c & 1) ? ra : rb;
+                tc_wait_ld(r);
+                if (c + 1 < kBN / 32) tc_ld32(taddr + static_cast<uint32_t>((c + 1) * 32), rn);
                 const int col0 = n0 + c * 32;
                 if (col0 >= p.N) continue;
                 const bool full_chunk = col0 + 32 <= p.N;
