@@ -77,7 +77,50 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     auto label_of = [&](int64_t it) -> int64_t {
         return (lab_cached && it < kLabCache) ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
     };
-    auto issue_next = [&]() {
+    // Fused kernel: the next load is found (label scan, address, size) before
+    // the row's barrier and only issued after it, so thread 0's warp leaves the
+    // barrier with little extra work and does not hold up the next one.
+    const char* q_src = nullptr;
+    uint32_t q_bytes = 0;
+    int q_state = 0;  // 0 nothing prepared, 1 a load, 2 a skipped load (test hook), 3 no rows left
+    auto prepare = [&]() {
+        if (q_state != 0) return;
+        while (p_it < n_it) {
+            const int64_t row = cid + p_it * ncl;
+            const int64_t y = label_of(p_it);
+            ++p_it;
+            if (y == p.ignore_index || y < 0 || y >= p.V) continue;
+            if (row == p.skip_load_row) {  // test hook: the stage's barrier is never completed
+                q_state = 2;
+                return;
+            }
+            const char* rowp = p.x + row * row_bytes;
+            const RowGeom gm = AL ? RowGeom{0, p.V / EPV, 0} : row_geom<ES>(rowp, p.V);
+            int64_t nl = gm.nb - v0;
+            nl = nl < 0 ? 0 : (nl > p.per ? p.per : nl);
+            q_bytes = static_cast<uint32_t>(nl) * 16u;
+            q_src = rowp + static_cast<int64_t>(gm.h) * ES + v0 * 16;
+            q_state = 1;
+            return;
+        }
+        q_state = 3;
+    };
+    auto fire = [&]() {
+        if (q_state == 1) {
+            const int st = static_cast<int>(p_v % static_cast<uint32_t>(p.stages));
+            uint64_t* bar = &bars[st];
+            mbar_arrive_expect_tx(bar, q_bytes);
+            unsigned char* dst = smem + static_cast<size_t>(st) * p.stage_bytes;
+            for (uint32_t off = 0; off < q_bytes; off += kBulkChunk)
+                bulk_g2s(dst + off, q_src + off, min(kBulkChunk, q_bytes - off), bar);
+        }
+        if (q_state == 1 || q_state == 2) {
+            ++p_v;
+            q_state = 0;
+        }
+    };
+    // Forward kernel: find and issue in one go after the barrier (measured faster there).
+    auto issue_direct = [&]() {
         while (p_it < n_it) {
             const int64_t row = cid + p_it * ncl;
             const int64_t y = label_of(p_it);
@@ -101,6 +144,14 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
             for (uint32_t off = 0; off < bytes; off += kBulkChunk)
                 bulk_g2s(dst + off, src + off, min(kBulkChunk, bytes - off), bar);
             return;
+        }
+    };
+    auto issue_next = [&]() {
+        if constexpr (GRAD) {
+            prepare();
+            fire();
+        } else {
+            issue_direct();
         }
     };
     if (tid == 0)
@@ -206,6 +257,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
             const int lv = tid + i * kRowThreads;
             v[i] = (AL || lv < nl) ? sb[lv] : pad;
         }
+        if (GRAD && tid == 0 && !aborted) prepare();  // measured: the forward sweep runs faster without
         float xs[kMaxScalars];
         float m = RowMath<ES>::template vmax<VPT>(v);
         if (ns > 0) {
@@ -234,7 +286,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
         if (s_abort) aborted = true;
         if (tid == 0 && !aborted) {
             fence_proxy_async_smem();
-            issue_next();
+            issue_next();  // fused: only fires what was prepared before the barrier
         }
         const float2 pr = lane < kRowWarps ? red_ms[rb][lane] : make_float2(kNegInf, 0.f);
         float M = GRAD ? warp_max(pr.x) : warp_max_redux(pr.x);
