@@ -43,6 +43,9 @@ SIGNATURES = {
     "foak_ce_forward": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                _vp]),
     "foak_ce_backward": (_i32, [_vp, _vp, _i32, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp]),
+    "foak_ce_host_workspace_size": (_sz, [_i64]),
+    "foak_ce_fwd_bwd_host": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _sz, _vp]),
     "foak_ce_fwd_bwd": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _sz,
                                _vp]),
     "foak_ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
@@ -214,6 +217,47 @@ def foak_ce_fwd_bwd(logits, labels, *, g: float = 1.0, ignore_index: int = -100,
                              _stream(dev, stream))
     _check(st, "foak_ce_fwd_bwd")
     return dict(loss=loss, n_valid=n_valid, err=err, lse=lse)
+
+
+def foak_ce_host_workspace_size(N: int) -> int:
+    return int(lib.foak_ce_host_workspace_size(int(N)))
+
+
+def foak_ce_fwd_bwd_host(host_logits, host_labels, dev_logits, dev_labels, *, g: float = 1.0,
+                         ignore_index: int = -100, denom: float = 0.0, workspace_tensor=None, out=None, stream=None):
+    """Fused forward + backward on HOST logits: the call copies labels and logits to
+    ``dev_logits`` / ``dev_labels`` in row chunks and sweeps each chunk as it lands;
+    ``dev_logits`` ends holding dlogits.
+
+    ``host_logits`` is a CPU bf16/fp32 tensor (pinned for a full-speed copy) with
+    the shape and row stride of ``dev_logits``; ``host_labels`` a CPU int64 tensor.
+    Returns dict(loss, n_valid, err) of pinned host tensors (pass ``out`` to reuse
+    them), valid once the stream has been synchronised.
+    """
+    N, V, ld, dt = _logits_args(dev_logits)
+    dev = dev_logits.device
+    if host_logits.is_cuda or host_logits.dtype != dev_logits.dtype or host_logits.dim() != 2:
+        raise ValueError("host_logits must be a CPU tensor of the device logits' dtype")
+    if tuple(host_logits.shape) != (N, V) or host_logits.stride(1) != 1 or (N > 1 and host_logits.stride(0) != ld):
+        raise ValueError("host_logits must have the shape and row stride of dev_logits")
+    if host_labels.is_cuda or host_labels.dtype != torch.int64 or host_labels.numel() != N:
+        raise ValueError("host_labels must be a CPU int64 tensor of N labels")
+    if not host_labels.is_contiguous():
+        raise ValueError("host_labels must be contiguous")
+    dev_labels = _labels_arg(dev_labels, N, dev)
+    if out is None:
+        out = dict(loss=torch.empty(1, dtype=torch.float32).pin_memory(),
+                   n_valid=torch.empty(1, dtype=torch.int32).pin_memory(),
+                   err=torch.empty(1, dtype=torch.int32).pin_memory())
+    need = foak_ce_host_workspace_size(N)
+    ws = workspace(N + 64, dev) if workspace_tensor is None else workspace_tensor  # + 256 bytes of results
+    if ws.numel() < need:
+        raise ValueError("workspace_tensor smaller than foak_ce_host_workspace_size(N)")
+    st = lib.foak_ce_fwd_bwd_host(_ptr(host_logits), dt, ld, _ptr(host_labels), N, V, int(ignore_index), float(g),
+                                  float(denom), _ptr(dev_logits), _ptr(dev_labels), _ptr(out["loss"]),
+                                  _ptr(out["n_valid"]), _ptr(out["err"]), _ptr(ws), ws.numel(), _stream(dev, stream))
+    _check(st, "foak_ce_fwd_bwd_host")
+    return out
 
 
 FOAK_CE_NOALLOC_MAX_ROWS = 262144

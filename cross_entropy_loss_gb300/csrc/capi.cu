@@ -1,7 +1,9 @@
 // C ABI of the library: argument checks, workspace layout, launches and the
 // optional synchronous error check.  Declarations and their contracts are in
 // include/foak_ce.h.
+#include <algorithm>
 #include <atomic>
+#include <map>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -111,6 +113,59 @@ foak_status rows_common(bool grad, const void* logits, int32_t dtype, int64_t ld
                                    ignore_index, g, denom, loss, lse, rl, n_valid, err, ws, s);
     if (e == cudaSuccess) e = cudaGetLastError();
     return finish(e, err, s);
+}
+
+// ---- host-buffer entry: layout, copy stream and events (one set per device)
+constexpr int kHostMaxChunks = 32;
+constexpr int64_t kHostChunkRows = 512;
+
+struct HostWs {
+    CeWsHeader* hdr;
+    float* row_loss;     // N
+    int32_t* chunk_err;  // kHostMaxChunks words, one per chunk launch
+    float* chunk_loss;   // loss output of the chunk launches (unused)
+    float* loss;
+    int32_t* n_valid;
+    int32_t* err;
+};
+
+size_t host_ws_bytes(int64_t N) {
+    return sizeof(CeWsHeader) + (static_cast<size_t>(N) * 4 + 255) / 256 * 256 + 256;
+}
+
+HostWs host_layout(void* base, int64_t N) {
+    char* b = static_cast<char*>(base);
+    HostWs w;
+    w.hdr = reinterpret_cast<CeWsHeader*>(b);
+    w.row_loss = reinterpret_cast<float*>(b + sizeof(CeWsHeader));
+    char* tail = b + sizeof(CeWsHeader) + (static_cast<size_t>(N) * 4 + 255) / 256 * 256;
+    w.chunk_err = reinterpret_cast<int32_t*>(tail);
+    w.chunk_loss = reinterpret_cast<float*>(tail + 4 * kHostMaxChunks);
+    w.loss = w.chunk_loss + 1;
+    w.n_valid = reinterpret_cast<int32_t*>(w.loss + 1);
+    w.err = w.n_valid + 1;
+    return w;
+}
+
+struct CopyLane {
+    cudaStream_t cs = nullptr;
+    cudaEvent_t ev[kHostMaxChunks + 1] = {};
+};
+std::mutex g_host_mu;  // serialises host-buffer calls: they share the lane of their device
+std::map<int, CopyLane> g_lanes;
+
+cudaError_t copy_lane(int dev, CopyLane** out) {
+    CopyLane& l = g_lanes[dev];
+    if (!l.cs) {
+        cudaError_t e = cudaStreamCreateWithFlags(&l.cs, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
+        for (auto& ev : l.ev) {
+            e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    *out = &l;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -247,6 +302,67 @@ foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const
     d.mode = static_cast<GemmOut>(out_mode);
     d.err = err;
     return finish(launch_gemm_bf16(d, s), err, s);
+}
+
+size_t foak_ce_host_workspace_size(int64_t N) { return N < 0 ? 0 : host_ws_bytes(N); }
+
+foak_status foak_ce_fwd_bwd_host(const void* host_logits, int32_t dtype, int64_t ld, const int64_t* host_labels,
+                                 int64_t N, int64_t V, int64_t ignore_index, float g, float denom,
+                                 void* dev_logits, int64_t* dev_labels, float* host_loss, int32_t* host_n_valid,
+                                 int32_t* host_err, void* workspace, size_t workspace_bytes, void* stream) {
+    int es = 0;
+    foak_status st = check_rows(dev_logits, dtype, ld, dev_labels, N, V, &es);
+    if (st != FOAK_OK) return st;
+    if (N > 0 && (!host_logits || !host_labels)) return FOAK_ERR_INVALID_ARG;
+    if (!host_loss || (dev_logits && !aligned(dev_logits, 16))) return FOAK_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, kCeWsAlign) || workspace_bytes < host_ws_bytes(N)) return FOAK_ERR_WORKSPACE;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return finish(e, nullptr, s);
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    CopyLane* lane = nullptr;
+    e = copy_lane(dev, &lane);
+    if (e != cudaSuccess) return finish(e, nullptr, s);
+    const HostWs w = host_layout(workspace, N);
+    const int64_t nchunks =
+        N == 0 ? 0 : std::min<int64_t>(kHostMaxChunks, std::max<int64_t>(1, (N + kHostChunkRows - 1) / kHostChunkRows));
+    const int64_t per = nchunks ? (N + nchunks - 1) / nchunks : 0;
+    const int64_t row_bytes = ld * es;
+    // The copies start after the work already queued on `stream` (it may still use the device buffers).
+    e = cudaEventRecord(lane->ev[0], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(lane->cs, lane->ev[0], 0);
+    if (e == cudaSuccess && N > 0)
+        e = cudaMemcpyAsync(dev_labels, host_labels, static_cast<size_t>(N) * 8, cudaMemcpyHostToDevice, lane->cs);
+    for (int64_t c = 0; c < nchunks && e == cudaSuccess; ++c) {
+        const int64_t r0 = c * per, r1 = std::min(N, r0 + per);
+        if (r0 >= r1) break;
+        const size_t bytes = static_cast<size_t>((r1 - r0 - 1) * ld + V) * es;  // up to the last row's V-th element
+        e = cudaMemcpyAsync(static_cast<char*>(dev_logits) + r0 * row_bytes,
+                            static_cast<const char*>(host_logits) + r0 * row_bytes, bytes, cudaMemcpyHostToDevice,
+                            lane->cs);
+        if (e == cudaSuccess) e = cudaEventRecord(lane->ev[1 + c], lane->cs);
+    }
+    // Each chunk is swept as soon as it has landed; every chunk divides by the n_valid of all N labels.
+    int64_t launched = 0;
+    for (int64_t c = 0; c < nchunks && e == cudaSuccess; ++c) {
+        const int64_t r0 = c * per, r1 = std::min(N, r0 + per);
+        if (r0 >= r1) break;
+        e = cudaStreamWaitEvent(s, lane->ev[1 + c], 0);
+        char* x = static_cast<char*>(dev_logits) + r0 * row_bytes;
+        if (e == cudaSuccess)
+            e = launch_ce_rows(true, es, x, x, ld, dev_labels + r0, r1 - r0, V, ignore_index, g, denom, w.chunk_loss,
+                               nullptr, w.row_loss + r0, nullptr, w.chunk_err + c, w.hdr, s, dev_labels, N);
+        ++launched;
+    }
+    if (e == cudaSuccess)
+        e = launch_rows_finalize(w.row_loss, dev_labels, N, V, ignore_index, denom, w.chunk_err, launched, w.loss,
+                                 w.n_valid, w.err, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(host_loss, w.loss, 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && host_n_valid) e = cudaMemcpyAsync(host_n_valid, w.n_valid, 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && host_err) e = cudaMemcpyAsync(host_err, w.err, 4, cudaMemcpyDeviceToHost, s);
+    return finish(e, w.err, s);
 }
 
 void foak_test_fail_next_launches(int32_t count) { g_fail_launches.store(count < 0 ? 0 : count); }

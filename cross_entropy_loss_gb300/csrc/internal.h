@@ -46,6 +46,11 @@ cudaError_t launch_ce_backward(int elem_bytes, void* dx, const void* x, int64_t 
 
 // Chunked linear + CE (linear_ce.cu): workspace bytes and the launch sequence.
 size_t linear_ce_workspace_bytes(int64_t N, int64_t V, int64_t chunk);
+// loss = (float64 sum of row_loss[0..N) in row order) / D, n_valid from labels, err
+// = OR of the nerr words in chunk_err plus FOAK_ERRBIT_LABEL_RANGE for bad labels.
+cudaError_t launch_rows_finalize(const float* row_loss, const int64_t* labels, int64_t N, int64_t V,
+                                 int64_t ignore_index, float denom, const int32_t* chunk_err, int64_t nerr,
+                                 float* loss, int32_t* n_valid, int32_t* err, cudaStream_t stream);
 cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t V, int64_t D,
                              int64_t ignore_index, int64_t chunk, float g, float denom, float* loss, void* dH,
                              float* dW, int32_t* n_valid, int32_t* err, void* workspace, cudaStream_t stream);

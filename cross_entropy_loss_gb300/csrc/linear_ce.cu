@@ -95,6 +95,14 @@ __global__ void __launch_bounds__(kFinThreads) linear_ce_finalize(const float* _
 
 }  // namespace
 
+cudaError_t launch_rows_finalize(const float* row_loss, const int64_t* labels, int64_t N, int64_t V,
+                                 int64_t ignore_index, float denom, const int32_t* chunk_err, int64_t nerr,
+                                 float* loss, int32_t* n_valid, int32_t* err, cudaStream_t stream) {
+    linear_ce_finalize<<<1, kFinThreads, 0, stream>>>(row_loss, labels, N, V, ignore_index, denom, chunk_err, nerr,
+                                                      loss, n_valid, err);
+    return cudaGetLastError();
+}
+
 size_t linear_ce_workspace_bytes(int64_t N, int64_t V, int64_t chunk) {
     return lin_layout(nullptr, N, V, chunk).bytes;
 }

@@ -143,6 +143,46 @@ foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of device workspace foak_ce_fwd_bwd_host needs for N rows: a 256-byte
+ * header, N float32 per-row loss terms and 256 bytes of per-chunk error words and
+ * results.  256-byte aligned, zero-filled before first use, left reusable by every
+ * call (the same rules as foak_ce_workspace_size).
+ */
+size_t foak_ce_host_workspace_size(int64_t N);
+
+/*
+ * Fused forward + backward on logits that live in HOST memory: the call copies
+ * the labels and then the logits to the device in row chunks on a copy stream of
+ * its own and runs the fused kernel of foak_ce_fwd_bwd on each chunk as soon as it
+ * has landed (on `stream`), so the arithmetic hides under the host-to-device copy;
+ * every chunk divides by the n_valid of all N rows (or denom), and one float64
+ * reduction in row order over all N rows gives the loss, as in foak_ce_fwd_bwd.
+ * This is the same mean-reduced cross-entropy and in-place gradient as the
+ * FastCrossEntropyLoss kernel of the FOAK pages (fms-acceleration PR #79,
+ * Description item 4); the pages fix no host interface, so this one is ours.
+ *   host_logits (host)   N x V in dtype, row stride ld elements; pinned memory
+ *                        (cudaHostAlloc / torch pin_memory) for a full-speed copy.
+ *                        Only the first V elements of each row are copied.
+ *   host_labels (host)   int64[N]
+ *   dev_logits (device)  N x ld in dtype, 16-byte aligned: receives the logits and
+ *                        ends holding dlogits (ignored rows +0.0)
+ *   dev_labels (device)  int64[N], receives the labels
+ *   host_loss (host)     float[1]; host_n_valid, host_err (host) int32[1] or NULL:
+ *                        written by device-to-host copies at the end of the work on
+ *                        `stream` (pinned memory keeps the call asynchronous;
+ *                        read them after synchronising the stream)
+ *   workspace (device)   foak_ce_host_workspace_size(N) bytes
+ *   other arguments      as for foak_ce_fwd_bwd
+ * Errors: as foak_ce_fwd_bwd for the arguments; FOAK_ERR_INVALID_ARG for a null
+ * host or device buffer when N > 0.  Calls for the same device from several host
+ * threads are serialised internally (they share the copy stream).
+ */
+foak_status foak_ce_fwd_bwd_host(const void* host_logits, int32_t dtype, int64_t ld, const int64_t* host_labels,
+                                 int64_t N, int64_t V, int64_t ignore_index, float g, float denom,
+                                 void* dev_logits, int64_t* dev_labels, float* host_loss, int32_t* host_n_valid,
+                                 int32_t* host_err, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace foak_linear_ce_chunked needs: a 256-byte header, N
  * float32 per-row loss terms, a few error words and two chunks of bf16 logits
  * (min(2 chunk, N) x V, rows padded to 64 elements: dW is updated once per pair

@@ -103,3 +103,32 @@ def test_status_strings(so):
     assert "unknown" in so.status_string(99)
     err = so.FoakError(so.FOAK_ERR_WORKSPACE, "x")
     assert "WORKSPACE" in str(err)
+
+
+def _host(so, hx=FAKE, dtype=1, ld=32000, hy=FAKE, N=4, V=32000, dx=FAKE, dy=FAKE, hl=FAKE, ws=FAKE,
+          wsb=1 << 20):
+    return so.lib.foak_ce_fwd_bwd_host(hx, dtype, ld, hy, N, V, -100, 1.0, 0.0, dx, dy, hl, None, None, ws, wsb,
+                                       None)
+
+
+def test_host_entry_argument_errors(so):
+    """foak_ce_fwd_bwd_host checks its host and device buffers before any copy."""
+    E = so
+    assert so.foak_ce_host_workspace_size(0) == 512
+    assert so.foak_ce_host_workspace_size(8192) == 256 + 8192 * 4 + 256
+    assert so.foak_ce_host_workspace_size(-1) == 0
+    assert _host(so, dtype=3) == E.FOAK_ERR_UNSUPPORTED
+    assert _host(so, ld=10) == E.FOAK_ERR_INVALID_ARG
+    assert _host(so, hx=None) == E.FOAK_ERR_INVALID_ARG
+    assert _host(so, hy=None) == E.FOAK_ERR_INVALID_ARG
+    assert _host(so, dx=None) == E.FOAK_ERR_INVALID_ARG
+    assert _host(so, dy=None) == E.FOAK_ERR_INVALID_ARG
+    assert _host(so, hl=None) == E.FOAK_ERR_INVALID_ARG
+    assert _host(so, dx=FAKE + 8) == E.FOAK_ERR_INVALID_ARG       # device logits 16-byte aligned
+    assert _host(so, ws=None) == E.FOAK_ERR_WORKSPACE
+    assert _host(so, wsb=512) == E.FOAK_ERR_WORKSPACE             # N rows need 256 + 256 + 256 bytes
+    so.lib.foak_test_fail_next_launches(1)
+    try:
+        assert _host(so) == E.FOAK_ERR_CUDA
+    finally:
+        so.lib.foak_test_fail_next_launches(0)
