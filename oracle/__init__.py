@@ -18,6 +18,9 @@ reading is the textbook one, stated in ``ce_oracle.c``):
   call LigerFusedLinearCrossEntropy -- "Running Liger Kernel Benchmarks" on the
   foak page -- and "chunked loss" -- PR #79, TODO list).  Chunking is a schedule,
   not a different result, so the oracle does not chunk.
+* ``rmsnorm`` / ``rmsnorm_backward`` / ``rmsnorm_linear_ce`` -- the RMSNorm the
+  foak page lists among its kernels ("Fast RMS LayerNorm Triton Kernels"), alone
+  and as the final norm in front of the chunked linear + cross-entropy.
 
 Parity pins (closed forms, invariants, finite differences, brute force, a
 hand-worked example) live in ``tests/test_oracle_pins.py``; every function here
@@ -173,3 +176,51 @@ def linear_ce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *, ignore_index:
     dW = dZ.T @ Hd
     return dict(loss=r["loss"], n_valid=r["n_valid"], n_bad=r["n_bad"], dH=dH, dW=dW, Z=Z, dZ=dZ,
                 lse=r["lse"], row_loss=r["row_loss"], state=r["state"], scale=r["scale"])
+
+
+# --------------------------------------------------------------------- RMSNorm
+# "Fast RMS LayerNorm Triton Kernels" (fms-acceleration-foak 0.7.4 page, list of
+# fused operations and kernels; the patch rule there swaps the model's RMSNorm
+# module for fast_rms_layernorm).  The pages print no formula; the reading taken
+# is the RMSNorm of the Llama / Mistral / Granite decoders they patch:
+#     r_i = 1 / sqrt(mean_j x_ij^2 + eps),   y_ij = x_ij * r_i * gamma_j.
+
+def rmsnorm(X: np.ndarray, gamma: np.ndarray, eps: float):
+    """y = x * r * gamma per row, r = 1 / sqrt(mean(x^2) + eps); float64.  Returns (Y, r)."""
+    Xd, gd = _to_f64(X), _to_f64(gamma)
+    ms = np.mean(Xd * Xd, axis=1)
+    r = 1.0 / np.sqrt(ms + eps)
+    return Xd * r[:, None] * gd[None, :], r
+
+
+def rmsnorm_backward(dY: np.ndarray, X: np.ndarray, gamma: np.ndarray, eps: float):
+    """Gradients of sum(dY * rmsnorm(X)) w.r.t. X and gamma, float64.
+
+    With xh = x * r and u = gamma * dy (per row):  dx = r * (u - xh * mean(xh * u)),
+    dgamma = sum over rows of dy * xh.
+    """
+    Xd, gd, dYd = _to_f64(X), _to_f64(gamma), _to_f64(dY)
+    _, r = rmsnorm(Xd, gd, eps)
+    xh = Xd * r[:, None]
+    u = dYd * gd[None, :]
+    dX = r[:, None] * (u - xh * np.mean(xh * u, axis=1)[:, None])
+    dgamma = np.sum(dYd * xh, axis=0)
+    return dX, dgamma
+
+
+def rmsnorm_linear_ce(X: np.ndarray, gamma: np.ndarray, W: np.ndarray, labels: np.ndarray, *, eps: float,
+                      ignore_index: int = -100, g: float = 1.0, denom: float = 0.0, threads: int | None = None,
+                      round_h=None):
+    """Final norm -> LM head -> cross-entropy: H = rmsnorm(X), then ``linear_ce`` on H,
+    then dX, dgamma through the norm; float64 throughout.
+
+    ``round_h`` (optional) maps H to the values the device stores (e.g. bf16 rounding)
+    before the linear layer; the gradient then flows through the unrounded norm, the
+    straight-through reading of a rounded activation.
+    """
+    H, r = rmsnorm(X, gamma, eps)
+    Hq = round_h(H) if round_h is not None else H
+    res = linear_ce(Hq, W, labels, ignore_index=ignore_index, g=g, denom=denom, threads=threads)
+    dX, dgamma = rmsnorm_backward(res["dH"], X, gamma, eps)
+    res.update(H=H, rstd=r, dX=dX, dgamma=dgamma)
+    return res

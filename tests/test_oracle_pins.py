@@ -295,3 +295,61 @@ def test_linear_chunks_of_rows_compose_to_whole():
         np.testing.assert_allclose(part["dH"], whole["dH"][c:c + 3], rtol=1e-12, atol=1e-16)
     assert tot == pytest.approx(whole["loss"], rel=1e-13)
     np.testing.assert_allclose(dW, whole["dW"], rtol=1e-12, atol=1e-16)
+
+
+# ------------------------------------------------------------------ RMSNorm pins
+
+def test_rmsnorm_hand_worked_and_closed_forms():
+    # hand-worked row: x = (3, 4), gamma = (1, 2), eps = 0: mean square 12.5, rms 3.5355339059327378
+    Y, r = oracle.rmsnorm(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.0)
+    assert r[0] == pytest.approx(0.28284271247461906, rel=1e-15)
+    np.testing.assert_allclose(Y[0], [0.8485281374238571, 2.2627416997969522], rtol=1e-15)
+    # a constant row c: y_j = c / sqrt(c^2 + eps) * gamma_j
+    g = np.array([0.5, -1.0, 2.0, 3.0])
+    Y, _ = oracle.rmsnorm(np.full((1, 4), 2.0), g, 0.25)
+    np.testing.assert_allclose(Y[0], 2.0 / math.sqrt(4.25) * g, rtol=1e-15)
+    # the normalised row's mean square is ms / (ms + eps)
+    rng = np.random.default_rng(7)
+    X = rng.normal(size=(5, 33)) * 3.0
+    Y, _ = oracle.rmsnorm(X, np.ones(33), 0.1)
+    ms = (X ** 2).sum(axis=1) / 33
+    np.testing.assert_allclose((Y ** 2).sum(axis=1) / 33, ms / (ms + 0.1), rtol=1e-14)
+    # with eps = 0 the norm is scale invariant
+    Ya, _ = oracle.rmsnorm(X, g[:1].repeat(33), 0.0)
+    Yb, _ = oracle.rmsnorm(3.7 * X, g[:1].repeat(33), 0.0)
+    np.testing.assert_allclose(Ya, Yb, rtol=1e-14)
+
+
+def _fd(f, a, h=1e-6):
+    out = np.zeros_like(a)
+    for idx in np.ndindex(a.shape):
+        p, m = a.copy(), a.copy()
+        p[idx] += h
+        m[idx] -= h
+        out[idx] = (f(p) - f(m)) / (2 * h)
+    return out
+
+
+def test_rmsnorm_backward_matches_finite_differences():
+    rng = np.random.default_rng(11)
+    X, g, dY, eps = rng.normal(size=(3, 5)), rng.normal(size=5), rng.normal(size=(3, 5)), 1e-3
+    dX, dg = oracle.rmsnorm_backward(dY, X, g, eps)
+    fx = _fd(lambda x: float(np.sum(dY * oracle.rmsnorm(x, g, eps)[0])), X)
+    fg = _fd(lambda gg: float(np.sum(dY * oracle.rmsnorm(X, gg, eps)[0])), g)
+    np.testing.assert_allclose(dX, fx, rtol=1e-7, atol=1e-9)
+    np.testing.assert_allclose(dg, fg, rtol=1e-7, atol=1e-9)
+
+
+def test_rmsnorm_linear_ce_matches_finite_differences():
+    """Final norm -> LM head -> CE on tiny sizes: dX, dgamma and dW against central
+    differences of the loss (one row ignored, so the mean is over 3 rows)."""
+    rng = np.random.default_rng(5)
+    N, D, V, eps = 4, 6, 5, 1e-4
+    X, g, W = rng.normal(size=(N, D)), rng.normal(size=D), rng.normal(size=(V, D)) * 0.5
+    y = np.array([1, -100, 4, 0], dtype=np.int64)
+    res = oracle.rmsnorm_linear_ce(X, g, W, y, eps=eps, g=1.3)
+    L = lambda x, gg, w: oracle.rmsnorm_linear_ce(x, gg, w, y, eps=eps, g=1.3)["loss"] * 1.3  # noqa: E731
+    np.testing.assert_allclose(res["dX"], _fd(lambda x: L(x, g, W), X, 1e-5), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(res["dgamma"], _fd(lambda gg: L(X, gg, W), g, 1e-5), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(res["dW"], _fd(lambda w: L(X, g, w), W, 1e-5), rtol=1e-6, atol=1e-9)
+    assert res["n_valid"] == 3
