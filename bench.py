@@ -479,6 +479,8 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
 
 CHUNKED_DESC = ("chunked linear+CE: H 8192x4096 bf16 ~N(0,1), W 32000x4096 bf16 ~N(0,0.02^2), 10% rows -100, "
                 "chunks of 1024 rows")
+NORM_TAIL_DESC = ("decoder tail: RMSNorm (eps 1e-5) of X 8192x4096 bf16 ~N(0,2^2), gamma ~N(1,0.1^2) -> "
+                  "chunked LM head W 32000x4096 + CE, 10% rows -100, chunks of 1024 rows")
 
 
 def chunked_timing(ce, torch, dev, stream, steps=5, warmup=2):
@@ -513,6 +515,36 @@ def chunked_timing(ce, torch, dev, stream, steps=5, warmup=2):
                 "tokens_per_s": N / (ms * 1e-3), "TFLOPs": tf, "frac": tf / peak, "peak": peak,
                 "peak_unit": "TFLOP/s bf16", "peak_source": src, "loss": float(out["loss"].item()),
                 "err": int(out["err"].item()), "gpu_launches_per_step": 4 * ((N + chunk - 1) // chunk) + 1})
+    # the decoder tail: final RMSNorm -> chunked LM head + CE -> norm backward
+    t = wl.norm_chunked()
+    X = torch.from_numpy(t["X"].view(np.int16)).to(dev).view(torch.bfloat16)
+    gam = torch.from_numpy(t["gamma"].view(np.int16)).to(dev).view(torch.bfloat16)
+    yt = torch.from_numpy(t["labels"]).to(dev)
+    dX = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    tail = lambda: ce.foak_rmsnorm_linear_ce_chunked(X, gam, W, yt, eps=t["eps"], chunk=chunk, dX=dX, dW=dW)  # noqa: E731
+    ms_t = timed(tail, steps, warmup)
+    out_t = tail()
+    tf_t = flops / (ms_t * 1e-3) / 1e12
+    res.append({"path": "foak_rmsnorm_linear_ce_chunked", "workload": NORM_TAIL_DESC, "steps": steps,
+                "ms_per_step": ms_t, "tokens_per_s": N / (ms_t * 1e-3), "TFLOPs": tf_t, "frac": tf_t / peak,
+                "peak": peak, "peak_unit": "TFLOP/s bf16 (6*N*V*D; the norm's bytes are not counted)",
+                "peak_source": src, "norm_overhead_ms": ms_t - ms, "loss": float(out_t["loss"].item()),
+                "err": int(out_t["err"].item())})
+    # the norm alone, forward and backward (HBM-bound: algorithmic bytes / time)
+    hbm, hsrc = _peak_hbm()
+    Y = torch.empty_like(X)
+    _, rstd = ce.foak_rmsnorm_forward(X, gam, eps=t["eps"], Y=Y)
+    ms_f = timed(lambda: ce.foak_rmsnorm_forward(X, gam, eps=t["eps"], Y=Y), 20, 3)
+    ms_b = timed(lambda: ce.foak_rmsnorm_backward(Y, X, gam, rstd, dX=dX), 20, 3)
+    nd2 = N * D * 2
+    for name, ms_k, byts in (("foak_rmsnorm_forward", ms_f, 2 * nd2 + 4 * N),
+                             ("foak_rmsnorm_backward (dX and dgamma)", ms_b, 5 * nd2 + 4 * N)):
+        gbs = byts / (ms_k * 1e-3) / 1e9
+        res.append({"path": name, "workload": "X 8192x4096 bf16 (the decoder tail's norm)", "steps": 20,
+                    "ms_per_step": ms_k, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm,
+                    "peak_source": hsrc,
+                    "bytes": "forward: read X, write Y; backward: read dY and X twice (dX, then dgamma), write dX"})
+    del X, dX, Y
     # the three products of one chunk, alone
     Z = torch.empty(chunk, V, dtype=torch.bfloat16, device=dev)
     Zs = torch.randn(chunk, V, device=dev).to(torch.bfloat16)

@@ -43,6 +43,13 @@ SIGNATURES = {
     "foak_ce_forward": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                _vp]),
     "foak_ce_backward": (_i32, [_vp, _vp, _i32, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp]),
+    "foak_rmsnorm_forward": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _f32, _vp, _i64, _vp, _vp]),
+    "foak_rmsnorm_workspace_size": (_sz, [_i64]),
+    "foak_rmsnorm_backward": (_i32, [_vp, _i64, _vp, _i64, _vp, _vp, _i32, _i64, _i64, _vp, _i64, _vp, _vp, _sz,
+                                     _vp]),
+    "foak_rmsnorm_linear_ce_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "foak_rmsnorm_linear_ce_chunked": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _f32, _f32, _f32,
+                                              _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "foak_ce_host_workspace_size": (_sz, [_i64]),
     "foak_ce_fwd_bwd_host": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _sz, _vp]),
@@ -351,3 +358,90 @@ def foak_linear_ce_chunked(H, W, labels, *, chunk: int = 1024, g: float = 1.0, i
                                     ws.numel(), _stream(dev, stream))
     _check(st, "foak_linear_ce_chunked")
     return dict(loss=loss, dH=dH, dW=dW, n_valid=n_valid, err=err)
+
+
+# --------------------------------------------------------------------- RMSNorm
+_norm_ws: dict = {}
+
+
+def _rows_arg(t, name):
+    if t.dim() != 2 or t.stride(1) != 1 or t.dtype not in _DT or not t.is_cuda:
+        raise ValueError(f"{name} must be a 2-D bfloat16/float32 CUDA tensor with unit column stride")
+    return t.shape[0], t.shape[1], (t.stride(0) if t.shape[0] > 1 else t.shape[1])
+
+
+def foak_rmsnorm_forward(X, gamma, *, eps: float = 1e-5, Y=None, want_rstd: bool = True, stream=None):
+    """Y = X / sqrt(mean(X^2) + eps) * gamma per row (fp32 arithmetic, one rounding).
+
+    Returns (Y, rstd); rstd (float32 [N]) is None unless ``want_rstd``.
+    """
+    N, D, ldx = _rows_arg(X, "X")
+    if gamma.dtype != X.dtype or gamma.numel() != D or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous vector of D elements in X's dtype")
+    Y = torch.empty_like(X) if Y is None else Y
+    _, _, ldy = _rows_arg(Y, "Y")
+    rstd = torch.empty(N, dtype=torch.float32, device=X.device) if want_rstd else None
+    st = lib.foak_rmsnorm_forward(_ptr(X), _DT[X.dtype], ldx, _ptr(gamma), N, D, float(eps), _ptr(Y), ldy, _ptr(rstd),
+                                  _stream(X.device, stream))
+    _check(st, "foak_rmsnorm_forward")
+    return Y, rstd
+
+
+def foak_rmsnorm_backward(dY, X, gamma, rstd, *, dX=None, want_dgamma: bool = True, stream=None):
+    """dX (X's dtype) and dgamma (float32 [D], or None) of sum(dY * rmsnorm(X))."""
+    N, D, lddy = _rows_arg(dY, "dY")
+    _, _, ldx = _rows_arg(X, "X")
+    dX = torch.empty_like(X) if dX is None else dX
+    _, _, lddx = _rows_arg(dX, "dX")
+    dev = X.device
+    dgamma = torch.empty(D, dtype=torch.float32, device=dev) if want_dgamma else None
+    need = int(lib.foak_rmsnorm_workspace_size(D))
+    with _ws_lock:
+        ws = _norm_ws.get(dev)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            _norm_ws[dev] = ws
+    st = lib.foak_rmsnorm_backward(_ptr(dY), lddy, _ptr(X), ldx, _ptr(gamma), _ptr(rstd), _DT[X.dtype], N, D, _ptr(dX),
+                                   lddx, _ptr(dgamma), _ptr(ws), ws.numel(), _stream(dev, stream))
+    _check(st, "foak_rmsnorm_backward")
+    return dX, dgamma
+
+
+def foak_rmsnorm_linear_ce_chunked(X, gamma, W, labels, *, eps: float = 1e-5, chunk: int = 1024, g: float = 1.0,
+                                   ignore_index: int = -100, denom: float = 0.0, dX=None, dW=None,
+                                   workspace_tensor=None, stream=None):
+    """Final norm -> LM head -> CE: loss, dX, dgamma, dW of CE(rmsnorm(X, gamma) W^T).
+
+    X: bf16 [N][D], gamma: bf16 [D], W: bf16 [V][D] (contiguous).  Returns
+    dict(loss, dX, dgamma, dW, n_valid, err); dX bf16, dgamma and dW float32.
+    """
+    for t, n in ((X, "X"), (gamma, "gamma"), (W, "W")):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous bfloat16 tensor")
+    N, D = X.shape
+    V = W.shape[0]
+    if W.shape[1] != D or gamma.numel() != D:
+        raise ValueError("X, gamma and W disagree on the hidden size")
+    dev = X.device
+    labels = _labels_arg(labels, N, dev)
+    dX = torch.empty_like(X) if dX is None else dX
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev) if dW is None else dW
+    dgamma = torch.empty(D, dtype=torch.float32, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int32, device=dev)
+    err = torch.empty(1, dtype=torch.int32, device=dev)
+    need = int(lib.foak_rmsnorm_linear_ce_workspace_size(N, V, D, chunk))
+    ws = workspace_tensor
+    if ws is None:
+        with _ws_lock:
+            key = ("norm_lin", dev)
+            ws = _norm_ws.get(key)
+            if ws is None or ws.numel() < need:
+                ws = torch.zeros(need, dtype=torch.uint8, device=dev)  # zero-filled before first use
+                _norm_ws[key] = ws
+    st = lib.foak_rmsnorm_linear_ce_chunked(_ptr(X), _ptr(gamma), _ptr(W), _ptr(labels), N, V, D, int(ignore_index),
+                                            int(chunk), float(eps), float(g), float(denom), _ptr(loss), _ptr(dX),
+                                            _ptr(dgamma), _ptr(dW), _ptr(n_valid), _ptr(err), _ptr(ws), ws.numel(),
+                                            _stream(dev, stream))
+    _check(st, "foak_rmsnorm_linear_ce_chunked")
+    return dict(loss=loss, dX=dX, dgamma=dgamma, dW=dW, n_valid=n_valid, err=err)

@@ -168,6 +168,39 @@ cudaError_t copy_lane(int dev, CopyLane** out) {
     return cudaSuccess;
 }
 
+// ---- RMSNorm entries
+bool rows16(const void* p, int64_t ld, int es) { return aligned(p, 16) && (ld * es) % 16 == 0; }
+
+inline size_t r256(size_t b) { return (b + 255) / 256 * 256; }
+
+struct NormLinWs {
+    void* lin;     // the chunked linear + CE workspace
+    void* H;       // bf16 [N][D]: the normalised hidden states
+    void* dH;      // bf16 [N][D]
+    float* rstd;   // [N]
+    float* part;   // dgamma partials
+    size_t bytes;
+};
+
+NormLinWs norm_lin_layout(void* base, int64_t N, int64_t V, int64_t D, int64_t chunk) {
+    char* b = static_cast<char*>(base);
+    NormLinWs w;
+    size_t off = 0;
+    w.lin = b + off;
+    off += r256(linear_ce_workspace_bytes(N, V, chunk));
+    const size_t hd = r256(static_cast<size_t>(N) * static_cast<size_t>(D) * 2);
+    w.H = b + off;
+    off += hd;
+    w.dH = b + off;
+    off += hd;
+    w.rstd = reinterpret_cast<float*>(b + off);
+    off += r256(static_cast<size_t>(N) * 4);
+    w.part = reinterpret_cast<float*>(b + off);
+    off += rmsnorm_workspace_bytes(D);
+    w.bytes = off;
+    return w;
+}
+
 }  // namespace
 }  // namespace foak
 
@@ -264,6 +297,73 @@ foak_status foak_linear_ce_chunked(const void* H, const void* W, const int64_t* 
     return finish(launch_linear_ce(H, W, labels, N, V, D, ignore_index, chunk, g, denom, loss, dH, dW, n_valid, err,
                                    workspace, s),
                   err, s);
+}
+
+size_t foak_rmsnorm_workspace_size(int64_t D) { return D < 1 ? 0 : rmsnorm_workspace_bytes(D); }
+
+foak_status foak_rmsnorm_forward(const void* X, int32_t dtype, int64_t ldx, const void* gamma, int64_t N, int64_t D,
+                                 float eps, void* Y, int64_t ldy, float* rstd, void* stream) {
+    const int es = elem_bytes_of(dtype);
+    if (!es) return FOAK_ERR_UNSUPPORTED;
+    if (N < 0 || D < 8 || ldx < D || ldy < D || !(eps >= 0.f)) return FOAK_ERR_INVALID_ARG;
+    if (D % 8) return FOAK_ERR_UNSUPPORTED;
+    if (!gamma || !aligned(gamma, 16) || (rstd && !aligned(rstd, 4))) return FOAK_ERR_INVALID_ARG;
+    if (N > 0 && (!X || !Y || !rows16(X, ldx, es) || !rows16(Y, ldy, es))) return FOAK_ERR_INVALID_ARG;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(launch_rmsnorm_fwd(es, X, ldx, gamma, N, D, eps, Y, ldy, rstd, s), nullptr, s);
+}
+
+foak_status foak_rmsnorm_backward(const void* dY, int64_t lddy, const void* X, int64_t ldx, const void* gamma,
+                                  const float* rstd, int32_t dtype, int64_t N, int64_t D, void* dX, int64_t lddx,
+                                  float* dgamma, void* workspace, size_t workspace_bytes, void* stream) {
+    const int es = elem_bytes_of(dtype);
+    if (!es) return FOAK_ERR_UNSUPPORTED;
+    if (N < 0 || D < 8 || ldx < D || lddy < D || lddx < D) return FOAK_ERR_INVALID_ARG;
+    if (D % 8) return FOAK_ERR_UNSUPPORTED;
+    if (!gamma || !aligned(gamma, 16) || (dgamma && !aligned(dgamma, 4))) return FOAK_ERR_INVALID_ARG;
+    if (N > 0 && (!dY || !X || !dX || !rstd || !rows16(dY, lddy, es) || !rows16(X, ldx, es) || !rows16(dX, lddx, es) ||
+                  !aligned(rstd, 4)))
+        return FOAK_ERR_INVALID_ARG;
+    if (dgamma && (!workspace || !aligned(workspace, kCeWsAlign) || workspace_bytes < rmsnorm_workspace_bytes(D)))
+        return FOAK_ERR_WORKSPACE;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(launch_rmsnorm_bwd(es, dY, lddy, X, ldx, gamma, rstd, N, D, dX, lddx, static_cast<float*>(workspace),
+                                     dgamma, s),
+                  nullptr, s);
+}
+
+size_t foak_rmsnorm_linear_ce_workspace_size(int64_t N, int64_t V, int64_t D, int64_t chunk) {
+    if (N < 0 || V < 1 || D < 1 || chunk < 1) return 0;
+    return norm_lin_layout(nullptr, N, V, D, chunk).bytes;
+}
+
+foak_status foak_rmsnorm_linear_ce_chunked(const void* X, const void* gamma, const void* W, const int64_t* labels,
+                                           int64_t N, int64_t V, int64_t D, int64_t ignore_index, int64_t chunk,
+                                           float eps, float g, float denom, float* loss, void* dX, float* dgamma,
+                                           float* dW, int32_t* n_valid, int32_t* err, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+    if (N < 0 || V < 1 || D < 8 || chunk < 1 || !(eps >= 0.f)) return FOAK_ERR_INVALID_ARG;
+    if (N > 0x7fffffffLL || V > 0x7fffffffLL || D > 0x7fffffffLL) return FOAK_ERR_UNSUPPORTED;
+    if (V > ce_rows_max_vocab(2) || D % 8) return FOAK_ERR_UNSUPPORTED;
+    if (!W || !dW || !loss || !gamma || !dgamma || !aligned(W, 16) || !aligned(dW, 16) || !aligned(loss, 4) ||
+        !aligned(gamma, 16) || !aligned(dgamma, 4))
+        return FOAK_ERR_INVALID_ARG;
+    if (N > 0 && (!X || !labels || !dX || !aligned(X, 16) || !aligned(dX, 16) || !aligned(labels, 8)))
+        return FOAK_ERR_INVALID_ARG;
+    if ((n_valid && !aligned(n_valid, 4)) || (err && !aligned(err, 4))) return FOAK_ERR_INVALID_ARG;
+    const NormLinWs w = norm_lin_layout(workspace, N, V, D, chunk);
+    if (!workspace || !aligned(workspace, kCeWsAlign) || workspace_bytes < w.bytes) return FOAK_ERR_WORKSPACE;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // final norm (prologue) -> chunked LM head + CE -> norm backward (epilogue); H and dH stay on the device
+    cudaError_t e = launch_rmsnorm_fwd(2, X, D, gamma, N, D, eps, w.H, D, w.rstd, s);
+    if (e == cudaSuccess)
+        e = launch_linear_ce(w.H, W, labels, N, V, D, ignore_index, chunk, g, denom, loss, w.dH, dW, n_valid, err,
+                             w.lin, s);
+    if (e == cudaSuccess) e = launch_rmsnorm_bwd(2, w.dH, D, X, D, gamma, w.rstd, N, D, dX, D, w.part, dgamma, s);
+    return finish(e, err, s);
 }
 
 foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const void* b, int64_t ldb,

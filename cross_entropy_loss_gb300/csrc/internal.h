@@ -57,6 +57,18 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
 
 // Test hooks (capi.cu): the barrier-wait limit given to the row kernel, and a row
 // whose slice the row kernel's producer skips (so a wait is sure to run out).
+// RMSNorm (rmsnorm.cu): dgamma partials of kRmsGammaGroups row groups x D floats.
+constexpr int kRmsGammaGroups = 64;
+inline size_t rmsnorm_workspace_bytes(int64_t D) {
+    return (static_cast<size_t>(kRmsGammaGroups) * static_cast<size_t>(D) * 4 + 255) / 256 * 256;
+}
+cudaError_t launch_rmsnorm_fwd(int es, const void* X, int64_t ldx, const void* gamma, int64_t N, int64_t D,
+                               float eps, void* Y, int64_t ldy, float* rstd, cudaStream_t s);
+// dX (if N > 0) and, when dgamma is given, dgamma through `part` (rmsnorm_workspace_bytes(D)).
+cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void* X, int64_t ldx, const void* gamma,
+                               const float* rstd, int64_t N, int64_t D, void* dX, int64_t lddx, float* part,
+                               float* dgamma, cudaStream_t s);
+
 uint64_t test_wait_limit_ns();
 int64_t test_skip_load_row();
 int32_t test_row_path();  // 0 automatic, 1 one pass (clusters), 2 two-pass streaming

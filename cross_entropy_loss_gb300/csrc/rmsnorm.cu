@@ -1,0 +1,220 @@
+// RMSNorm forward and backward -- the "Fast RMS LayerNorm" kernels the FOAK pages
+// list among their fused operations (fms-acceleration-foak 0.7.4 page; the patch
+// rule there swaps a decoder's RMSNorm module for fast_rms_layernorm).  The pages
+// print no formula; the operation is the decoders' RMSNorm:
+//     r_i = 1 / sqrt(mean_j x_ij^2 + eps),   y_ij = x_ij * r_i * gamma_j
+// computed in fp32 and rounded once to the storage type, and its gradients
+//     xh = x * r,  u = gamma * dy,  dx = r * (u - xh * mean(xh * u)),
+//     dgamma_j = sum_i dy_ij * xh_ij.
+//
+// Both row kernels give one warp a row (D elements, 16-byte vectors, D % 8 == 0)
+// and read it twice: the first pass reduces over the row, the second re-reads it
+// (from L1: 8 KB at D = 4096 bf16) and writes.  HBM traffic is the algorithmic
+// one: forward reads X and writes Y; backward reads dY and X and writes dX.  dgamma
+// is a column reduction over rows: a separate kernel gives each thread 8
+// consecutive columns and one of 64 row groups, writes per-group partials, and a
+// last kernel sums the 64 partials in a fixed order -- deterministic, no atomics.
+#include <algorithm>
+
+#include "common.cuh"
+#include "foak_ce.h"
+#include "internal.h"
+
+namespace foak {
+
+namespace {
+
+constexpr int kNormThreads = 256;  // 8 warps, one row each at a time
+constexpr int kGammaThreads = 128;
+
+template <int ES>
+__device__ __forceinline__ void load8(const char* p, float (&f)[16 / ES]) {
+    const uint4 v = ld_global_v4(reinterpret_cast<const uint4*>(p));
+    if constexpr (ES == 2) {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    } else {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+}
+
+template <int ES>
+__device__ __forceinline__ void store8(char* p, const float (&f)[16 / ES]) {
+    uint4 v;
+    if constexpr (ES == 2) {
+        v.x = pack_bf16x2(f[0], f[1]); v.y = pack_bf16x2(f[2], f[3]);
+        v.z = pack_bf16x2(f[4], f[5]); v.w = pack_bf16x2(f[6], f[7]);
+    } else {
+        v.x = __float_as_uint(f[0]); v.y = __float_as_uint(f[1]);
+        v.z = __float_as_uint(f[2]); v.w = __float_as_uint(f[3]);
+    }
+    *reinterpret_cast<uint4*>(p) = v;
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const char* __restrict__ X, int64_t ldx,
+                                                                   const char* __restrict__ gamma, int64_t N,
+                                                                   int64_t D, float eps, char* __restrict__ Y,
+                                                                   int64_t ldy, float* __restrict__ rstd) {
+    constexpr int EPV = 16 / ES;
+    const int lane = threadIdx.x & 31;
+    const int64_t nvec = D / EPV;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kNormThreads / 32);
+    for (int64_t row = blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); row < N; row += warps) {
+        const char* x = X + row * ldx * ES;
+        float ss = 0.f;
+        for (int64_t v = lane; v < nvec; v += 32) {
+            float f[EPV];
+            load8<ES>(x + v * 16, f);
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) ss = fmaf(f[k], f[k], ss);
+        }
+        ss = warp_sum(ss);
+        const float r = rsqrtf(ss / static_cast<float>(D) + eps);
+        char* y = Y + row * ldy * ES;
+        for (int64_t v = lane; v < nvec; v += 32) {
+            float f[EPV], gm[EPV];
+            load8<ES>(x + v * 16, f);
+            load8<ES>(gamma + v * 16, gm);
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) f[k] = f[k] * r * gm[k];
+            store8<ES>(y + v * 16, f);
+        }
+        if (lane == 0 && rstd) rstd[row] = r;
+    }
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_bwd_kernel(const char* __restrict__ dY, int64_t lddy,
+                                                                   const char* __restrict__ X, int64_t ldx,
+                                                                   const char* __restrict__ gamma,
+                                                                   const float* __restrict__ rstd, int64_t N,
+                                                                   int64_t D, char* __restrict__ dX, int64_t lddx) {
+    constexpr int EPV = 16 / ES;
+    const int lane = threadIdx.x & 31;
+    const int64_t nvec = D / EPV;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kNormThreads / 32);
+    for (int64_t row = blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); row < N; row += warps) {
+        const char* x = X + row * ldx * ES;
+        const char* dy = dY + row * lddy * ES;
+        const float r = rstd[row];
+        float dot = 0.f;  // sum of xh * u over the row
+        for (int64_t v = lane; v < nvec; v += 32) {
+            float fx[EPV], fd[EPV], gm[EPV];
+            load8<ES>(x + v * 16, fx);
+            load8<ES>(dy + v * 16, fd);
+            load8<ES>(gamma + v * 16, gm);
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) dot = fmaf(fx[k] * r, gm[k] * fd[k], dot);
+        }
+        dot = warp_sum(dot);
+        const float m = dot / static_cast<float>(D);
+        char* dx = dX + row * lddx * ES;
+        for (int64_t v = lane; v < nvec; v += 32) {
+            float fx[EPV], fd[EPV], gm[EPV], o[EPV];
+            load8<ES>(x + v * 16, fx);
+            load8<ES>(dy + v * 16, fd);
+            load8<ES>(gamma + v * 16, gm);
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) o[k] = r * (gm[k] * fd[k] - fx[k] * r * m);
+            store8<ES>(dx + v * 16, o);
+        }
+    }
+}
+
+// part[g][j] = sum over rows i = g, g + G, ... of dy_ij * x_ij * r_i; thread = 8 columns.
+template <int ES>
+__global__ void __launch_bounds__(kGammaThreads) rmsnorm_dgamma_kernel(const char* __restrict__ dY, int64_t lddy,
+                                                                       const char* __restrict__ X, int64_t ldx,
+                                                                       const float* __restrict__ rstd, int64_t N,
+                                                                       int64_t D, float* __restrict__ part) {
+    constexpr int EPV = 16 / ES;
+    const int64_t v = static_cast<int64_t>(blockIdx.x) * kGammaThreads + threadIdx.x;  // vector of columns
+    if (v * EPV >= D) return;
+    const int64_t grp = blockIdx.y, G = gridDim.y;
+    float acc[EPV];
+#pragma unroll
+    for (int k = 0; k < EPV; ++k) acc[k] = 0.f;
+    for (int64_t i = grp; i < N; i += G) {
+        float fx[EPV], fd[EPV];
+        load8<ES>(X + (i * ldx + v * EPV) * ES, fx);
+        load8<ES>(dY + (i * lddy + v * EPV) * ES, fd);
+        const float r = rstd[i];
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) acc[k] = fmaf(fd[k], fx[k] * r, acc[k]);
+    }
+    float* p = part + grp * D + v * EPV;
+#pragma unroll
+    for (int k = 0; k < EPV; ++k) p[k] = acc[k];
+}
+
+__global__ void rmsnorm_dgamma_reduce(const float* __restrict__ part, int G, int64_t D, float* __restrict__ dgamma) {
+    for (int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; j < D;
+         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float s = 0.f;
+        for (int g = 0; g < G; ++g) s += part[g * D + j];
+        dgamma[j] = s;
+    }
+}
+
+int norm_grid(int64_t N) {
+    const int64_t rows_per_cta = kNormThreads / 32;
+    const int64_t want = (N + rows_per_cta - 1) / rows_per_cta;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(device_sm_count()) * 8)));
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_fwd(int es, const void* X, int64_t ldx, const void* gamma, int64_t N, int64_t D,
+                               float eps, void* Y, int64_t ldy, float* rstd, cudaStream_t s) {
+    if (N == 0) return cudaSuccess;
+    const int grid = norm_grid(N);
+    if (es == 2)
+        rmsnorm_fwd_kernel<2><<<grid, kNormThreads, 0, s>>>(static_cast<const char*>(X), ldx,
+                                                            static_cast<const char*>(gamma), N, D, eps,
+                                                            static_cast<char*>(Y), ldy, rstd);
+    else
+        rmsnorm_fwd_kernel<4><<<grid, kNormThreads, 0, s>>>(static_cast<const char*>(X), ldx,
+                                                            static_cast<const char*>(gamma), N, D, eps,
+                                                            static_cast<char*>(Y), ldy, rstd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void* X, int64_t ldx, const void* gamma,
+                               const float* rstd, int64_t N, int64_t D, void* dX, int64_t lddx, float* part,
+                               float* dgamma, cudaStream_t s) {
+    if (N > 0) {
+        const int grid = norm_grid(N);
+        if (es == 2)
+            rmsnorm_bwd_kernel<2><<<grid, kNormThreads, 0, s>>>(static_cast<const char*>(dY), lddy,
+                                                                static_cast<const char*>(X), ldx,
+                                                                static_cast<const char*>(gamma), rstd, N, D,
+                                                                static_cast<char*>(dX), lddx);
+        else
+            rmsnorm_bwd_kernel<4><<<grid, kNormThreads, 0, s>>>(static_cast<const char*>(dY), lddy,
+                                                                static_cast<const char*>(X), ldx,
+                                                                static_cast<const char*>(gamma), rstd, N, D,
+                                                                static_cast<char*>(dX), lddx);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (!dgamma) return cudaSuccess;
+    const int epv = 16 / es;
+    const dim3 ggrid(static_cast<unsigned>((D / epv + kGammaThreads - 1) / kGammaThreads), kRmsGammaGroups);
+    if (es == 2)
+        rmsnorm_dgamma_kernel<2><<<ggrid, kGammaThreads, 0, s>>>(static_cast<const char*>(dY), lddy,
+                                                                 static_cast<const char*>(X), ldx, rstd, N, D,
+                                                                 part);
+    else
+        rmsnorm_dgamma_kernel<4><<<ggrid, kGammaThreads, 0, s>>>(static_cast<const char*>(dY), lddy,
+                                                                 static_cast<const char*>(X), ldx, rstd, N, D,
+                                                                 part);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + 255) / 256)), 256, 0, s>>>(
+        part, kRmsGammaGroups, D, dgamma);
+    return cudaGetLastError();
+}
+
+}  // namespace foak

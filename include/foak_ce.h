@@ -183,6 +183,67 @@ foak_status foak_ce_fwd_bwd_host(const void* host_logits, int32_t dtype, int64_t
                                  int32_t* host_err, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * RMSNorm, the "Fast RMS LayerNorm" kernel the FOAK pages list among their fused
+ * operations (fms-acceleration-foak 0.7.4 page; its patch rule swaps a decoder's
+ * RMSNorm module for fast_rms_layernorm).  The pages print no formula; the
+ * operation is the Llama / Mistral / Granite RMSNorm, in fp32, rounded once:
+ *     r_i = 1 / sqrt(mean_j X_ij^2 + eps),   Y_ij = X_ij * r_i * gamma_j
+ *   X (device)      N x D in dtype (bf16 or fp32), row stride ldx elements
+ *   gamma (device)  D in dtype
+ *   Y (device)      N x D in dtype, row stride ldy (may equal X)
+ *   rstd (device)   float[N] or NULL: r_i, needed by the backward
+ * D % 8 == 0; X, Y, gamma 16-byte aligned with 16-byte row strides; eps >= 0.
+ */
+foak_status foak_rmsnorm_forward(const void* X, int32_t dtype, int64_t ldx, const void* gamma, int64_t N, int64_t D,
+                                 float eps, void* Y, int64_t ldy, float* rstd, void* stream);
+
+/* Bytes of device workspace foak_rmsnorm_backward needs for dgamma (64 x D floats). */
+size_t foak_rmsnorm_workspace_size(int64_t D);
+
+/*
+ * RMSNorm backward: with xh = X * r and u = gamma * dY (per row),
+ *     dX = r * (u - xh * mean(xh * u)),    dgamma_j = sum_i dY_ij * xh_ij
+ *   dY, X (device)  N x D in dtype (row strides lddy, ldx); rstd from the forward
+ *   dX (device)     N x D in dtype, row stride lddx (may equal dY)
+ *   dgamma (device) float32[D], overwritten, or NULL to skip it; it is summed in a
+ *                   fixed order (deterministic) through `workspace`
+ *                   (foak_rmsnorm_workspace_size(D) bytes, 256-byte aligned)
+ * Alignment as for the forward.
+ */
+foak_status foak_rmsnorm_backward(const void* dY, int64_t lddy, const void* X, int64_t ldx, const void* gamma,
+                                  const float* rstd, int32_t dtype, int64_t N, int64_t D, void* dX, int64_t lddx,
+                                  float* dgamma, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of device workspace foak_rmsnorm_linear_ce_chunked needs: the chunked
+ * linear + CE workspace, the normalised hidden states H and their gradient dH
+ * (bf16 N x D each), r (float[N]) and the dgamma partials.
+ */
+size_t foak_rmsnorm_linear_ce_workspace_size(int64_t N, int64_t V, int64_t D, int64_t chunk);
+
+/*
+ * The decoder's tail: final RMSNorm -> LM head -> cross-entropy, the norm and the
+ * chunked linear + CE of the FOAK pages composed on the device (the norm as the
+ * chunked path's prologue and its backward as the epilogue; H and dH never leave
+ * the device, the logits are never materialised):
+ *     H = rmsnorm(X, gamma, eps) (bf16), loss / dH / dW as foak_linear_ce_chunked on
+ *     H, then dX, dgamma through the norm (the rounding of H to bf16 is passed
+ *     through as the identity).
+ *   X (device)       bf16 [N][D] dense (row stride D), D % 8 == 0
+ *   gamma (device)   bf16 [D]
+ *   W, labels, chunk, g, denom, loss, dW, n_valid, err: as foak_linear_ce_chunked
+ *   eps              >= 0 (1e-5 for Mistral and Llama-3)
+ *   dX (device)      bf16 [N][D], overwritten
+ *   dgamma (device)  float32 [D], overwritten
+ * All pointers 16-byte aligned (loss, dgamma, n_valid, err: 4-byte).
+ */
+foak_status foak_rmsnorm_linear_ce_chunked(const void* X, const void* gamma, const void* W, const int64_t* labels,
+                                           int64_t N, int64_t V, int64_t D, int64_t ignore_index, int64_t chunk,
+                                           float eps, float g, float denom, float* loss, void* dX, float* dgamma,
+                                           float* dW, int32_t* n_valid, int32_t* err, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace foak_linear_ce_chunked needs: a 256-byte header, N
  * float32 per-row loss terms, a few error words and two chunks of bf16 logits
  * (min(2 chunk, N) x V, rows padded to 64 elements: dW is updated once per pair

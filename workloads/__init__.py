@@ -43,7 +43,7 @@ IGNORE_INDEX = -100
 F32, BF16 = 0, 1
 
 # stream ids (any distinct constants)
-S_LOGITS, S_SPIKE, S_LABELS, S_IGNORE, S_SEQLEN, S_PROMPT, S_H, S_W = range(1, 9)
+S_LOGITS, S_SPIKE, S_LABELS, S_IGNORE, S_SEQLEN, S_PROMPT, S_H, S_W, S_X, S_GAMMA = range(1, 11)
 
 
 def build_lib(force: bool = False) -> str:
@@ -230,6 +230,21 @@ def chunked(seed: int = SEED_BASE + 5, n: int = 8192, v: int = 32000, d: int = 4
     y = uniform_labels(n, v, seed=seed)
     y[pick_rows(n, round(0.1 * n), seed=seed)] = IGNORE_INDEX
     return dict(name="chunked", H=h, W=w, labels=y, N=n, V=v, D=d, chunk=chunk, g=1.0, seed=seed)
+
+
+def norm_chunked(seed: int = SEED_BASE + 6, n: int = 8192, v: int = 32000, d: int = 4096,
+                 chunk: int = 1024, eps: float = 1e-5):
+    """The decoder's tail -- final RMSNorm, LM head, cross-entropy -- at the chunked
+    workload's sizes: X 8192x4096 bf16 ~N(0, 2^2) (pre-norm hidden states), gamma
+    bf16 ~N(1, 0.1^2) (a trained norm weight near one), W and labels as ``chunked``."""
+    x = normal_matrix(n, d, seed=seed, sigma=2.0, dtype=BF16, stream=S_X)
+    gz = normal_matrix(1, d, seed=seed, sigma=0.1, dtype=F32, stream=S_GAMMA)[0].astype(np.float64)
+    gamma = f64_to_bf16_bits(1.0 + gz)
+    w = normal_matrix(v, d, seed=seed, sigma=0.02, dtype=BF16, stream=S_W)
+    y = uniform_labels(n, v, seed=seed)
+    y[pick_rows(n, round(0.1 * n), seed=seed)] = IGNORE_INDEX
+    return dict(name="norm_chunked", X=x, gamma=gamma, W=w, labels=y, N=n, V=v, D=d, chunk=chunk, eps=eps, g=1.0,
+                seed=seed)
 
 
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
