@@ -12,8 +12,8 @@
 // (from L1: 8 KB at D = 4096 bf16) and writes.  HBM traffic is the algorithmic
 // one: forward reads X and writes Y; backward reads dY and X and writes dX.  dgamma
 // is a column reduction over rows: a separate kernel gives each thread 8
-// consecutive columns and one of 64 row groups, writes per-group partials, and a
-// last kernel sums the 64 partials in a fixed order -- deterministic, no atomics.
+// consecutive columns and one of 128 row groups, writes per-group partials, and a
+// last kernel sums the 128 partials in a fixed order -- deterministic, no atomics.
 #include <algorithm>
 
 #include "common.cuh"
@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(kGammaThreads) rmsnorm_dgamma_kernel(const cha
     float acc[EPV];
 #pragma unroll
     for (int k = 0; k < EPV; ++k) acc[k] = 0.f;
-    for (int64_t i = grp; i < N; i += G) {
+#pragma unroll 4
+    for (int64_t i = grp; i < N; i += G) {  // unrolled: several rows' loads in flight per thread
         float fx[EPV], fd[EPV];
         load8<ES>(X + (i * ldx + v * EPV) * ES, fx);
         load8<ES>(dY + (i * lddy + v * EPV) * ES, fd);
@@ -152,9 +153,18 @@ __global__ void __launch_bounds__(kGammaThreads) rmsnorm_dgamma_kernel(const cha
 __global__ void rmsnorm_dgamma_reduce(const float* __restrict__ part, int G, int64_t D, float* __restrict__ dgamma) {
     for (int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; j < D;
          j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float s = 0.f;
-        for (int g = 0; g < G; ++g) s += part[g * D + j];
-        dgamma[j] = s;
+        // fixed order: four interleaved running sums over the groups, added at the end
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int g = 0;
+#pragma unroll 4
+        for (; g + 4 <= G; g += 4) {
+            s0 += part[(g + 0) * D + j];
+            s1 += part[(g + 1) * D + j];
+            s2 += part[(g + 2) * D + j];
+            s3 += part[(g + 3) * D + j];
+        }
+        for (; g < G; ++g) s0 += part[g * D + j];
+        dgamma[j] = (s0 + s1) + (s2 + s3);
     }
 }
 
@@ -212,7 +222,7 @@ cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void*
                                                                  part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + 255) / 256)), 256, 0, s>>>(
+    rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + 63) / 64)), 64, 0, s>>>(
         part, kRmsGammaGroups, D, dgamma);
     return cudaGetLastError();
 }

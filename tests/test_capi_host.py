@@ -132,3 +132,36 @@ def test_host_entry_argument_errors(so):
         assert _host(so) == E.FOAK_ERR_CUDA
     finally:
         so.lib.foak_test_fail_next_launches(0)
+
+
+def test_rmsnorm_entries_argument_errors(so):
+    """The RMSNorm calls reject bad sizes, dtypes and alignments before any launch."""
+    E = so
+    L = so.lib
+    assert L.foak_rmsnorm_workspace_size(4096) == 128 * 4096 * 4
+    assert L.foak_rmsnorm_workspace_size(0) == 0
+    fwd = lambda X=FAKE, dt=1, ldx=64, g=FAKE, N=4, D=64, eps=1e-5, Y=FAKE, ldy=64, r=FAKE: (  # noqa: E731
+        L.foak_rmsnorm_forward(X, dt, ldx, g, N, D, eps, Y, ldy, r, None))
+    assert fwd(dt=2) == E.FOAK_ERR_UNSUPPORTED
+    assert fwd(D=60, ldx=60, ldy=60) == E.FOAK_ERR_UNSUPPORTED       # D % 8
+    assert fwd(ldx=32) == E.FOAK_ERR_INVALID_ARG                     # ld < D
+    assert fwd(eps=-1.0) == E.FOAK_ERR_INVALID_ARG
+    assert fwd(X=FAKE + 2) == E.FOAK_ERR_INVALID_ARG                 # rows start on 16 bytes
+    assert fwd(ldx=68) == E.FOAK_ERR_INVALID_ARG                     # 136-byte row stride
+    assert fwd(g=None) == E.FOAK_ERR_INVALID_ARG
+    bwd = lambda dY=FAKE, r=FAKE, dg=FAKE, ws=FAKE, wsb=1 << 20: (  # noqa: E731
+        L.foak_rmsnorm_backward(dY, 64, FAKE, 64, FAKE, r, 1, 4, 64, FAKE, 64, dg, ws, wsb, None))
+    assert bwd(dY=None) == E.FOAK_ERR_INVALID_ARG
+    assert bwd(r=None) == E.FOAK_ERR_INVALID_ARG
+    assert bwd(wsb=16) == E.FOAK_ERR_WORKSPACE
+    assert bwd(ws=None) == E.FOAK_ERR_WORKSPACE
+    assert L.foak_rmsnorm_linear_ce_workspace_size(8192, 32000, 4096, 1024) > 2 * 8192 * 4096 * 2
+    tail = lambda X=FAKE, g=FAKE, D=64, eps=1e-5, dg=FAKE, wsb=1 << 30: (  # noqa: E731
+        L.foak_rmsnorm_linear_ce_chunked(X, g, FAKE, FAKE, 4, 100, D, -100, 1024, eps, 1.0, 0.0, FAKE, FAKE, dg,
+                                         FAKE, None, None, FAKE, wsb, None))
+    assert tail(D=60) == E.FOAK_ERR_UNSUPPORTED
+    assert tail(eps=-0.5) == E.FOAK_ERR_INVALID_ARG
+    assert tail(g=None) == E.FOAK_ERR_INVALID_ARG
+    assert tail(dg=None) == E.FOAK_ERR_INVALID_ARG
+    assert tail(X=FAKE + 8) == E.FOAK_ERR_INVALID_ARG
+    assert tail(wsb=1024) == E.FOAK_ERR_WORKSPACE
