@@ -21,6 +21,8 @@ reading is the textbook one, stated in ``ce_oracle.c``):
 * ``rmsnorm`` / ``rmsnorm_backward`` / ``rmsnorm_linear_ce`` -- the RMSNorm the
   foak page lists among its kernels ("Fast RMS LayerNorm Triton Kernels"), alone
   and as the final norm in front of the chunked linear + cross-entropy.
+* ``rope`` / ``rope_angles`` -- the rotary position embedding the foak page lists
+  ("Fast RoPE Triton Kernels"), with explicit position ids.
 
 Parity pins (closed forms, invariants, finite differences, brute force, a
 hand-worked example) live in ``tests/test_oracle_pins.py``; every function here
@@ -224,3 +226,33 @@ def rmsnorm_linear_ce(X: np.ndarray, gamma: np.ndarray, W: np.ndarray, labels: n
     dX, dgamma = rmsnorm_backward(res["dH"], X, gamma, eps)
     res.update(H=H, rstd=r, dX=dX, dgamma=dgamma)
     return res
+
+
+# --------------------------------------------------------------------- RoPE
+# "Fast RoPE Triton Kernels" (fms-acceleration-foak 0.7.4 page, list of fused
+# operations and kernels; its Known Issues, and "Notes on FastKernels" of
+# fms-hf-tuning PR #280, say the FOAK version takes no position_ids).  The pages
+# print no formula; the reading taken is the rotary embedding of the Llama /
+# Mistral decoders in the "rotate half" pairing: for head dimension d and
+# i < d/2, element i pairs with element i + d/2 and the pair turns by
+#     theta(p, i) = p * base^(-2i/d),   p = the token's position id.
+
+def rope_angles(positions: np.ndarray, d: int, base: float) -> np.ndarray:
+    """theta[t, i] = positions[t] * base^(-2i/d), float64, shape (T, d/2)."""
+    i = np.arange(d // 2, dtype=np.float64)
+    inv_freq = np.power(float(base), -2.0 * i / d)
+    return np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]
+
+
+def rope(X: np.ndarray, positions: np.ndarray, base: float, *, inverse: bool = False) -> np.ndarray:
+    """Rotate every head vector of X (T x H x d, any float dtype or bf16 bits) by its
+    token's angles; ``inverse`` turns by -theta (the backward: the rotation is
+    orthogonal, so the gradient of sum(G * rope(X)) is rope(G, inverse=True))."""
+    Xd = _to_f64(X)
+    T, H, d = Xd.shape
+    th = rope_angles(positions, d, base)
+    c, s = np.cos(th)[:, None, :], np.sin(th)[:, None, :]
+    if inverse:
+        s = -s
+    lo, hi = Xd[..., : d // 2], Xd[..., d // 2:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)

@@ -353,3 +353,42 @@ def test_rmsnorm_linear_ce_matches_finite_differences():
     np.testing.assert_allclose(res["dgamma"], _fd(lambda gg: L(X, gg, W), g, 1e-5), rtol=1e-6, atol=1e-9)
     np.testing.assert_allclose(res["dW"], _fd(lambda w: L(X, g, w), W, 1e-5), rtol=1e-6, atol=1e-9)
     assert res["n_valid"] == 3
+
+
+# ------------------------------------------------------------------ RoPE pins
+
+def test_rope_hand_worked_and_identity():
+    # d = 4, base 100: angles (p, p / 10); q = e0 at p = 1 turns into (cos 1, 0, sin 1, 0)
+    out = oracle.rope(np.array([[[1.0, 0.0, 0.0, 0.0]]]), np.array([1]), 100.0)
+    np.testing.assert_allclose(out[0, 0], [math.cos(1.0), 0.0, math.sin(1.0), 0.0], atol=1e-16)
+    # the second pair (elements 1 and 3) turns by 0.1 rad at p = 1
+    out = oracle.rope(np.array([[[0.0, 2.0, 0.0, 0.0]]]), np.array([1]), 100.0)
+    np.testing.assert_allclose(out[0, 0], [0.0, 2 * math.cos(0.1), 0.0, 2 * math.sin(0.1)], atol=1e-15)
+    # position 0 is the identity
+    X = np.random.default_rng(1).normal(size=(3, 2, 8))
+    np.testing.assert_array_equal(oracle.rope(X, np.zeros(3, dtype=np.int64), 1e4), X)
+
+
+def test_rope_is_a_rotation_and_relative():
+    rng = np.random.default_rng(2)
+    X = rng.normal(size=(5, 3, 16))
+    p = np.array([0, 7, 100, 4095, 8191])
+    Y = oracle.rope(X, p, 5e5)
+    # each (i, i + d/2) pair keeps its length; the inverse turns it back
+    half = 8
+    np.testing.assert_allclose(Y[..., :half] ** 2 + Y[..., half:] ** 2, X[..., :half] ** 2 + X[..., half:] ** 2,
+                               rtol=1e-12)
+    np.testing.assert_allclose(oracle.rope(Y, p, 5e5, inverse=True), X, atol=1e-12)
+    # the defining property: <rope(q, m), rope(k, n)> depends on m - n only
+    q, k = rng.normal(size=(1, 1, 16)), rng.normal(size=(1, 1, 16))
+    a = np.sum(oracle.rope(q, np.array([10]), 1e4) * oracle.rope(k, np.array([3]), 1e4))
+    b = np.sum(oracle.rope(q, np.array([1007]), 1e4) * oracle.rope(k, np.array([1000]), 1e4))
+    assert a == pytest.approx(b, rel=1e-10)
+
+
+def test_rope_backward_matches_finite_differences():
+    rng = np.random.default_rng(3)
+    X, G, p = rng.normal(size=(2, 2, 6)), rng.normal(size=(2, 2, 6)), np.array([3, 11])
+    dX = oracle.rope(G, p, 1e4, inverse=True)
+    fd = _fd(lambda x: float(np.sum(G * oracle.rope(x, p, 1e4))), X)
+    np.testing.assert_allclose(dX, fd, rtol=1e-8, atol=1e-10)
