@@ -479,6 +479,8 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
 
 CHUNKED_DESC = ("chunked linear+CE: H 8192x4096 bf16 ~N(0,1), W 32000x4096 bf16 ~N(0,0.02^2), 10% rows -100, "
                 "chunks of 1024 rows")
+ROPE_DESC = ("rotary embedding, Llama-3-8B attention shapes: Q 8192x32x128 and K 8192x8x128 bf16 ~N(0,1), "
+             "packed sequences of up to 2048 tokens (position ids restart per sequence), base 500000")
 NORM_TAIL_DESC = ("decoder tail: RMSNorm (eps 1e-5) of X 8192x4096 bf16 ~N(0,2^2), gamma ~N(1,0.1^2) -> "
                   "chunked LM head W 32000x4096 + CE, 10% rows -100, chunks of 1024 rows")
 
@@ -545,6 +547,24 @@ def chunked_timing(ce, torch, dev, stream, steps=5, warmup=2):
                     "peak_source": hsrc,
                     "bytes": "forward: read X, write Y; backward: read dY and X twice (dX, then dgamma), write dX"})
     del X, dX, Y
+    # rotary embedding on Llama-3-8B attention shapes (Q and K in place; HBM-bound)
+    r = wl.rope_llama3()
+    q = torch.from_numpy(r["Q"].view(np.int16)).to(dev).view(torch.bfloat16)
+    k = torch.from_numpy(r["K"].view(np.int16)).to(dev).view(torch.bfloat16)
+    pos = torch.from_numpy(r["positions"]).to(dev)
+    cache = ce.foak_rope_cache(r["max_pos"], r["d"], base=r["base"], device=dev)
+
+    def rope_step():
+        ce.foak_rope_apply(q, pos, cache)
+        ce.foak_rope_apply(k, pos, cache)
+
+    ms_r = timed(rope_step, 20, 3)
+    byts = 2 * (q.numel() + k.numel()) * 2 + 8 * pos.numel()
+    gbs = byts / (ms_r * 1e-3) / 1e9
+    res.append({"path": "foak_rope_apply (Q then K, in place)", "workload": ROPE_DESC, "steps": 20,
+                "ms_per_step": ms_r, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm, "peak_source": hsrc,
+                "bytes": "Q and K read and written once, positions; the 4 MB cos/sin table stays in L2"})
+    del q, k, cache
     # the three products of one chunk, alone
     Z = torch.empty(chunk, V, dtype=torch.bfloat16, device=dev)
     Zs = torch.randn(chunk, V, device=dev).to(torch.bfloat16)

@@ -50,6 +50,9 @@ SIGNATURES = {
     "foak_rmsnorm_linear_ce_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
     "foak_rmsnorm_linear_ce_chunked": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _f32, _f32, _f32,
                                               _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "foak_rope_cache_size": (_sz, [_i64, _i64]),
+    "foak_rope_build_cache": (_i32, [ctypes.c_double, _i64, _i64, _vp, _sz, _vp]),
+    "foak_rope_apply": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _vp]),
     "foak_ce_host_workspace_size": (_sz, [_i64]),
     "foak_ce_fwd_bwd_host": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _sz, _vp]),
@@ -445,3 +448,35 @@ def foak_rmsnorm_linear_ce_chunked(X, gamma, W, labels, *, eps: float = 1e-5, ch
                                             _stream(dev, stream))
     _check(st, "foak_rmsnorm_linear_ce_chunked")
     return dict(loss=loss, dX=dX, dgamma=dgamma, dW=dW, n_valid=n_valid, err=err)
+
+
+# --------------------------------------------------------------------- RoPE
+def foak_rope_cache(max_pos: int, d: int, base: float = 10000.0, device="cuda", stream=None):
+    """The cos/sin table for positions [0, max_pos) and head dimension d (uint8 device tensor)."""
+    need = int(lib.foak_rope_cache_size(int(max_pos), int(d)))
+    if need == 0:
+        raise ValueError("unsupported max_pos / d (d must be a multiple of 16)")
+    dev = torch.device(device)
+    cache = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = lib.foak_rope_build_cache(float(base), int(d), int(max_pos), _ptr(cache), need, _stream(dev, stream))
+    _check(st, "foak_rope_build_cache")
+    cache.max_pos, cache.head_dim = int(max_pos), int(d)
+    return cache
+
+
+def foak_rope_apply(x, positions, cache, *, inverse: bool = False, stream=None):
+    """Rotate ``x`` (T x H x d bf16/fp32 CUDA view, heads contiguous) in place by the
+    angles of ``positions`` (int64 [T]); returns the device error word."""
+    if x.dim() != 3 or x.stride(2) != 1 or x.stride(1) != x.shape[2] or x.dtype not in _DT or not x.is_cuda:
+        raise ValueError("x must be a T x H x d CUDA view with contiguous heads")
+    T, H, d = x.shape
+    if d != cache.head_dim:
+        raise ValueError("cache built for another head dimension")
+    if positions.dtype != torch.int64 or positions.numel() != T or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous int64 vector of length T")
+    ldt = x.stride(0) if T > 1 else H * d
+    err = torch.empty(1, dtype=torch.int32, device=x.device)
+    st = lib.foak_rope_apply(_ptr(x), _DT[x.dtype], T, H, ldt, d, _ptr(positions), _ptr(cache), cache.max_pos,
+                             1 if inverse else 0, _ptr(err), _stream(x.device, stream))
+    _check(st, "foak_rope_apply")
+    return err

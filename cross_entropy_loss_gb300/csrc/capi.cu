@@ -366,6 +366,41 @@ foak_status foak_rmsnorm_linear_ce_chunked(const void* X, const void* gamma, con
     return finish(e, err, s);
 }
 
+size_t foak_rope_cache_size(int64_t max_pos, int64_t d) {
+    if (max_pos < 1 || d < 16 || d % 16 || d > (1 << 16)) return 0;
+    return rope_cache_bytes(max_pos, static_cast<int>(d));
+}
+
+foak_status foak_rope_build_cache(double base, int64_t d, int64_t max_pos, void* cache, size_t cache_bytes,
+                                  void* stream) {
+    if (max_pos < 1 || !(base > 1.0)) return FOAK_ERR_INVALID_ARG;
+    if (d < 16 || d % 16 || d > (1 << 16)) return FOAK_ERR_UNSUPPORTED;
+    if (!cache || !aligned(cache, 256)) return FOAK_ERR_INVALID_ARG;
+    if (cache_bytes < rope_cache_bytes(max_pos, static_cast<int>(d))) return FOAK_ERR_WORKSPACE;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(launch_rope_cache(base, static_cast<int>(d), max_pos, cache, s), nullptr, s);
+}
+
+foak_status foak_rope_apply(void* X, int32_t dtype, int64_t T, int64_t H, int64_t ldt, int64_t d,
+                            const int64_t* positions, const void* cache, int64_t max_pos, int32_t inverse,
+                            int32_t* err, void* stream) {
+    const int es = elem_bytes_of(dtype);
+    if (!es) return FOAK_ERR_UNSUPPORTED;
+    if (d < 16 || d % 16 || d > (1 << 16)) return FOAK_ERR_UNSUPPORTED;
+    if (T < 0 || H < 0 || H > 0x7fffffffLL || max_pos < 1 || ldt < H * d) return FOAK_ERR_INVALID_ARG;
+    if (!cache || !aligned(cache, 256) || (err && !aligned(err, 4))) return FOAK_ERR_INVALID_ARG;
+    if (T > 0 && H > 0 && (!X || !positions || !aligned(X, 16) || (ldt * es) % 16 || !aligned(positions, 8)))
+        return FOAK_ERR_INVALID_ARG;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = err ? cudaMemsetAsync(err, 0, sizeof(int32_t), s) : cudaSuccess;
+    if (e == cudaSuccess)
+        e = launch_rope_apply(es, X, T, static_cast<int>(H), ldt, static_cast<int>(d), positions, cache, max_pos,
+                              inverse != 0, err, s);
+    return finish(e, err, s);
+}
+
 foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const void* b, int64_t ldb,
                            int32_t b_mn_major, int64_t M, int64_t N, int64_t K, void* out, int64_t ldo,
                            int32_t out_mode, int32_t* err, void* stream) {

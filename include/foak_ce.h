@@ -244,6 +244,48 @@ foak_status foak_rmsnorm_linear_ce_chunked(const void* X, const void* gamma, con
                                            size_t workspace_bytes, void* stream);
 
 /*
+ * Rotary position embedding, the "Fast RoPE" kernel the FOAK pages list among
+ * their fused operations (fms-acceleration-foak 0.7.4 page), with the explicit
+ * position ids the pages note the FOAK version lacks (foak page, Known Issues;
+ * fms-hf-tuning PR #280, Notes on FastKernels).  The pages print no formula; the
+ * operation is the Llama / Mistral rotary embedding, "rotate half" pairing: for
+ * head dimension d and i < d/2, elements i and i + d/2 of every head vector of
+ * token t turn by theta = positions[t] * base^(-2i/d).
+ *
+ * Bytes of the cos/sin table for positions [0, max_pos) and head dimension d
+ * (two fp32 planes of max_pos x d/2); 0 for an unsupported d (d % 16 != 0).
+ */
+size_t foak_rope_cache_size(int64_t max_pos, int64_t d);
+
+/*
+ * Build the table on the device: cos and sin of every (position, frequency),
+ * the angle and its reduction in float64, stored as fp32.  base > 1 (10000 for
+ * Llama-2 / Mistral, 500000 for Llama-3).  cache (device): 256-byte aligned,
+ * foak_rope_cache_size(max_pos, d) bytes, owned by the caller; build it once per
+ * (base, d, max_pos) and reuse it.
+ */
+foak_status foak_rope_build_cache(double base, int64_t d, int64_t max_pos, void* cache, size_t cache_bytes,
+                                  void* stream);
+
+/*
+ * Apply the rotation in place (inverse != 0: turn by -theta, the backward: the
+ * gradient of sum(G * rope(X)) is rope(G, inverse)).
+ *   X (device)          T tokens x H heads x d in dtype (bf16 or fp32); heads of a
+ *                       token contiguous, token stride ldt >= H*d elements (so Q
+ *                       and K may be views into a fused QKV buffer); 16-byte
+ *                       aligned, ldt * sizeof(dtype) % 16 == 0
+ *   positions (device)  int64[T]: the token's position id (restarting at 0 per
+ *                       sequence in a packed batch)
+ *   cache (device)      the table of foak_rope_build_cache for max_pos, d
+ *   err (device)        int32[1] or NULL: FOAK_ERRBIT_LABEL_RANGE when a position
+ *                       is outside [0, max_pos); that token is left unchanged
+ * d % 16 == 0 (FOAK_ERR_UNSUPPORTED otherwise).
+ */
+foak_status foak_rope_apply(void* X, int32_t dtype, int64_t T, int64_t H, int64_t ldt, int64_t d,
+                            const int64_t* positions, const void* cache, int64_t max_pos, int32_t inverse,
+                            int32_t* err, void* stream);
+
+/*
  * Bytes of device workspace foak_linear_ce_chunked needs: a 256-byte header, N
  * float32 per-row loss terms, a few error words and two chunks of bf16 logits
  * (min(2 chunk, N) x V, rows padded to 64 elements: dW is updated once per pair

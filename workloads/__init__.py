@@ -247,6 +247,30 @@ def norm_chunked(seed: int = SEED_BASE + 6, n: int = 8192, v: int = 32000, d: in
                 seed=seed)
 
 
+def packed_positions(n: int, *, seed: int, max_len: int = 2048) -> np.ndarray:
+    """Position ids of a padding-free packed batch: sequences of lengths U{64..max_len}
+    (the last truncated) laid end to end, each counting from 0."""
+    pos = np.empty(n, dtype=np.int64)
+    at, k = 0, 0
+    while at < n:
+        L = 64 + int(np.floor(uniform(seed, S_SEQLEN, 1, start=k)[0] * (max_len - 64 + 1)))
+        L = min(L, n - at)
+        pos[at:at + L] = np.arange(L)
+        at += L
+        k += 1
+    return pos
+
+
+def rope_llama3(dtype: int = BF16, seed: int = SEED_BASE + 7, tokens: int = 8192):
+    """Llama-3-8B attention shapes for the rotary embedding: Q (T x 32 x 128) and K
+    (T x 8 x 128) ~N(0, 1) in a packed batch of sequences up to 2048 tokens, rope
+    base 500000, table for 8192 positions."""
+    q = normal_matrix(tokens, 32 * 128, seed=seed, sigma=1.0, dtype=dtype, stream=S_X).reshape(tokens, 32, 128)
+    k = normal_matrix(tokens, 8 * 128, seed=seed, sigma=1.0, dtype=dtype, stream=S_H).reshape(tokens, 8, 128)
+    return dict(name="rope_llama3", Q=q, K=k, positions=packed_positions(tokens, seed=seed), base=500000.0,
+                max_pos=8192, d=128, dtype=dtype, seed=seed)
+
+
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float64 (plain data conversion)."""
     return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
