@@ -555,13 +555,12 @@ def chunked_timing(ce, torch, dev, stream, steps=5, warmup=2):
     cache = ce.foak_rope_cache(r["max_pos"], r["d"], base=r["base"], device=dev)
 
     def rope_step():
-        ce.foak_rope_apply(q, pos, cache)
-        ce.foak_rope_apply(k, pos, cache)
+        ce.foak_rope_apply_qk(q, k, pos, cache)
 
     ms_r = timed(rope_step, 20, 3)
     byts = 2 * (q.numel() + k.numel()) * 2 + 8 * pos.numel()
     gbs = byts / (ms_r * 1e-3) / 1e9
-    res.append({"path": "foak_rope_apply (Q then K, in place)", "workload": ROPE_DESC, "steps": 20,
+    res.append({"path": "foak_rope_apply_qk (Q and K in one launch, in place)", "workload": ROPE_DESC, "steps": 20,
                 "ms_per_step": ms_r, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm, "peak_source": hsrc,
                 "bytes": "Q and K read and written once, positions; the 4 MB cos/sin table stays in L2"})
     del q, k, cache

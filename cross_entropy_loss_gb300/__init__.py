@@ -53,6 +53,8 @@ SIGNATURES = {
     "foak_rope_cache_size": (_sz, [_i64, _i64]),
     "foak_rope_build_cache": (_i32, [ctypes.c_double, _i64, _i64, _vp, _sz, _vp]),
     "foak_rope_apply": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _vp]),
+    "foak_rope_apply_qk": (_i32, [_vp, _i64, _i64, _vp, _i64, _i64, _i32, _i64, _i64, _vp, _vp, _i64, _i32, _vp,
+                                  _vp]),
     "foak_ce_host_workspace_size": (_sz, [_i64]),
     "foak_ce_fwd_bwd_host": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _sz, _vp]),
@@ -479,4 +481,27 @@ def foak_rope_apply(x, positions, cache, *, inverse: bool = False, stream=None):
     st = lib.foak_rope_apply(_ptr(x), _DT[x.dtype], T, H, ldt, d, _ptr(positions), _ptr(cache), cache.max_pos,
                              1 if inverse else 0, _ptr(err), _stream(x.device, stream))
     _check(st, "foak_rope_apply")
+    return err
+
+
+def foak_rope_apply_qk(q, k, positions, cache, *, inverse: bool = False, stream=None):
+    """Rotate Q (T x Hq x d) and K (T x Hk x d) in place in one launch; returns the error word."""
+    views = []
+    for x in (q, k):
+        if x.dim() != 3 or x.stride(2) != 1 or x.stride(1) != x.shape[2] or x.dtype not in _DT or not x.is_cuda:
+            raise ValueError("q and k must be T x H x d CUDA views with contiguous heads")
+        T, H, d = x.shape
+        views.append((H, x.stride(0) if T > 1 else H * d))
+    if q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2] or q.dtype != k.dtype:
+        raise ValueError("q and k disagree on tokens, head dimension or dtype")
+    T, _, d = q.shape
+    if d != cache.head_dim:
+        raise ValueError("cache built for another head dimension")
+    if positions.dtype != torch.int64 or positions.numel() != T or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous int64 vector of length T")
+    err = torch.empty(1, dtype=torch.int32, device=q.device)
+    (hq, ldq), (hk, ldk) = views
+    st = lib.foak_rope_apply_qk(_ptr(q), hq, ldq, _ptr(k), hk, ldk, _DT[q.dtype], T, d, _ptr(positions), _ptr(cache),
+                                cache.max_pos, 1 if inverse else 0, _ptr(err), _stream(q.device, stream))
+    _check(st, "foak_rope_apply_qk")
     return err

@@ -396,8 +396,31 @@ foak_status foak_rope_apply(void* X, int32_t dtype, int64_t T, int64_t H, int64_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = err ? cudaMemsetAsync(err, 0, sizeof(int32_t), s) : cudaSuccess;
     if (e == cudaSuccess)
-        e = launch_rope_apply(es, X, T, static_cast<int>(H), ldt, static_cast<int>(d), positions, cache, max_pos,
-                              inverse != 0, err, s);
+        e = launch_rope_apply(es, X, T, static_cast<int>(H), ldt, nullptr, 0, 0, static_cast<int>(d), positions, cache,
+                              max_pos, inverse != 0, err, s);
+    return finish(e, err, s);
+}
+
+foak_status foak_rope_apply_qk(void* Q, int64_t Hq, int64_t ldq, void* K, int64_t Hk, int64_t ldk, int32_t dtype,
+                               int64_t T, int64_t d, const int64_t* positions, const void* cache, int64_t max_pos,
+                               int32_t inverse, int32_t* err, void* stream) {
+    const int es = elem_bytes_of(dtype);
+    if (!es) return FOAK_ERR_UNSUPPORTED;
+    if (d < 16 || d % 16 || d > (1 << 16)) return FOAK_ERR_UNSUPPORTED;
+    if (T < 0 || Hq < 0 || Hk < 0 || Hq > 0x3fffffffLL || Hk > 0x3fffffffLL || max_pos < 1 || ldq < Hq * d ||
+        ldk < Hk * d)
+        return FOAK_ERR_INVALID_ARG;
+    if (!cache || !aligned(cache, 256) || (err && !aligned(err, 4))) return FOAK_ERR_INVALID_ARG;
+    if (T > 0 && (!positions || !aligned(positions, 8))) return FOAK_ERR_INVALID_ARG;
+    if (T > 0 && Hq > 0 && (!Q || !aligned(Q, 16) || (ldq * es) % 16)) return FOAK_ERR_INVALID_ARG;
+    if (T > 0 && Hk > 0 && (!K || !aligned(K, 16) || (ldk * es) % 16)) return FOAK_ERR_INVALID_ARG;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = err ? cudaMemsetAsync(err, 0, sizeof(int32_t), s) : cudaSuccess;
+    if (e == cudaSuccess)
+        e = launch_rope_apply(es, Hq > 0 ? Q : nullptr, T, static_cast<int>(Hq), ldq, Hk > 0 ? K : nullptr,
+                              static_cast<int>(Hk), ldk, static_cast<int>(d), positions, cache, max_pos, inverse != 0,
+                              err, s);
     return finish(e, err, s);
 }
 

@@ -72,8 +72,10 @@ cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void*
 // RoPE (rope.cu): cos and sin planes of max_pos x d/2 floats, each 256-byte aligned.
 size_t rope_cache_bytes(int64_t max_pos, int d);
 cudaError_t launch_rope_cache(double base, int d, int64_t max_pos, void* cache, cudaStream_t s);
-cudaError_t launch_rope_apply(int es, void* X, int64_t T, int H, int64_t ldt, int d, const int64_t* positions,
-                              const void* cache, int64_t max_pos, bool inverse, int32_t* err, cudaStream_t s);
+// X (H heads, token stride ldt) and, when X2 is non-null, X2 (H2 heads, ldt2) in one launch.
+cudaError_t launch_rope_apply(int es, void* X, int64_t T, int H, int64_t ldt, void* X2, int H2, int64_t ldt2, int d,
+                              const int64_t* positions, const void* cache, int64_t max_pos, bool inverse,
+                              int32_t* err, cudaStream_t s);
 
 uint64_t test_wait_limit_ns();
 int64_t test_skip_load_row();

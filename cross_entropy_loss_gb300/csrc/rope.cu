@@ -71,10 +71,16 @@ __device__ __forceinline__ void st8(char* p, const float (&f)[16 / ES]) {
     *reinterpret_cast<uint4*>(p) = v;
 }
 
-// X: T tokens x H heads x d, token stride ldt elements, heads contiguous (stride d).
+// Up to two tensors (Q and K) in one launch: tensor k is T tokens x H[k] heads x d,
+// token stride ldt[k] elements, heads contiguous (stride d).
+struct RopeTensors {
+    char* X[2];
+    int H[2];
+    int64_t ldt[2];
+};
+
 template <int ES>
-__global__ void __launch_bounds__(kRopeThreads) rope_apply_kernel(char* __restrict__ X, int64_t T, int H,
-                                                                  int64_t ldt, int d,
+__global__ void __launch_bounds__(kRopeThreads) rope_apply_kernel(const RopeTensors a, int64_t T, int d,
                                                                   const int64_t* __restrict__ positions,
                                                                   const float* __restrict__ cos_t,
                                                                   const float* __restrict__ sin_t, int64_t P,
@@ -82,9 +88,15 @@ __global__ void __launch_bounds__(kRopeThreads) rope_apply_kernel(char* __restri
     constexpr int EPV = 16 / ES;
     const int half = d / 2;
     const int per_head = half / EPV;  // vector pairs per head
-    const int64_t n = T * H * per_head;
-    for (int64_t w = blockIdx.x * static_cast<int64_t>(kRopeThreads) + threadIdx.x; w < n;
-         w += static_cast<int64_t>(gridDim.x) * kRopeThreads) {
+    const int64_t n0 = T * a.H[0] * per_head;
+    const int64_t n = n0 + T * a.H[1] * per_head;
+    for (int64_t w0 = blockIdx.x * static_cast<int64_t>(kRopeThreads) + threadIdx.x; w0 < n;
+         w0 += static_cast<int64_t>(gridDim.x) * kRopeThreads) {
+        const int which = w0 < n0 ? 0 : 1;
+        const int64_t w = which ? w0 - n0 : w0;
+        const int H = a.H[which];
+        const int64_t ldt = a.ldt[which];
+        char* X = a.X[which];
         const int j = static_cast<int>(w % per_head);
         const int64_t th = w / per_head;
         const int h = static_cast<int>(th % H);
@@ -135,23 +147,29 @@ cudaError_t launch_rope_cache(double base, int d, int64_t max_pos, void* cache, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_rope_apply(int es, void* X, int64_t T, int H, int64_t ldt, int d, const int64_t* positions,
-                              const void* cache, int64_t max_pos, bool inverse, int32_t* err, cudaStream_t s) {
-    if (T == 0 || H == 0) return cudaSuccess;
+cudaError_t launch_rope_apply(int es, void* X, int64_t T, int H, int64_t ldt, void* X2, int H2, int64_t ldt2, int d,
+                              const int64_t* positions, const void* cache, int64_t max_pos, bool inverse,
+                              int32_t* err, cudaStream_t s) {
+    if (T == 0 || H + H2 == 0) return cudaSuccess;
     const float* cos_t = static_cast<const float*>(cache);
     const float* sin_t =
         reinterpret_cast<const float*>(static_cast<const char*>(cache) + rope_cache_bytes(max_pos, d) / 2);
-    const int64_t n = T * H * (d / 2 / (16 / es));
+    RopeTensors a;
+    a.X[0] = static_cast<char*>(X);
+    a.H[0] = H;
+    a.ldt[0] = ldt;
+    a.X[1] = static_cast<char*>(X2);
+    a.H[1] = X2 ? H2 : 0;
+    a.ldt[1] = ldt2;
+    const int64_t n = T * (a.H[0] + a.H[1]) * (d / 2 / (16 / es));
     const int grid =
         static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + kRopeThreads - 1) / kRopeThreads,
                                                                 static_cast<int64_t>(device_sm_count()) * 8)));
     const float sign = inverse ? -1.f : 1.f;
     if (es == 2)
-        rope_apply_kernel<2><<<grid, kRopeThreads, 0, s>>>(static_cast<char*>(X), T, H, ldt, d, positions, cos_t,
-                                                           sin_t, max_pos, sign, err);
+        rope_apply_kernel<2><<<grid, kRopeThreads, 0, s>>>(a, T, d, positions, cos_t, sin_t, max_pos, sign, err);
     else
-        rope_apply_kernel<4><<<grid, kRopeThreads, 0, s>>>(static_cast<char*>(X), T, H, ldt, d, positions, cos_t,
-                                                           sin_t, max_pos, sign, err);
+        rope_apply_kernel<4><<<grid, kRopeThreads, 0, s>>>(a, T, d, positions, cos_t, sin_t, max_pos, sign, err);
     return cudaGetLastError();
 }
 

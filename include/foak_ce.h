@@ -286,6 +286,16 @@ foak_status foak_rope_apply(void* X, int32_t dtype, int64_t T, int64_t H, int64_
                             int32_t* err, void* stream);
 
 /*
+ * foak_rope_apply on the Q and K of one layer in a single launch: Q is T x Hq x d
+ * (token stride ldq), K is T x Hk x d (token stride ldk), both in dtype, same
+ * positions and table; either may be empty (H = 0, pointer may be NULL).  Rules
+ * and errors as foak_rope_apply.
+ */
+foak_status foak_rope_apply_qk(void* Q, int64_t Hq, int64_t ldq, void* K, int64_t Hk, int64_t ldk, int32_t dtype,
+                               int64_t T, int64_t d, const int64_t* positions, const void* cache, int64_t max_pos,
+                               int32_t inverse, int32_t* err, void* stream);
+
+/*
  * Bytes of device workspace foak_linear_ce_chunked needs: a 256-byte header, N
  * float32 per-row loss terms, a few error words and two chunks of bf16 logits
  * (min(2 chunk, N) x V, rows padded to 64 elements: dW is updated once per pair

@@ -117,3 +117,19 @@ def test_rope_llama3_full_size(cuda_lib, dtype):
         torch.cuda.synchronize()
         assert err.item() == 0
         _close(to_f64(x), oracle.rope(w[name], w["positions"], w["base"]), dtype)
+
+
+@pytest.mark.parametrize("inverse", [False, True])
+def test_rope_qk_one_launch_matches_separate_calls(cuda_lib, inverse):
+    """Q and K views of a fused QKV buffer rotated in one launch give the same bits as two calls."""
+    T, d = 333, 128
+    qkv = torch.randn(T, 48, d, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    two = qkv.clone()
+    pos = torch.from_numpy(wl.packed_positions(T, seed=5, max_len=100)).cuda()
+    cache = cuda_lib.foak_rope_cache(2048, d, base=500000.0)
+    err = cuda_lib.foak_rope_apply_qk(qkv[:, :32], qkv[:, 32:40], pos, cache, inverse=inverse)
+    cuda_lib.foak_rope_apply(two[:, :32], pos, cache, inverse=inverse)
+    cuda_lib.foak_rope_apply(two[:, 32:40], pos, cache, inverse=inverse)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(qkv.view(torch.int16), two.view(torch.int16))
