@@ -165,3 +165,29 @@ def test_rmsnorm_entries_argument_errors(so):
     assert tail(dg=None) == E.FOAK_ERR_INVALID_ARG
     assert tail(X=FAKE + 8) == E.FOAK_ERR_INVALID_ARG
     assert tail(wsb=1024) == E.FOAK_ERR_WORKSPACE
+
+
+def test_rope_entries_argument_errors(so):
+    """The RoPE calls reject bad head dimensions, strides and alignments before any launch."""
+    E = so
+    L = so.lib
+    assert L.foak_rope_cache_size(8192, 128) == 2 * 8192 * 64 * 4
+    assert L.foak_rope_cache_size(8192, 120) == 0                    # d % 16
+    assert L.foak_rope_cache_size(0, 128) == 0
+    assert L.foak_rope_build_cache(1e4, 120, 16, FAKE, 1 << 20, None) == E.FOAK_ERR_UNSUPPORTED
+    assert L.foak_rope_build_cache(0.5, 128, 16, FAKE, 1 << 20, None) == E.FOAK_ERR_INVALID_ARG   # base > 1
+    assert L.foak_rope_build_cache(1e4, 128, 16, FAKE + 16, 1 << 20, None) == E.FOAK_ERR_INVALID_ARG
+    assert L.foak_rope_build_cache(1e4, 128, 16, FAKE, 64, None) == E.FOAK_ERR_WORKSPACE
+    ap = lambda X=FAKE, dt=1, T=4, H=2, ldt=256, d=128, pos=FAKE, c=FAKE: (  # noqa: E731
+        L.foak_rope_apply(X, dt, T, H, ldt, d, pos, c, 16, 0, None, None))
+    assert ap(dt=2) == E.FOAK_ERR_UNSUPPORTED
+    assert ap(d=72, ldt=144) == E.FOAK_ERR_UNSUPPORTED
+    assert ap(ldt=255) == E.FOAK_ERR_INVALID_ARG                     # ldt < H * d
+    assert ap(X=FAKE + 2) == E.FOAK_ERR_INVALID_ARG
+    assert ap(ldt=260) == E.FOAK_ERR_INVALID_ARG                     # 520-byte token stride
+    assert ap(pos=None) == E.FOAK_ERR_INVALID_ARG
+    assert ap(c=FAKE + 64) == E.FOAK_ERR_INVALID_ARG                 # table 256-byte aligned
+    qk = lambda Q=FAKE, K=FAKE, ldk=128: (  # noqa: E731
+        L.foak_rope_apply_qk(Q, 2, 256, K, 1, ldk, 1, 4, 128, FAKE, FAKE, 16, 0, None, None))
+    assert qk(K=None) == E.FOAK_ERR_INVALID_ARG
+    assert qk(ldk=64) == E.FOAK_ERR_INVALID_ARG
