@@ -540,12 +540,12 @@ def chunked_timing(ce, torch, dev, stream, steps=5, warmup=2):
     ms_b = timed(lambda: ce.foak_rmsnorm_backward(Y, X, gam, rstd, dX=dX), 20, 3)
     nd2 = N * D * 2
     for name, ms_k, byts in (("foak_rmsnorm_forward", ms_f, 2 * nd2 + 4 * N),
-                             ("foak_rmsnorm_backward (dX and dgamma)", ms_b, 5 * nd2 + 4 * N)):
+                             ("foak_rmsnorm_backward (dX and dgamma)", ms_b, 3 * nd2 + 4 * N)):
         gbs = byts / (ms_k * 1e-3) / 1e9
         res.append({"path": name, "workload": "X 8192x4096 bf16 (the decoder tail's norm)", "steps": 20,
                     "ms_per_step": ms_k, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm,
                     "peak_source": hsrc,
-                    "bytes": "forward: read X, write Y; backward: read dY and X twice (dX, then dgamma), write dX"})
+                    "bytes": "forward: read X, write Y; backward (one pass): read dY and X, write dX"})
     del X, dX, Y
     # rotary embedding on Llama-3-8B attention shapes (Q and K in place; HBM-bound)
     r = wl.rope_llama3()

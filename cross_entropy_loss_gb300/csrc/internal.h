@@ -57,10 +57,10 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
 
 // Test hooks (capi.cu): the barrier-wait limit given to the row kernel, and a row
 // whose slice the row kernel's producer skips (so a wait is sure to run out).
-// RMSNorm (rmsnorm.cu): dgamma partials of kRmsGammaGroups row groups x D floats.
+// RMSNorm (rmsnorm.cu): dgamma partials, up to 512 rows (CTAs or row groups) x D floats.
 constexpr int kRmsGammaGroups = 128;
 inline size_t rmsnorm_workspace_bytes(int64_t D) {
-    return (static_cast<size_t>(kRmsGammaGroups) * static_cast<size_t>(D) * 4 + 255) / 256 * 256;
+    return (static_cast<size_t>(512) * static_cast<size_t>(D) * 4 + 255) / 256 * 256;
 }
 cudaError_t launch_rmsnorm_fwd(int es, const void* X, int64_t ldx, const void* gamma, int64_t N, int64_t D,
                                float eps, void* Y, int64_t ldy, float* rstd, cudaStream_t s);

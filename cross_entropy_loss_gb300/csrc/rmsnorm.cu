@@ -40,6 +40,17 @@ __device__ __forceinline__ void load8(const char* p, float (&f)[16 / ES]) {
 }
 
 template <int ES>
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[16 / ES]) {
+    if constexpr (ES == 2) {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    } else {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+}
+
+template <int ES>
 __device__ __forceinline__ void store8(char* p, const float (&f)[16 / ES]) {
     uint4 v;
     if constexpr (ES == 2) {
@@ -150,6 +161,81 @@ __global__ void __launch_bounds__(kGammaThreads) rmsnorm_dgamma_kernel(const cha
     for (int k = 0; k < EPV; ++k) p[k] = acc[k];
 }
 
+// Backward in one pass over dY and X, for rows of at most 1024 vectors: thread v
+// owns column vector v of every row; a CTA takes kFuseRows rows at a time, reduces
+// their sums of xh * u in one round (warp shuffles, one barrier; the buffer is
+// double-buffered by batch parity), writes dX from registers and keeps its
+// columns' dgamma sums in registers; each CTA writes one partial row at the end.
+constexpr int kFuseRows = 4;
+constexpr int kFuseMaxGrid = 512;
+
+template <int ES>
+__global__ void __launch_bounds__(1024) rmsnorm_bwd_fused_kernel(const char* __restrict__ dY, int64_t lddy,
+                                                                 const char* __restrict__ X, int64_t ldx,
+                                                                 const char* __restrict__ gamma,
+                                                                 const float* __restrict__ rstd, int64_t N,
+                                                                 int64_t D, char* __restrict__ dX, int64_t lddx,
+                                                                 float* __restrict__ part) {
+    constexpr int EPV = 16 / ES;
+    __shared__ float red[2][kFuseRows][32];
+    const int v = threadIdx.x, lane = v & 31, warp = v >> 5, warps = blockDim.x >> 5;
+    const bool active = static_cast<int64_t>(v) * EPV < D;
+    float gm[EPV], acc[EPV];
+#pragma unroll
+    for (int k = 0; k < EPV; ++k) {
+        gm[k] = 0.f;
+        acc[k] = 0.f;
+    }
+    if (active) load8<ES>(gamma + static_cast<int64_t>(v) * 16, gm);
+    int par = 0;
+    for (int64_t row0 = static_cast<int64_t>(blockIdx.x) * kFuseRows; row0 < N;
+         row0 += static_cast<int64_t>(gridDim.x) * kFuseRows, par ^= 1) {
+        uint4 xv[kFuseRows], dv[kFuseRows];  // kept packed: 8 registers per row
+        float r[kFuseRows];
+#pragma unroll
+        for (int q = 0; q < kFuseRows; ++q) {
+            const int64_t row = row0 + q;
+            float dot = 0.f;
+            r[q] = 0.f;
+            xv[q] = dv[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (row < N && active) {
+                xv[q] = ld_global_v4(reinterpret_cast<const uint4*>(X + (row * ldx + static_cast<int64_t>(v) * EPV) * ES));
+                dv[q] = ld_global_v4(reinterpret_cast<const uint4*>(dY + (row * lddy + static_cast<int64_t>(v) * EPV) * ES));
+                r[q] = rstd[row];
+                float fx[EPV], fd[EPV];
+                unpack<ES>(xv[q], fx);
+                unpack<ES>(dv[q], fd);
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) dot = fmaf(fx[k] * r[q], gm[k] * fd[k], dot);
+            }
+            dot = warp_sum(dot);
+            if (lane == 0) red[par][q][warp] = dot;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < kFuseRows; ++q) {
+            const int64_t row = row0 + q;
+            const float m = warp_sum(lane < warps ? red[par][q][lane] : 0.f) / static_cast<float>(D);
+            if (row < N && active) {
+                float fx[EPV], fd[EPV], o[EPV];
+                unpack<ES>(xv[q], fx);
+                unpack<ES>(dv[q], fd);
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) {
+                    o[k] = r[q] * (gm[k] * fd[k] - fx[k] * r[q] * m);
+                    acc[k] = fmaf(fd[k], fx[k] * r[q], acc[k]);
+                }
+                store8<ES>(dX + (row * lddx + static_cast<int64_t>(v) * EPV) * ES, o);
+            }
+        }
+    }
+    if (active) {
+        float* p = part + static_cast<int64_t>(blockIdx.x) * D + static_cast<int64_t>(v) * EPV;
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) p[k] = acc[k];
+    }
+}
+
 __global__ void rmsnorm_dgamma_reduce(const float* __restrict__ part, int G, int64_t D, float* __restrict__ dgamma) {
     for (int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; j < D;
          j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -194,6 +280,28 @@ cudaError_t launch_rmsnorm_fwd(int es, const void* X, int64_t ldx, const void* g
 cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void* X, int64_t ldx, const void* gamma,
                                const float* rstd, int64_t N, int64_t D, void* dX, int64_t lddx, float* part,
                                float* dgamma, cudaStream_t s) {
+    const int64_t nvec = D / (16 / es);
+    if (dgamma && N > 0 && nvec <= 1024) {
+        // one pass: dX and the dgamma partials of each CTA, then the fixed-order reduce
+        const int threads = static_cast<int>((nvec + 31) / 32 * 32);
+        const int grid = static_cast<int>(std::min<int64_t>(
+            {(N + kFuseRows - 1) / kFuseRows, static_cast<int64_t>(device_sm_count()) * 2, kFuseMaxGrid}));
+        if (es == 2)
+            rmsnorm_bwd_fused_kernel<2><<<grid, threads, 0, s>>>(static_cast<const char*>(dY), lddy,
+                                                                 static_cast<const char*>(X), ldx,
+                                                                 static_cast<const char*>(gamma), rstd, N, D,
+                                                                 static_cast<char*>(dX), lddx, part);
+        else
+            rmsnorm_bwd_fused_kernel<4><<<grid, threads, 0, s>>>(static_cast<const char*>(dY), lddy,
+                                                                 static_cast<const char*>(X), ldx,
+                                                                 static_cast<const char*>(gamma), rstd, N, D,
+                                                                 static_cast<char*>(dX), lddx, part);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + 63) / 64)), 64, 0, s>>>(part, grid, D,
+                                                                                                       dgamma);
+        return cudaGetLastError();
+    }
     if (N > 0) {
         const int grid = norm_grid(N);
         if (es == 2)

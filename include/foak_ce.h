@@ -197,7 +197,7 @@ foak_status foak_ce_fwd_bwd_host(const void* host_logits, int32_t dtype, int64_t
 foak_status foak_rmsnorm_forward(const void* X, int32_t dtype, int64_t ldx, const void* gamma, int64_t N, int64_t D,
                                  float eps, void* Y, int64_t ldy, float* rstd, void* stream);
 
-/* Bytes of device workspace foak_rmsnorm_backward needs for dgamma (128 x D floats). */
+/* Bytes of device workspace foak_rmsnorm_backward needs for dgamma (512 x D floats of partial sums). */
 size_t foak_rmsnorm_workspace_size(int64_t D);
 
 /*
