@@ -236,21 +236,33 @@ __global__ void __launch_bounds__(1024) rmsnorm_bwd_fused_kernel(const char* __r
     }
 }
 
-__global__ void rmsnorm_dgamma_reduce(const float* __restrict__ part, int G, int64_t D, float* __restrict__ dgamma) {
-    for (int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; j < D;
-         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        // fixed order: four interleaved running sums over the groups, added at the end
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        int g = 0;
-#pragma unroll 4
-        for (; g + 4 <= G; g += 4) {
-            s0 += part[(g + 0) * D + j];
-            s1 += part[(g + 1) * D + j];
-            s2 += part[(g + 2) * D + j];
-            s3 += part[(g + 3) * D + j];
+// dgamma[j] = sum of part[g][j] over g < G, in a fixed order: 8 slices of 64
+// columns per CTA, slice sl summing g = sl, sl + 8, ... (four interleaved running
+// sums), then slice 0 adding the 8 slice sums in slice order.
+constexpr int kRedCols = 64, kRedSlices = 8;
+__global__ void __launch_bounds__(kRedCols * kRedSlices) rmsnorm_dgamma_reduce(const float* __restrict__ part, int G,
+                                                                             int64_t D, float* __restrict__ dgamma) {
+    __shared__ float ss[kRedSlices][kRedCols];
+    const int c = threadIdx.x % kRedCols, sl = threadIdx.x / kRedCols;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kRedCols + c;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    if (j < D) {
+        int g = sl;
+        for (; g + 3 * kRedSlices < G; g += 4 * kRedSlices) {
+            s0 += part[static_cast<int64_t>(g) * D + j];
+            s1 += part[static_cast<int64_t>(g + kRedSlices) * D + j];
+            s2 += part[static_cast<int64_t>(g + 2 * kRedSlices) * D + j];
+            s3 += part[static_cast<int64_t>(g + 3 * kRedSlices) * D + j];
         }
-        for (; g < G; ++g) s0 += part[g * D + j];
-        dgamma[j] = (s0 + s1) + (s2 + s3);
+        for (; g < G; g += kRedSlices) s0 += part[static_cast<int64_t>(g) * D + j];
+    }
+    ss[sl][c] = (s0 + s1) + (s2 + s3);
+    __syncthreads();
+    if (sl == 0 && j < D) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < kRedSlices; ++k) t += ss[k][c];
+        dgamma[j] = t;
     }
 }
 
@@ -298,7 +310,7 @@ cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void*
                                                                  static_cast<char*>(dX), lddx, part);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + 63) / 64)), 64, 0, s>>>(part, grid, D,
+        rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols)), kRedCols * kRedSlices, 0, s>>>(part, grid, D,
                                                                                                        dgamma);
         return cudaGetLastError();
     }
@@ -330,7 +342,7 @@ cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void*
                                                                  part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + 63) / 64)), 64, 0, s>>>(
+    rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols)), kRedCols * kRedSlices, 0, s>>>(
         part, kRmsGammaGroups, D, dgamma);
     return cudaGetLastError();
 }
