@@ -59,19 +59,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe: has the phase with the given parity completed?
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // when limit_ns (default kWaitLimitNs) elapsed first.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
@@ -147,15 +134,6 @@ __device__ __forceinline__ void cluster_wait_acquire() {
 __device__ __forceinline__ void cluster_sync() {
     cluster_arrive_release();
     cluster_wait_acquire();
-}
-
-// Read a float2 at the same shared-memory offset in cluster CTA `rank`.
-__device__ __forceinline__ float2 ld_dsmem_f2(const void* local, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote) : "memory");
-    return v;
 }
 
 // Address of the same shared-memory location in cluster CTA `rank`.

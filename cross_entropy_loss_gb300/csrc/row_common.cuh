@@ -62,34 +62,6 @@ __device__ __forceinline__ RowGeom row_geom(const char* rowp, int64_t V) {
 }
 
 template <int ES>
-__device__ __forceinline__ void unpack(const uint4& v, float (&f)[16 / ES]) {
-    if constexpr (ES == 2) {
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-        f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-    } else {
-        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
-        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
-    }
-}
-
-template <int ES>
-__device__ __forceinline__ uint4 pack(const float (&f)[16 / ES]) {
-    uint4 v;
-    if constexpr (ES == 2) {
-        v.x = pack_bf16x2(f[0], f[1]);
-        v.y = pack_bf16x2(f[2], f[3]);
-        v.z = pack_bf16x2(f[4], f[5]);
-        v.w = pack_bf16x2(f[6], f[7]);
-    } else {
-        v.x = __float_as_uint(f[0]); v.y = __float_as_uint(f[1]);
-        v.z = __float_as_uint(f[2]); v.w = __float_as_uint(f[3]);
-    }
-    return v;
-}
-
-template <int ES>
 __device__ __forceinline__ float load_scalar(const char* p) {
     if constexpr (ES == 2) return bf16_lo(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)));
     else return *reinterpret_cast<const float*>(p);
@@ -211,33 +183,6 @@ struct RowMath<4> {  // fp32: 4 elements per vector, 2 packed pairs
         return o;
     }
 };
-
-// Element e (runtime index) of a vector, without dynamic register indexing.
-template <int ES>
-__device__ __forceinline__ float vec_elem(const uint4& v, int e) {
-    float f[16 / ES];
-    unpack<ES>(v, f);
-    float r = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16 / ES; ++k)
-        if (k == e) r = f[k];
-    return r;
-}
-
-// The label's vector: same values as the fast path, minus scale at element e.
-template <int ES>
-__device__ __forceinline__ uint4 vec_grad_label(const uint4& v, int e_own, float c, bool mul, float scale) {
-    constexpr int EPV = 16 / ES;
-    float f[EPV], d[EPV];
-    unpack<ES>(v, f);
-#pragma unroll
-    for (int k = 0; k < EPV; ++k) {
-        float q = ex2(fmaf(f[k], kLog2e, -c));
-        if (mul) q *= scale;
-        d[k] = k == e_own ? q - scale : q;
-    }
-    return pack<ES>(d);
-}
 
 // One CTA per row, the row streamed through shared memory in 64 KB chunks
 // twice (log-sum-exp, then gradient): for rows longer than one CTA's slice.
