@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const char* _
     for (int64_t row = blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); row < N; row += warps) {
         const char* x = X + row * ldx * ES;
         float ss = 0.f;
-        for (int64_t v = lane; v < nvec; v += 32) {
+#pragma unroll 4
+        for (int64_t v = lane; v < nvec; v += 32) {  // unrolled: several 16-byte loads in flight per lane
             float f[EPV];
             load8<ES>(x + v * 16, f);
 #pragma unroll
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const char* _
         ss = warp_sum(ss);
         const float r = rsqrtf(ss / static_cast<float>(D) + eps);
         char* y = Y + row * ldy * ES;
+#pragma unroll 4
         for (int64_t v = lane; v < nvec; v += 32) {
             float f[EPV], gm[EPV];
             load8<ES>(x + v * 16, f);
