@@ -623,17 +623,20 @@ def run_reference(args, rank, world):
     cfg = _make(args.workload)
     threads = oracle.default_threads()
     N = cfg["logits"].shape[0]
-    rows = 64
+    rows = 512  # per step: 32 rows per thread on 16 cores, so thread start-up does not dominate
+    # distinct samples prepared before the timed region (their generation is not the oracle's work)
+    pool = [_oracle_sample(cfg, rows, i * rows) for i in range(min(8, args.steps + args.warmup))]
     for i in range(args.warmup):
-        x, y = _oracle_sample(cfg, rows, i * rows)
+        x, y = pool[i % len(pool)]
         oracle.ce(x, y, cfg["V"], threads=threads)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        x, y = _oracle_sample(cfg, rows, (args.warmup + i) * rows)
+        x, y = pool[(args.warmup + i) % len(pool)]
         oracle.ce(x, y, cfg["V"], threads=threads)
     dt = time.perf_counter() - t0
     val = rows * args.steps / dt
-    sample = f"{rows} consecutive rows of the headline workload per step (N={N}), float64 fwd+bwd incl. gradient"
+    sample = (f"{rows} consecutive rows of the headline workload per step (N={N}; {len(pool)} distinct samples "
+              "cycled), float64 fwd+bwd incl. gradient")
     return {"metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
