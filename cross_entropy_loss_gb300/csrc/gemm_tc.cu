@@ -1,11 +1,6 @@
 // Persistent bf16 GEMM on the fifth-generation tensor cores (tcgen05) for the
 // chunked linear + cross-entropy:  C (+)= A * B^T  with fp32 accumulation.
 //
-// CTAs work in pairs (clusters of 2) on M-neighbouring tiles (2i, n), (2i+1, n):
-// each loads its own A tile and half of the shared B tile, multicast into both
-// CTAs' shared memory, and each MMA releases a stage to both producers, so a pair
-// reads a B tile from L2 once -- a third less operand traffic per tile (the
-// products are L2-bandwidth-bound at 48 KB per 64-deep k-block without it).
 // One CTA per SM walks output tiles of 128 x 256.  The walk runs along the
 // shorter tile dimension first (M fastest when there are fewer M tiles than N
 // tiles, else N fastest), so the CTAs working at once share a few tiles of the
@@ -58,21 +53,15 @@ struct GemmParams {
     int mode;
     int tiles_m, tiles_n;
     int n_fast;  // tile walk: N index fastest (else M)
-    int pair;    // CTA pairs (clusters of 2) on tiles (2i, n), (2i+1, n) share the B tile
     uint32_t idesc;
     void* out;
     int64_t ldo;
     int32_t* err;
 };
 
-// Work units: single tiles, or (with pairs) pairs of M-neighbouring tiles, walked
-// along the shorter dimension first; rank = the CTA's place in its pair.
-__device__ __forceinline__ int units_m(const GemmParams& p) { return p.pair ? (p.tiles_m + 1) / 2 : p.tiles_m; }
-__device__ __forceinline__ int tile_m(const GemmParams& p, int u, int rank) {
-    const int um = p.n_fast ? u / p.tiles_n : u % units_m(p);
-    return p.pair ? 2 * um + rank : um;
-}
-__device__ __forceinline__ int tile_n(const GemmParams& p, int u) { return p.n_fast ? u % p.tiles_n : u / units_m(p); }
+// Output tiles walked along the shorter dimension first.
+__device__ __forceinline__ int tile_m(const GemmParams& p, int t) { return p.n_fast ? t / p.tiles_n : t % p.tiles_m; }
+__device__ __forceinline__ int tile_n(const GemmParams& p, int t) { return p.n_fast ? t % p.tiles_n : t / p.tiles_m; }
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -82,13 +71,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     __shared__ volatile int abort_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rank = p.pair ? static_cast<int>(cluster_ctarank()) : 0;
-    const int unit0 = p.pair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int unit_step = p.pair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int unit0 = static_cast<int>(blockIdx.x);
+    const int unit_step = static_cast<int>(gridDim.x);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], p.pair ? 2 : 1);  // with pairs both CTAs' MMAs release a stage
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -105,10 +93,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     }
     tc_fence_before();
     __syncthreads();
-    if (p.pair) cluster_sync();  // the peer's barriers exist before its first multicast
     tc_fence_after();
     const uint32_t tbase = tmem_base_sh;
-    const int num_tiles = units_m(p) * p.tiles_n;  // work units
+    const int num_tiles = p.tiles_m * p.tiles_n;
     const int nk = (p.K + kBK - 1) / kBK;
 
     auto give_up = [&]() {
@@ -121,7 +108,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
             int stage = 0;
             uint32_t phase = 0;
             for (int t = unit0; t < num_tiles && !abort_sh; t += unit_step) {
-                const int m0 = tile_m(p, t, rank) * kBM, n0 = tile_n(p, t) * kBN;
+                const int m0 = tile_m(p, t) * kBM, n0 = tile_n(p, t) * kBN;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) { give_up(); break; }
                     if (abort_sh) break;
@@ -135,17 +122,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                         tma_load_2d(sA, &p.tmA, m0, k0, &full[stage]);
                         tma_load_2d(sA + kMNBlock, &p.tmA, m0 + 64, k0, &full[stage]);
                     }
-                    if (p.pair) {
-                        // this CTA's half of the shared B tile, into both CTAs' stage
-                        if (!p.b_mn) {
-                            tma_load_2d_mc(sB + rank * (kBBytes / 2), &p.tmB, k0, n0 + rank * (kBN / 2), &full[stage],
-                                           0x3);
-                        } else {
-#pragma unroll
-                            for (int j = 2 * rank; j < 2 * rank + 2; ++j)
-                                tma_load_2d_mc(sB + j * kMNBlock, &p.tmB, n0 + 64 * j, k0, &full[stage], 0x3);
-                        }
-                    } else if (!p.b_mn) {
+                    if (!p.b_mn) {
                         tma_load_2d(sB, &p.tmB, k0, n0, &full[stage]);
                     } else {
 #pragma unroll
@@ -181,8 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                                                    : smem_desc_sw128(sB + kk * 32, 16, 1024);
                         tc_mma_bf16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    if (p.pair) tc_commit_mc(&empty[stage], 0x3);  // both producers may refill it
-                    else tc_commit(&empty[stage]);
+                    tc_commit(&empty[stage]);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -207,7 +183,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 break;
             }
             tc_fence_after();
-            const int m0 = tile_m(p, t, rank) * kBM, n0 = tile_n(p, t) * kBN;
+            const int m0 = tile_m(p, t) * kBM, n0 = tile_n(p, t) * kBN;
             const int row_blk = m0 + q * 32;  // first row of this warp's 32
             const int row = row_blk + lane;
             // TMEM -> registers one 32-column chunk ahead: chunk c + 1 is loading while
@@ -279,8 +255,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
     }
-    // no CTA of a pair leaves while its peer may still multicast into it or arrive on its barriers
-    if (p.pair) cluster_sync();
 }
 
 // ------------------------------------------------------------------ host side
@@ -337,19 +311,12 @@ bool g_gemm_attr[64] = {false};
 cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     if (d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaSuccess;
     GemmParams p = {};
-    static const int pair_env = [] {
-        const char* e = std::getenv("FOAK_GEMM_PAIR");  // tuning override: 0 = single CTAs
-        return e ? std::atoi(e) : 1;
-    }();
-    const int tiles_m = (d.M + kBM - 1) / kBM;
-    p.pair = pair_env != 0 && tiles_m >= 2 && device_sm_count() >= 2 ? 1 : 0;
     // K-major [rows][K]: inner K, boxes of 64 x rows-tile; MN-major [K][rows]: inner rows, 64 x 64 boxes.
     bool ok = d.a_mn_major ? encode_bf16(&p.tmA, d.a, static_cast<uint64_t>(d.M), static_cast<uint64_t>(d.K), d.lda, 64)
                            : encode_bf16(&p.tmA, d.a, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.M), d.lda, kBM);
     ok = ok && (d.b_mn_major
                     ? encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.K), d.ldb, 64)
-                    : encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N), d.ldb,
-                                  p.pair ? kBN / 2 : kBN));  // pairs load half a B tile each
+                    : encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N), d.ldb, kBN));
     if (ok && d.mode != kGemmOutBf16)
         ok = encode_f32_out(&p.tmC, d.out, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.M), d.ldo);
     if (!ok) return cudaErrorInvalidValue;
@@ -379,37 +346,10 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
             g_gemm_attr[dev] = true;
         }
     }
-    if (!p.pair) {
-        const int tiles = p.tiles_m * p.tiles_n;
-        const int grid = std::min(tiles, device_sm_count());
-        gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(p);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = kGemmSmem;
-    cfg.stream = stream;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    static int max_pairs[64] = {0};
-    {
-        std::lock_guard<std::mutex> lock(g_gemm_mu);
-        if (max_pairs[dev] == 0) {
-            cfg.gridDim = dim3(2, 1, 1);
-            int n = 0;
-            e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel, &cfg);
-            if (e != cudaSuccess) return e;
-            max_pairs[dev] = std::max(1, n);
-        }
-    }
-    const int units = (p.tiles_m + 1) / 2 * p.tiles_n;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(units, max_pairs[dev])), 1, 1);
-    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel, p);
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int grid = std::min(tiles, device_sm_count());
+    gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace foak
