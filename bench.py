@@ -13,9 +13,14 @@ batch, the Llama-3 vocabulary in bf16 and fp32, the separate forward and backwar
 entry points, and the chunked linear+CE call when the library exports it.
 
 ``--impl reference`` times the CPU oracle (float64 C, all host cores) on bounded
-samples of the same workload instead.  Under torchrun (N > 1) every rank runs an
-independent replica of the workload (weak scaling, no collective on the data path);
-rank 0 prints the line with the max time over ranks.
+samples of the same workload instead.
+
+``--gpus N`` with N > 1 starts N ranks itself (``torch.distributed.run``, one per
+GPU, NCCL) unless it already runs under torchrun.  Every rank holds its own batch of
+the workload (weak scaling) and each timed step is the data-parallel per-token mean:
+the rank counts its valid tokens on the device, the counts are all-reduced (NCCL, on
+the device), the fused kernel divides by the total, and the ranks' partial losses
+are all-reduced.  Rank 0 prints the line with the max time over ranks.
 """
 from __future__ import annotations
 
@@ -37,7 +42,7 @@ import numpy as np  # noqa: E402
 
 import workloads as wl  # noqa: E402
 
-METRIC = "CE fwd+bwd tokens/s and HBM GB/s (% of peak), V=32k/128k bf16, 1xGB300"
+METRIC = "CE fwd+bwd tokens/s and HBM GB/s (% of peak), V=32k/128k bf16, 1\u00d7GB300"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 RING_BUDGET_BYTES = 64 << 30
@@ -310,6 +315,18 @@ def run_ours(args, rank, world, dist):
     if args.profile and args.path == "chunked":
         return {"metric": "chunked linear+CE (profiling run)", "chunked": chunked_timing(ce, torch, dev, stream)}
     call = None
+    if dist is not None:
+        # the data-parallel step: local count -> all-reduce on the device -> fused call reading the total
+        from cross_entropy_loss_gb300 import dp
+
+        cnt_buf = torch.empty(1, dtype=torch.int64, device=dev)
+        V_main = main["V"]
+
+        def call(b, y, workspace_tensor):
+            return dp.fused_step(lambda yy: ce.foak_ce_count_valid(yy, V_main, out=cnt_buf),
+                                 lambda xx, yy, d: ce.foak_ce_fwd_bwd_devdenom(xx, yy, d,
+                                                                               workspace_tensor=workspace_tensor),
+                                 b, y)
     if args.profile and args.path == "forward":
         call = lambda b, y, workspace_tensor: ce.foak_ce_forward(b, y, workspace_tensor=workspace_tensor)  # noqa: E731
     if args.profile and args.path == "backward":
@@ -346,19 +363,22 @@ def run_ours(args, rank, world, dist):
         "vs_baseline": None,
         "dtype": "bf16" if main["dtype"] == wl.BF16 else "f32",
         "data": "synthetic (seeded SplitMix64 + Box-Muller; no dataset)",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "N": N, "V": main["V"],
-                   "seed": main["seed"], "parallelism": f"dp{world} (independent replicas)",
-                   "l2": "inputs larger than L2: each timed step has its own 262 MB-class logits copy"
-                         + (" (ring reused: steps > ring)" if reused else ""),
-                   "hbm_GBps_algorithmic": achieved,
-                   "hbm_GBps_stated_2NVs": stated / (ms * 1e-3) / 1e9,
-                   "loss": loss, "err": err},
+        "config": _config(main, args.workload),
+        "parallelism": (f"dp{world}: a batch per rank, per-token mean over all ranks (valid-token count "
+                        "all-reduced on the device each step, partial losses all-reduced)") if world > 1
+                       else "dp1",
+        "l2": "inputs larger than L2: each timed step has its own 262 MB-class logits copy"
+              + (" (ring reused: steps > ring)" if reused else ""),
+        "hbm_GBps_algorithmic": achieved,
+        "hbm_GBps_stated_2NVs": stated / (ms * 1e-3) / 1e9,
+        "loss": loss, "err": err,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": _traffic(prof_name, sha),
                      "algorithmic_bytes_per_launch": algo, "kernel": kernel,
                      "kernel_source_sha": sha},
-        "gpu_launches": args.steps,
+        # our kernels per timed step: the fused kernel (N > 1: plus the label count; NCCL's are not ours)
+        "gpu_launches": args.steps * (2 if world > 1 else 1),
     }
 
     if args.profile:
@@ -366,7 +386,7 @@ def run_ours(args, rank, world, dist):
     # end-to-end through the public API: pinned host logits -> device, fused call, loss -> host
     if rank == 0 or dist is not None:
         res["e2e"] = e2e_timing(ce, torch, dev, stream, main, max(3, min(args.steps, 20)), upload, barrier,
-                                max_over_ranks, world)
+                                max_over_ranks, world, dist)
 
     if rank == 0 and not args.quick:
         res["secondary"] = secondary(ce, torch, dev, stream, upload, fused_timing, args)
@@ -374,13 +394,34 @@ def run_ours(args, rank, world, dist):
         res["clocks"] = sampler.summary()
     if rank == 0:
         res["cpu_baseline"] = cpu_baseline(main)
+        # the metric's second vocabulary, last on the line so a tail of the output keeps it
+        by = {s.get("key"): s for s in res.get("secondary", []) if s.get("key")}
+        res["v128k_bf16"] = _compact(by.get("llama3"))
+        res["v128k_f32"] = _compact(by.get("llama3_f32"))
+        res["packed_v32k_bf16"] = _compact(by.get("packed"))
     return res
 
 
-def e2e_timing(ce, torch, dev, stream, cfg, steps, upload, barrier, max_over_ranks, world):
+def _compact(s):
+    if not s:
+        return None
+    return {"workload": s["workload_key"], "ms_per_step": s["ms_per_step"], "tokens_per_s": s["tokens_per_s"],
+            "GBps_algorithmic": s["GBps_algorithmic"], "frac": s["frac"], "peak": s["peak"],
+            "peak_source": s["peak_source"]}
+
+
+def _config(cfg, name):
+    """The workload, the same keys in both arms (ours and the reference's)."""
+    return {"workload": WORKLOAD_DESC[name], "N": int(cfg["logits"].shape[0]), "V": int(cfg["V"]),
+            "seed": int(cfg["seed"])}
+
+
+def e2e_timing(ce, torch, dev, stream, cfg, steps, upload, barrier, max_over_ranks, world, dist=None):
     """The fused call on HOST buffers through the C ABI (foak_ce_fwd_bwd_host): each step
     copies that step's pinned logits and labels to the device in row chunks, sweeps
-    every chunk as it lands, and reads the loss, n_valid and error word back."""
+    every chunk as it lands, and reads the loss, n_valid and error word back.  With
+    several ranks each step first copies the labels, counts them on the device and
+    all-reduces the count, which the host call then takes as its denominator."""
     es = 2 if cfg["dtype"] == wl.BF16 else 4
     host_x = torch.from_numpy(cfg["logits"].view(np.int16) if es == 2 else cfg["logits"]).pin_memory()
     if es == 2:
@@ -394,8 +435,16 @@ def e2e_timing(ce, torch, dev, stream, cfg, steps, upload, barrier, max_over_ran
                n_valid=torch.empty(1, dtype=torch.int32).pin_memory(),
                err=torch.empty(1, dtype=torch.int32).pin_memory())
 
+    cnt = torch.empty(1, dtype=torch.int64, device=dev)
+
     def step():
-        ce.foak_ce_fwd_bwd_host(host_x, host_y, x, y, workspace_tensor=ws, out=out, stream=stream)
+        denom = 0.0
+        if dist is not None:
+            y.copy_(host_y, non_blocking=True)
+            ce.foak_ce_count_valid(y, cfg["V"], out=cnt)
+            dist.all_reduce(cnt)
+            denom = float(cnt.item())
+        ce.foak_ce_fwd_bwd_host(host_x, host_y, x, y, denom=denom, workspace_tensor=ws, out=out, stream=stream)
 
     for _ in range(3):
         step()
@@ -408,7 +457,7 @@ def e2e_timing(ce, torch, dev, stream, cfg, steps, upload, barrier, max_over_ran
     e1.record(stream)
     e1.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / steps)
-    h2d = host_x.numel() * host_x.element_size() + host_y.numel() * 8
+    h2d = host_x.numel() * host_x.element_size() + host_y.numel() * 8 * (2 if dist is not None else 1)
     return {"value": world * N / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 12,
             "loss": float(out["loss"].item()), "err": int(out["err"].item()),
@@ -425,7 +474,8 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
         ms, loss, err, _ = fused_timing(cfg, k, w, False, use_dist=False)
         algo = _algo_bytes(cfg)
         gbs = algo / (ms * 1e-3) / 1e9
-        out.append({"path": "foak_ce_fwd_bwd", "kernel": _row_kernel(cfg)[0], "workload": WORKLOAD_DESC[name],
+        out.append({"key": name, "workload_key": f"{name}: N={cfg['logits'].shape[0]} V={cfg['V']}",
+                    "path": "foak_ce_fwd_bwd", "kernel": _row_kernel(cfg)[0], "workload": WORKLOAD_DESC[name],
                     "steps": k, "ms_per_step": ms,
                     "tokens_per_s": cfg["logits"].shape[0] / (ms * 1e-3), "GBps_algorithmic": gbs,
                     "GBps_stated_2NVs": _stated_bytes(cfg) / (ms * 1e-3) / 1e9, "frac": gbs / peak,
@@ -640,13 +690,24 @@ def run_reference(args, rank, world):
     return {"metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC[args.workload], "N": N, "V": cfg["V"], "seed": cfg["seed"]},
+            "config": _config(cfg, args.workload),
             "impl": "reference",
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 # ----------------------------------------------------------------------------- main
+
+def _dp_module():
+    """The data-parallel helpers, loaded without the package (the reference arm needs no library)."""
+    import importlib.util
+
+    path = os.path.join(ROOT, "cross_entropy_loss_gb300", "dp.py")
+    spec = importlib.util.spec_from_file_location("_foak_dp", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -665,8 +726,11 @@ def main():
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    dp = _dp_module()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU (NCCL): start the ranks; rank 0 prints the line
+        return dp.relaunch(args.gpus, os.path.abspath(__file__), sys.argv[1:])
+    rank, world, local = dp.rank_env()
     dist = None
     if world > 1:
         if args.impl == "reference":
@@ -677,7 +741,7 @@ def main():
         import torch
         import torch.distributed as tdist
 
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.cuda.set_device(local)
         tdist.init_process_group("nccl")
         dist = tdist
 

@@ -60,6 +60,9 @@ SIGNATURES = {
                                     _sz, _vp]),
     "foak_ce_fwd_bwd": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _sz,
                                _vp]),
+    "foak_ce_count_valid": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "foak_ce_fwd_bwd_devdenom": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _sz, _vp]),
     "foak_ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
                                        _vp]),
     "foak_gemm_bf16": (_i32, [_vp, _i64, _i32, _vp, _i64, _i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _vp]),
@@ -231,6 +234,44 @@ def foak_ce_fwd_bwd(logits, labels, *, g: float = 1.0, ignore_index: int = -100,
     return dict(loss=loss, n_valid=n_valid, err=err, lse=lse)
 
 
+def foak_ce_count_valid(labels, V: int, *, ignore_index: int = -100, out=None, err=None, stream=None):
+    """Number of labels in [0, V) (not ignore_index), as an int64 device tensor of one element
+    (``out`` if given), e.g. this rank's term of a data-parallel all-reduced denominator."""
+    if labels.dtype != torch.int64 or labels.dim() != 1 or not labels.is_contiguous():
+        raise ValueError("labels must be a contiguous int64 vector")
+    dev = labels.device
+    if out is None:
+        out = torch.empty(1, dtype=torch.int64, device=dev)
+    if out.dtype != torch.int64 or out.numel() != 1:
+        raise ValueError("out must be a one-element int64 tensor")
+    st = lib.foak_ce_count_valid(_ptr(labels), labels.numel(), int(V), int(ignore_index), _ptr(out), _ptr(err),
+                                 _stream(dev, stream))
+    _check(st, "foak_ce_count_valid")
+    return out
+
+
+def foak_ce_fwd_bwd_devdenom(logits, labels, denom_count, *, g: float = 1.0, ignore_index: int = -100,
+                             want_lse: bool = False, workspace_tensor=None, stream=None):
+    """foak_ce_fwd_bwd dividing by the int64 count in device memory ``denom_count`` (read when the
+    kernel runs, e.g. after an all-reduce on the same stream).  ``loss`` is this call's share
+    sum(l_i) / D.  Returns dict(loss, n_valid, err, lse)."""
+    N, V, ld, dt = _logits_args(logits)
+    dev = logits.device
+    labels = _labels_arg(labels, N, dev)
+    if denom_count.dtype != torch.int64 or denom_count.numel() != 1 or denom_count.device != dev:
+        raise ValueError("denom_count must be a one-element int64 tensor on the logits' device")
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int32, device=dev)
+    err = torch.empty(1, dtype=torch.int32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
+    ws = workspace(N, dev) if workspace_tensor is None else workspace_tensor
+    st = lib.foak_ce_fwd_bwd_devdenom(_ptr(logits), dt, ld, _ptr(labels), N, V, int(ignore_index), float(g),
+                                      _ptr(denom_count), _ptr(loss), _ptr(lse), _ptr(n_valid), _ptr(err), _ptr(ws),
+                                      ws.numel(), _stream(dev, stream))
+    _check(st, "foak_ce_fwd_bwd_devdenom")
+    return dict(loss=loss, n_valid=n_valid, err=err, lse=lse)
+
+
 def foak_ce_host_workspace_size(N: int) -> int:
     return int(lib.foak_ce_host_workspace_size(int(N)))
 
@@ -292,9 +333,11 @@ def foak_ce_fwd_bwd_noalloc(logits, labels, *, g: float = 1.0, ignore_index: int
     n_valid = torch.empty(1, dtype=torch.int32, device=dev)
     err = torch.empty(1, dtype=torch.int32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
-    st = lib.foak_ce_fwd_bwd_noalloc(_ptr(logits), dt, ld, _ptr(labels), N, V, int(ignore_index), float(g),
-                                     float(denom), _ptr(loss), _ptr(lse), _ptr(n_valid), _ptr(err),
-                                     _stream(dev, stream))
+    # the library uses the scratch array of the CURRENT device: make it the logits' device
+    with torch.cuda.device(dev):
+        st = lib.foak_ce_fwd_bwd_noalloc(_ptr(logits), dt, ld, _ptr(labels), N, V, int(ignore_index), float(g),
+                                         float(denom), _ptr(loss), _ptr(lse), _ptr(n_valid), _ptr(err),
+                                         _stream(dev, stream))
     _check(st, "foak_ce_fwd_bwd_noalloc")
     return dict(loss=loss, n_valid=n_valid, err=err, lse=lse)
 

@@ -95,7 +95,7 @@ foak_status finish(cudaError_t e, int32_t* err, cudaStream_t stream) {
 foak_status rows_common(bool grad, const void* logits, int32_t dtype, int64_t ld, const int64_t* labels,
                         int64_t N, int64_t V, int64_t ignore_index, float g, float denom, float* loss,
                         float* lse, float* row_loss, int32_t* n_valid, int32_t* err, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+                        size_t workspace_bytes, void* stream, const int64_t* denom_dev = nullptr) {
     int es = 0;
     foak_status st = check_rows(logits, dtype, ld, labels, N, V, &es);
     if (st != FOAK_OK) return st;
@@ -110,7 +110,8 @@ foak_status rows_common(bool grad, const void* logits, int32_t dtype, int64_t ld
     float* rl = row_loss ? row_loss : reinterpret_cast<float*>(static_cast<char*>(workspace) + sizeof(CeWsHeader));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_ce_rows(grad, es, logits, grad ? const_cast<void*>(logits) : nullptr, ld, labels, N, V,
-                                   ignore_index, g, denom, loss, lse, rl, n_valid, err, ws, s);
+                                   ignore_index, g, denom, loss, lse, rl, n_valid, err, ws, s, nullptr, 0,
+                                   denom_dev);
     if (e == cudaSuccess) e = cudaGetLastError();
     return finish(e, err, s);
 }
@@ -244,6 +245,26 @@ foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64
                             void* stream) {
     return rows_common(true, logits, dtype, ld, labels, N, V, ignore_index, g, denom, loss, lse, nullptr,
                        n_valid, err, workspace, workspace_bytes, stream);
+}
+
+foak_status foak_ce_count_valid(const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, int64_t* n_valid,
+                                int32_t* err, void* stream) {
+    if (N < 0 || V < 1 || !n_valid || !aligned(n_valid, 8)) return FOAK_ERR_INVALID_ARG;
+    if (N > 0 && (!labels || !aligned(labels, 8))) return FOAK_ERR_INVALID_ARG;
+    if (N > 0x7fffffffLL) return FOAK_ERR_UNSUPPORTED;
+    if (err && !aligned(err, 4)) return FOAK_ERR_INVALID_ARG;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(launch_count_valid(labels, N, V, ignore_index, n_valid, err, s), err, s);
+}
+
+foak_status foak_ce_fwd_bwd_devdenom(void* logits, int32_t dtype, int64_t ld, const int64_t* labels, int64_t N,
+                                     int64_t V, int64_t ignore_index, float g, const int64_t* denom_count,
+                                     float* loss, float* lse, int32_t* n_valid, int32_t* err, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+    if (!denom_count || !aligned(denom_count, 8)) return FOAK_ERR_INVALID_ARG;
+    return rows_common(true, logits, dtype, ld, labels, N, V, ignore_index, g, 0.f, loss, lse, nullptr, n_valid, err,
+                       workspace, workspace_bytes, stream, denom_count);
 }
 
 foak_status foak_ce_backward(void* dlogits, const void* logits, int32_t dtype, int64_t ld, const int64_t* labels,

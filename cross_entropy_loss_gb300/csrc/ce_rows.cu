@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
 
     int n_valid = 0, n_bad = 0;
     count_labels(p.count_labels, p.count_N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
-    const float D = p.denom > 0.f ? p.denom : static_cast<float>(n_valid);
+    const float D = row_denominator(p, n_valid);
     const float scale = p.g / D;
     // Labels of this CTA's first rows, for the row loop and the producer.
     for (int64_t it = tid; it < n_it && it < kLabCache; it += blockDim.x) s_lab[it] = __ldg(p.labels + cid + it * ncl);
@@ -538,7 +538,7 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
                            const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, float g,
                            float denom, float* loss, float* lse, float* row_loss, int32_t* n_valid,
                            int32_t* err, CeWsHeader* ws, cudaStream_t stream, const int64_t* count_labels,
-                           int64_t count_N) {
+                           int64_t count_N, const int64_t* denom_dev) {
     Plan pl;
     if (!plan_rows(elem_bytes, V, &pl)) return cudaErrorInvalidValue;
     CeRowParams prm = {};
@@ -551,6 +551,7 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
     prm.ignore_index = ignore_index;
     prm.g = g;
     prm.denom = denom;
+    prm.denom_dev = denom_dev;
     prm.loss = loss;
     prm.lse = lse;
     prm.row_loss = row_loss;

@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
 
     int n_valid = 0, n_bad = 0;
     count_labels(p.count_labels, p.count_N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
-    const float D = p.denom > 0.f ? p.denom : static_cast<float>(n_valid);
+    const float D = row_denominator(p, n_valid);
     const float scale = p.g / D;
     for (int64_t it = tid; it < n_it && it < kLabCache; it += THREADS) s_lab[it] = __ldg(p.labels + cid + it * ncl);
     __syncthreads();

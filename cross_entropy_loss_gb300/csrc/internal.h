@@ -37,7 +37,13 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
                            const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, float g,
                            float denom, float* loss, float* lse, float* row_loss, int32_t* n_valid,
                            int32_t* err, CeWsHeader* ws, cudaStream_t stream,
-                           const int64_t* count_labels = nullptr, int64_t count_N = 0);
+                           const int64_t* count_labels = nullptr, int64_t count_N = 0,
+                           const int64_t* denom_dev = nullptr);
+
+// Valid labels of labels[0, N) into *n_valid (int64, device) and, when err is
+// given, FOAK_ERRBIT_LABEL_RANGE if some label is neither ignore_index nor in [0, V).
+cudaError_t launch_count_valid(const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, int64_t* n_valid,
+                               int32_t* err, cudaStream_t stream);
 
 cudaError_t launch_ce_backward(int elem_bytes, void* dx, const void* x, int64_t ld,
                                const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index,

@@ -26,6 +26,7 @@ struct CeRowParams {
     const int64_t* labels;
     int64_t N, V, ignore_index;
     float g, denom;
+    const int64_t* denom_dev;  // if set: the denominator, read from device memory (overrides denom)
     float* loss;
     float* lse;
     float* row_loss;
@@ -184,6 +185,14 @@ struct RowMath<4> {  // fp32: 4 elements per vector, 2 packed pairs
     }
 };
 
+// The mean's denominator D: a count in device memory (the data-parallel total of
+// valid tokens, all-reduced by the caller), else the caller's denom, else this
+// call's own count of valid labels.
+__device__ __forceinline__ float row_denominator(const CeRowParams& p, int n_valid) {
+    if (p.denom_dev) return static_cast<float>(__ldg(p.denom_dev));
+    return p.denom > 0.f ? p.denom : static_cast<float>(n_valid);
+}
+
 // One CTA per row, the row streamed through shared memory in 64 KB chunks
 // twice (log-sum-exp, then gradient): for rows longer than one CTA's slice.
 cudaError_t launch_ce_rows_long(bool grad, int elem_bytes, const CeRowParams& base, cudaStream_t stream);
@@ -215,7 +224,7 @@ __device__ __forceinline__ void rows_finish(const CeRowParams& p, bool aborted, 
     if (tid == 0) {
         double tot = 0.0;
         for (int w = 0; w < WARPS; ++w) tot += dred[w];
-        const double Dd = p.denom > 0.f ? static_cast<double>(p.denom) : static_cast<double>(n_valid);
+        const double Dd = static_cast<double>(row_denominator(p, n_valid));
         *p.loss = static_cast<float>(tot / Dd);
         if (p.n_valid) *p.n_valid = n_valid;
         unsigned e = atomicExch(&p.ws->err, 0u);

@@ -143,6 +143,41 @@ foak_status foak_ce_fwd_bwd(void* logits, int32_t dtype, int64_t ld, const int64
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The data-parallel per-token mean (fms-hf-tuning PR #280, "Early Version Of This
+ * Plugin": LossAccelerationPlugin, --loss_across_gpus mean token) divides every
+ * rank's share by the number of valid tokens of ALL ranks, which each rank knows
+ * only after an all-reduce.  These two calls keep that exchange on the device:
+ * a rank counts its valid labels into device memory, the caller sums the counts
+ * across ranks in place (e.g. an NCCL all-reduce of one int64), and the fused
+ * call reads the total from device memory, with no host synchronisation between.
+ *
+ * foak_ce_count_valid: number of rows whose label is not ignore_index and lies in
+ * [0, V).
+ *   labels (device)   int64[N] (may be NULL when N == 0)
+ *   n_valid (device)  int64[1], 8-byte aligned: the count
+ *   err (device)      int32[1] or NULL: FOAK_ERRBIT_LABEL_RANGE if a label is
+ *                     neither ignore_index nor in [0, V), else 0
+ * Errors: FOAK_ERR_INVALID_ARG for N < 0, V < 1, a null or misaligned pointer.
+ */
+foak_status foak_ce_count_valid(const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index,
+                                int64_t* n_valid, int32_t* err, void* stream);
+
+/*
+ * foak_ce_fwd_bwd with the denominator read from device memory: D = *denom_count
+ * (int64, e.g. the all-reduced sum of every rank's foak_ce_count_valid), read by
+ * the kernel when it runs, so the count may still be in flight on `stream` when
+ * the call is made.  loss is then this rank's share sum_{valid i} l_i / D (the
+ * ranks' losses add up to the global mean); n_valid is this call's own count.
+ * With D == 0 the loss is NaN and every gradient row +0.0, as in foak_ce_fwd_bwd.
+ *   denom_count (device)  int64[1], 8-byte aligned
+ *   other arguments       as for foak_ce_fwd_bwd (there is no host denom)
+ */
+foak_status foak_ce_fwd_bwd_devdenom(void* logits, int32_t dtype, int64_t ld, const int64_t* labels,
+                                     int64_t N, int64_t V, int64_t ignore_index, float g,
+                                     const int64_t* denom_count, float* loss, float* lse, int32_t* n_valid,
+                                     int32_t* err, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace foak_ce_fwd_bwd_host needs for N rows: a 256-byte
  * header, N float32 per-row loss terms and 256 bytes of per-chunk error words and
  * results.  256-byte aligned, zero-filled before first use, left reusable by every
@@ -367,9 +402,10 @@ foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const
  *                     FOAK_ERR_WORKSPACE before anything is enqueued
  *   stream            besides the kernel, the call enqueues a 256-byte
  *                     cudaMemsetAsync that clears the scratch header
- * The first call on a device looks up the scratch array's device address (once
- * per device, with that device current); make that first call before any stream
- * capture begins.  Every call on a device shares the one scratch array, so calls
+ * The scratch used is the CURRENT device's: make the device that holds the
+ * buffers and owns `stream` current before the call.  The first call on a device
+ * looks up the scratch array's device address (once per device, with that device
+ * current); make that first call before any stream capture begins.  Every call on a device shares the one scratch array, so calls
  * that overlap on the GPU (different streams without ordering) race and give
  * wrong results: serialise them.
  */

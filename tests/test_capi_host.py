@@ -75,6 +75,19 @@ def test_argument_errors_return_before_launch(so):
     assert _fwd_bwd(so, ws=None) == E.FOAK_ERR_WORKSPACE
     assert _fwd_bwd(so, ws=FAKE + 16) == E.FOAK_ERR_WORKSPACE        # 256-byte alignment
     assert _fwd_bwd(so, wsb=256) == E.FOAK_ERR_WORKSPACE             # too small for N rows
+    # data-parallel pair: count into an 8-byte aligned int64, fused call with a device denominator
+    assert so.lib.foak_ce_count_valid(FAKE, 4, 32000, -100, None, None, None) == E.FOAK_ERR_INVALID_ARG
+    assert so.lib.foak_ce_count_valid(FAKE, 4, 32000, -100, FAKE + 4, None, None) == E.FOAK_ERR_INVALID_ARG
+    assert so.lib.foak_ce_count_valid(None, 4, 32000, -100, FAKE, None, None) == E.FOAK_ERR_INVALID_ARG
+    assert so.lib.foak_ce_count_valid(FAKE, -1, 32000, -100, FAKE, None, None) == E.FOAK_ERR_INVALID_ARG
+    assert so.lib.foak_ce_count_valid(FAKE, 4, 0, -100, FAKE, None, None) == E.FOAK_ERR_INVALID_ARG
+    dd = so.lib.foak_ce_fwd_bwd_devdenom
+    assert dd(FAKE, 1, 32000, FAKE, 4, 32000, -100, 1.0, None, FAKE, None, None, None, FAKE, 1 << 20,
+              None) == E.FOAK_ERR_INVALID_ARG                          # no denominator
+    assert dd(FAKE, 1, 32000, FAKE, 4, 32000, -100, 1.0, FAKE + 4, FAKE, None, None, None, FAKE, 1 << 20,
+              None) == E.FOAK_ERR_INVALID_ARG                          # misaligned int64
+    assert dd(FAKE, 1, 31999, FAKE, 4, 32000, -100, 1.0, FAKE, FAKE, None, None, None, FAKE, 1 << 20,
+              None) == E.FOAK_ERR_INVALID_ARG                          # ld < V
     # backward: dlogits must share logits' 16-byte phase
     st = so.lib.foak_ce_backward(FAKE + 2, FAKE, 1, 32000, FAKE, 4, 32000, -100, FAKE, None, 0.0, None, None)
     assert st == E.FOAK_ERR_INVALID_ARG

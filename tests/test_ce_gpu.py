@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads as wl
-from ce_helpers import (assert_grad_close, assert_loss_close, bits, sample_rows, to_device, to_f64)
+from ce_helpers import (assert_grad_close, assert_grad_rows, assert_loss_close, bits, to_device, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -181,6 +181,48 @@ def test_data_parallel_shards_compose(cuda_lib):
     np.testing.assert_array_equal(bits(torch.cat(parts)), bits(full))
 
 
+@pytest.mark.parametrize("dtype,V", [(wl.BF16, 5000), (wl.F32, 70001)])
+def test_device_denominator_shards_compose(cuda_lib, dtype, V):
+    """The data-parallel pair: foak_ce_count_valid counts each shard's labels on the
+    device, the counts are summed on the device (what an all-reduce does across
+    ranks), and foak_ce_fwd_bwd_devdenom divides by that total -- the shards'
+    losses add up to the whole batch's and their gradients equal it bit for bit,
+    and each shard equals foak_ce_fwd_bwd given the same denominator on the host."""
+    ce = cuda_lib
+    x, y = _rand(96, V, dtype, seed=32, sigma=2.0)
+    y[7] = V + 3  # a bad label: flagged by the count and by the fused call
+    n_valid, n_bad = oracle.count(y, V)
+    full = to_device(x, dtype)
+    o = ce.foak_ce_fwd_bwd(full, torch.from_numpy(y).cuda())
+    spans = [(0, 40), (40, 96)]
+    cnts, errs = [], []
+    for a, b in spans:
+        e = torch.empty(1, dtype=torch.int32, device="cuda")
+        cnts.append(ce.foak_ce_count_valid(torch.from_numpy(y[a:b].copy()).cuda(), V, err=e))
+        errs.append(e)
+    total = cnts[0] + cnts[1]  # the all-reduce of two ranks, on the device
+    tot_loss, parts = 0.0, []
+    for a, b in spans:
+        s = to_device(np.ascontiguousarray(x[a:b]), dtype)
+        s2 = s.clone()
+        ys = torch.from_numpy(y[a:b].copy()).cuda()
+        r = ce.foak_ce_fwd_bwd_devdenom(s, ys, total)
+        h = ce.foak_ce_fwd_bwd(s2, ys, denom=float(n_valid))
+        torch.cuda.synchronize()
+        assert r["loss"].item() == h["loss"].item()
+        assert torch.equal(bits_view(s), bits_view(s2))
+        tot_loss += r["loss"].item()
+        parts.append(s)
+    torch.cuda.synchronize()
+    assert [int(c.item()) for c in cnts] == [oracle.count(y[a:b], V)[0] for a, b in spans]
+    assert int(total.item()) == n_valid and n_bad == 1
+    assert [int(e.item()) for e in errs] == [1, 0]
+    assert tot_loss == pytest.approx(o["loss"].item(), rel=1e-6)
+    np.testing.assert_array_equal(bits(torch.cat(parts)), bits(full))
+    # an empty shard counts 0
+    assert int(ce.foak_ce_count_valid(torch.empty(0, dtype=torch.int64, device="cuda"), V).item()) == 0
+
+
 def test_deterministic_and_workspace_reuse(cuda_lib):
     x, y = _rand(300, 2048, wl.BF16, seed=8)
     losses = set()
@@ -197,9 +239,10 @@ def test_deterministic_and_workspace_reuse(cuda_lib):
 
 # ------------------------------------------------------------ full-size workloads
 
-def _full_size(cuda_lib, cfg, extra_rows=()):
+def _full_size(cuda_lib, cfg):
+    """The fused call on a whole workload: loss, n_valid, lse of every valid row and
+    every row of the in-place gradient against the oracle."""
     x, y, V, dtype = cfg["logits"], cfg["labels"], cfg["V"], cfg["dtype"]
-    N = x.shape[0]
     n_valid, _ = oracle.count(y, V)
     scale = oracle.scale_of(1.0, 0.0, n_valid)
     lse, rl, st, _ = oracle.rows(x, y, V, scale=scale, want_grad=False)
@@ -211,14 +254,7 @@ def _full_size(cuda_lib, cfg, extra_rows=()):
     assert out["n_valid"].item() == n_valid and out["err"].item() == 0
     valid = st == oracle.VALID
     np.testing.assert_allclose(to_f64(out["lse"])[valid], lse[valid], rtol=2e-6, atol=2e-6)
-    rows = sample_rows(N, y, extra=extra_rows)
-    _, _, _, g = oracle.rows(x[rows], y[rows], V, scale=scale)
-    idx = torch.from_numpy(rows).cuda()
-    got = to_f64(t.index_select(0, idx))
-    assert_grad_close(got, g)
-    ign = torch.from_numpy(np.nonzero(~valid)[0]).cuda()
-    assert int(t.index_select(0, ign).view(torch.int16 if dtype == wl.BF16 else torch.int32)
-               .count_nonzero().item()) == 0
+    assert_grad_rows(t, x, y, V, scale)
     return out, lse
 
 
@@ -233,11 +269,61 @@ def test_packed_batch_full_size(cuda_lib):
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
 def test_llama3_vocab_full_size(cuda_lib, dtype):
     cfg = wl.llama3(dtype=dtype)
-    out, lse = _full_size(cuda_lib, cfg, extra_rows=(wl.LLAMA3_CONST_ROW,))
+    out, lse = _full_size(cuda_lib, cfg)
     r = wl.LLAMA3_CONST_ROW
     # the all-equal row: lse = 3 + ln V exactly in the oracle
     assert lse[r] == pytest.approx(3.0 + math.log(128256), abs=1e-12)
     assert to_f64(out["lse"])[r] == pytest.approx(3.0 + math.log(128256), abs=3e-6)
+
+
+_WORKLOADS = {"mistral": wl.mistral, "packed": wl.packed,
+              "llama3": lambda: wl.llama3(dtype=wl.BF16), "llama3_f32": lambda: wl.llama3(dtype=wl.F32)}
+
+
+@pytest.mark.parametrize("in_place", [False, True], ids=["out_of_place", "in_place"])
+@pytest.mark.parametrize("name", sorted(_WORKLOADS))
+def test_forward_then_backward_full_size(cuda_lib, name, in_place):
+    """The separate forward and backward (FastCrossEntropyLoss as a pair) on whole
+    workloads, where every persistent CTA of the forward takes many rows (its ring
+    of stages wraps) and the backward's grid-stride loop runs many items per CTA:
+    loss, n_valid, lse and row_loss of every row, logits left unchanged by the
+    forward, and every row of the gradient (g = 0.75 from a device scalar)."""
+    cfg = _WORKLOADS[name]()
+    x, y, V, dtype = cfg["logits"], cfg["labels"], cfg["V"], cfg["dtype"]
+    N = x.shape[0]
+    g = 0.75
+    n_valid, _ = oracle.count(y, V)
+    scale = oracle.scale_of(g, 0.0, n_valid)
+    lse, rl, st, _ = oracle.rows(x, y, V, scale=scale, want_grad=False)
+    valid = st == oracle.VALID
+    t = to_device(x, dtype)
+    yd = torch.from_numpy(y).cuda()
+    f = cuda_lib.foak_ce_forward(t, yd, want_lse=True, want_row_loss=True)
+    torch.cuda.synchronize()
+    assert_loss_close(f["loss"].item(), oracle.mean(rl, st), dtype)
+    assert f["n_valid"].item() == n_valid and f["err"].item() == 0
+    np.testing.assert_allclose(to_f64(f["lse"])[valid], lse[valid], rtol=2e-6, atol=2e-6)
+    # a row term lse - x_y carries the lse's own rounding (the lse bar above) besides the
+    # loss bar's relative error: a label on a spike leaves ~1e-4 after subtracting ~25
+    rtol = 1e-5 if dtype == wl.F32 else 2e-3
+    got_rl = to_f64(f["row_loss"])
+    tol = rtol * np.abs(rl[valid]) + 2e-6 * (1.0 + np.abs(lse[valid]))
+    assert np.all(np.abs(got_rl[valid] - rl[valid]) <= tol), "row_loss out of tolerance"
+    assert np.all(got_rl[~valid] == 0.0)
+    x_dev = to_device(x, dtype)
+    assert torch.equal(bits_view(t), bits_view(x_dev)), "the forward must not write the logits"
+    del x_dev
+    gd = torch.tensor([g], dtype=torch.float32, device="cuda")
+    d, err = cuda_lib.foak_ce_backward(t, yd, f["lse"], gd, dlogits=t if in_place else None)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert (d.data_ptr() == t.data_ptr()) == in_place
+    assert_grad_rows(d, x, y, V, scale)
+    assert N == d.shape[0]
+
+
+def bits_view(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32)
 
 
 # ------------------------------------------------------------ failure detection

@@ -76,6 +76,63 @@ def test_shard_rows_partition():
             assert max(sizes) - min(sizes) <= 1
 
 
+def test_launcher_command_line():
+    dp = _dp()
+    argv = dp.launch_argv(4, "/x/bench.py", ["--gpus", "4", "--steps", "3"], 29512, python="py")
+    assert argv == ["py", "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=4", "--master-addr",
+                    "127.0.0.1", "--master-port=29512", "/x/bench.py", "--gpus", "4", "--steps", "3"]
+    with pytest.raises(ValueError):
+        dp.launch_argv(0, "b.py", [], 1)
+
+
+def test_rank_env(monkeypatch):
+    dp = _dp()
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert dp.rank_env() == (0, 1, 0)
+    monkeypatch.setenv("RANK", "3")
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    monkeypatch.setenv("LOCAL_RANK", "3")
+    assert dp.rank_env() == (3, 4, 3)
+    monkeypatch.setenv("RANK", "4")
+    with pytest.raises(ValueError):
+        dp.rank_env()
+
+
+def test_launched_ranks_run_the_data_parallel_step(tmp_path):
+    """Two gloo ranks started by the bench's launcher run dp.fused_step -- the bench's
+    timed step for N > 1 -- on their row shards: the all-reduced denominator is the
+    batch's n_valid, the summed partial losses are the batch's mean loss on both ranks,
+    and the shards' gradients are the whole batch's."""
+    import subprocess
+    import sys
+
+    import oracle
+
+    dp = _dp()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = os.path.join(root, "tests", "dp_rank_main.py")
+    env = dict(os.environ)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    r = subprocess.run(dp.launch_argv(2, script, [str(tmp_path)], _free_port()), env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    sys.path.insert(0, os.path.join(root, "tests"))
+    import dp_rank_main
+
+    x, y, V = dp_rank_main.case()
+    whole = oracle.ce(x, y, V)
+    grads = []
+    for rank in range(2):
+        b, e, denom, loss, world = open(tmp_path / f"res{rank}.txt").read().split()
+        assert int(world) == 2 and int(denom) == whole["n_valid"]
+        assert float(loss) == pytest.approx(whole["loss"], rel=1e-13)
+        assert (int(b), int(e)) == dp.shard_rows(x.shape[0], rank, 2)
+        grads.append(np.load(tmp_path / f"grad{rank}.npy"))
+    np.testing.assert_allclose(np.concatenate(grads), whole["grad"], rtol=1e-13, atol=1e-18)
+
+
 def test_two_ranks_reproduce_whole_batch(tmp_path):
     import oracle
 
