@@ -550,6 +550,6 @@ void foak_test_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns == 0 ? 
 
 void foak_test_skip_row_load(int64_t row) { g_skip_load_row.store(row < 0 ? -1 : row); }
 
-void foak_test_set_row_path(int32_t path) { g_row_path.store(path == 1 || path == 2 ? path : 0); }
+void foak_test_set_row_path(int32_t path) { g_row_path.store(path >= 1 && path <= 3 ? path : 0); }
 
 }  // extern "C"

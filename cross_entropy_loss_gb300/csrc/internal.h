@@ -85,7 +85,7 @@ cudaError_t launch_rope_apply(int es, void* X, int64_t T, int H, int64_t ldt, vo
 
 uint64_t test_wait_limit_ns();
 int64_t test_skip_load_row();
-int32_t test_row_path();  // 0 automatic, 1 one pass (clusters), 2 two-pass streaming
+int32_t test_row_path();  // 0 automatic, 1 one pass (CTA / clusters), 2 two-pass streaming, 3 independent warps
 
 // Streaming multiprocessor count of the current device (cached per device).
 int device_sm_count();

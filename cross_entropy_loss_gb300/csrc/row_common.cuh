@@ -197,6 +197,12 @@ __device__ __forceinline__ float row_denominator(const CeRowParams& p, int n_val
 // twice (log-sum-exp, then gradient): for rows longer than one CTA's slice.
 cudaError_t launch_ce_rows_long(bool grad, int elem_bytes, const CeRowParams& base, cudaStream_t stream);
 
+// Aligned rows of at most one 64 KB slice (V * elem_bytes a multiple of 16, every
+// row on a 16-byte boundary, dlogits in place): one CTA per SM, its 16 warps each
+// moving a 4 KB region of every row on their own.
+bool ce_rows_warp_fits(int elem_bytes, int64_t V);
+cudaError_t launch_ce_rows_warp(bool grad, int elem_bytes, const CeRowParams& base, cudaStream_t stream);
+
 // End of a row kernel: every CTA counts itself done; the last one reduces the
 // row loss terms in row order in float64 over D, publishes n_valid and the
 // error word, and resets the workspace header for the next call.

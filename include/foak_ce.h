@@ -434,11 +434,13 @@ void foak_test_skip_row_load(int64_t row);
 
 /*
  * Test hook: which row kernel the forward and fused calls use.  0 (default):
- * automatic -- rows that fit one CTA's 64 KB slice are swept once by one CTA,
- * longer rows are streamed twice by one CTA (log-sum-exp, then gradient);
- * 1: one pass, longer rows split over a cluster of 2, 4 or 8 CTAs; 2: the
- * two-pass streaming kernel for every row length.  Results agree up to fp32
- * summation order.  Other values are treated as 0.
+ * automatic -- aligned rows that fit one CTA's 64 KB slice go to the kernel whose
+ * 16 warps each stream a 4 KB region of every row on their own, other rows of one
+ * slice are swept once by one CTA in step, longer rows are streamed twice by one
+ * CTA (log-sum-exp, then gradient); 1: one pass with the CTA in step, longer rows
+ * split over a cluster of 2, 4 or 8 CTAs; 2: the two-pass streaming kernel for
+ * every row length; 3: as 0 (the independent-warp kernel wherever it applies).
+ * Results agree up to fp32 summation order.  Other values are treated as 0.
  */
 void foak_test_set_row_path(int32_t path);
 

@@ -1,9 +1,13 @@
-"""Both row kernels on the same inputs: the one-pass kernel (one CTA per row, or a
-cluster of 2-8 CTAs when the row is longer than a 64 KB slice) and the two-pass
-streaming kernel (one CTA per row, the row loaded twice in 64 KB chunks).  The
-automatic choice uses the one-pass kernel for rows of one slice and the
-two-pass kernel beyond; here each is forced through the row-path test hook and
-checked against the oracle with the same bars as the other fused tests.
+"""Every row kernel on the same inputs: the one-pass kernel (one CTA per row in
+step, or a cluster of 2-8 CTAs when the row is longer than a 64 KB slice), the
+two-pass streaming kernel (one CTA per row, the row loaded twice in 64 KB chunks)
+and the independent-warp kernel (aligned rows of one slice; each warp streams a
+4 KB region of every row).  The automatic choice takes the independent-warp
+kernel for aligned rows of one slice, the one-pass kernel for other rows of one
+slice and the two-pass kernel beyond; here each is forced through the row-path
+test hook (the independent-warp hook falls back to the automatic choice where
+it does not apply) and checked against the oracle with the same bars as the
+other fused tests.
 """
 import math
 
@@ -18,7 +22,7 @@ from test_ce_gpu import _check_fused, _rand
 
 pytestmark = pytest.mark.gpu
 
-ONE_PASS, TWO_PASS = 1, 2
+ONE_PASS, TWO_PASS, WARPS = 1, 2, 3
 
 
 @pytest.fixture
@@ -28,7 +32,7 @@ def row_path(cuda_lib, request):
     cuda_lib.lib.foak_test_set_row_path(0)
 
 
-@pytest.mark.parametrize("row_path", [ONE_PASS, TWO_PASS], indirect=True)
+@pytest.mark.parametrize("row_path", [ONE_PASS, TWO_PASS, WARPS], indirect=True)
 @pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
 @pytest.mark.parametrize("N,V", [(1, 1), (5, 7), (9, 8), (64, 1000), (33, 4097), (13, 32003), (6, 40000),
                                  (7, 70001), (5, 128256), (3, 200003)])
@@ -138,3 +142,31 @@ def test_two_pass_all_ignored_and_empty(cuda_lib):
         assert math.isnan(out["loss"].item()) and out["err"].item() == 0
     finally:
         ce.lib.foak_test_set_row_path(0)
+
+
+@pytest.mark.parametrize("row_path", [WARPS, ONE_PASS], indirect=True)
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+@pytest.mark.parametrize("g,denom", [(0.37, 123.0), (-1.5, 0.0), (0.0, 0.0)])
+def test_aligned_rows_scale_signs(cuda_lib, row_path, dtype, g, denom):
+    # aligned rows of one slice: a positive scale is folded into the exponent, zero
+    # and negative scales multiply; several rows per CTA so the row rings wrap
+    x, y = _rand(700, 4096, dtype, seed=43, n_ignore=60)
+    _check_fused(cuda_lib, x, y, 4096, dtype, g=g, denom=denom)
+
+
+@pytest.mark.parametrize("row_path", [WARPS], indirect=True)
+@pytest.mark.parametrize("V", [8, 1024, 8000, 16384, 32768])
+def test_independent_warps_region_edges(cuda_lib, row_path, V):
+    # rows that end inside, or exactly at the end of, a warp's 4 KB region and a
+    # 64 KB stage; labels at the first and last column and at a region boundary
+    dtype = wl.BF16
+    x, y = _rand(400, V, dtype, seed=V + 7, n_ignore=37, spikes=1e-3)
+    y[0], y[1], y[2] = 0, V - 1, min(V - 1, 2048)
+    _check_fused(cuda_lib, x, y, V, dtype)
+    f = cuda_lib.foak_ce_forward(to_device(x, dtype), torch.from_numpy(y).cuda(), want_lse=True,
+                                 want_row_loss=True)
+    torch.cuda.synchronize()
+    ref = oracle.ce(x, y, V)
+    assert_loss_close(f["loss"].item(), ref["loss"], dtype)
+    valid = ref["state"] == oracle.VALID
+    np.testing.assert_allclose(to_f64(f["lse"])[valid], ref["lse"][valid], rtol=2e-6, atol=2e-6)
