@@ -25,8 +25,10 @@ struct CeBwdParams {
     const int64_t* labels;
     int64_t N, V, ignore_index;
     const float* lse;
-    const float* g_ptr;
+    const float* g_ptr;    // device g; null: g_host
+    float g_host;
     float denom;
+    const int64_t* denom_dev;  // if set: the denominator, read from device memory
     int32_t* err;
     int64_t nseg;
 };
@@ -50,11 +52,12 @@ __global__ void __launch_bounds__(kBwdThreads) ce_backward_kernel(const CeBwdPar
     const int tid = threadIdx.x;
 
     int n_valid = 0, n_bad = 0;
-    if (p.denom <= 0.f || blockIdx.x == 0)
+    if ((!p.denom_dev && p.denom <= 0.f) || blockIdx.x == 0)
         count_labels(p.labels, p.N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
     if (blockIdx.x == 0 && tid == 0 && p.err) *p.err = n_bad > 0 ? FOAK_ERRBIT_LABEL_RANGE : 0;
-    const float g = p.g_ptr ? __ldg(p.g_ptr) : 1.f;
-    const float D = p.denom > 0.f ? p.denom : static_cast<float>(n_valid);
+    const float g = p.g_ptr ? __ldg(p.g_ptr) : p.g_host;
+    const float D = p.denom_dev ? static_cast<float>(__ldg(p.denom_dev))
+                                : (p.denom > 0.f ? p.denom : static_cast<float>(n_valid));
     const float scale = g / D;
     const int64_t row_bytes = p.ld * ES;
     const int64_t items = p.N * p.nseg;
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(kBwdThreads) ce_backward_kernel(const CeBwdPar
 cudaError_t launch_ce_backward(int elem_bytes, void* dx, const void* x, int64_t ld,
                                const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index,
                                const float* lse, const float* g_ptr, float denom, int32_t* err,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, float g_host, const int64_t* denom_dev) {
     CeBwdParams prm = {};
     prm.x = static_cast<const char*>(x);
     prm.dx = static_cast<char*>(dx);
@@ -167,7 +170,9 @@ cudaError_t launch_ce_backward(int elem_bytes, void* dx, const void* x, int64_t 
     prm.ignore_index = ignore_index;
     prm.lse = lse;
     prm.g_ptr = g_ptr;
+    prm.g_host = g_host;
     prm.denom = denom;
+    prm.denom_dev = denom_dev;
     prm.err = err;
     const int64_t nb_max = V * elem_bytes / 16;
     prm.nseg = std::max<int64_t>(1, (nb_max + kBwdSegVec - 1) / kBwdSegVec);

@@ -57,7 +57,12 @@ struct GemmParams {
     void* out;
     int64_t ldo;
     int32_t* err;
+    const int64_t* labels;  // statistics mode
+    float2* stats;
+    int stats_ld;
+    float* zlab;
 };
+static_assert(kBN == kGemmTileN, "statistics tiles are the output tiles");
 
 // Output tiles walked along the shorter dimension first.
 __device__ __forceinline__ int tile_m(const GemmParams& p, int t) { return p.n_fast ? t / p.tiles_n : t % p.tiles_m; }
@@ -186,6 +191,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
             const int m0 = tile_m(p, t) * kBM, n0 = tile_n(p, t) * kBN;
             const int row_blk = m0 + q * 32;  // first row of this warp's 32
             const int row = row_blk + lane;
+            // statistics mode: this row's running (max, sum of exp(c - max)) over the tile's
+            // columns, in natural-log units, and its label (its logit is kept when it is a column here)
+            const bool stats = p.mode == kGemmOutBf16Stats && row < p.M;
+            float st_m = kNegInf, st_s = 0.f;
+            const int64_t ylab = stats ? __ldg(p.labels + row) : -1;
             // TMEM -> registers one 32-column chunk ahead: chunk c + 1 is loading while
             // chunk c is converted and stored (two register sets, loop unrolled)
             const uint32_t taddr = tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
@@ -200,8 +210,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 const int col0 = n0 + c * 32;
                 if (col0 >= p.N) continue;
                 const bool full_chunk = col0 + 32 <= p.N;
-                if (p.mode == kGemmOutBf16) {
+                if (p.mode == kGemmOutBf16 || p.mode == kGemmOutBf16Stats) {
                     if (row >= p.M) continue;
+                    if (stats) {
+                        const int nv = min(32, p.N - col0);
+                        float cm = kNegInf;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nv) cm = fmaxf(cm, __uint_as_float(r[j]));
+                        const float mn = fmaxf(st_m, cm);
+                        const float mb = mn * kLog2e;
+                        float cs = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nv) cs += ex2(fmaf(__uint_as_float(r[j]), kLog2e, -mb));
+                        st_s = st_s * ex2(fmaf(st_m, kLog2e, -mb)) + cs;
+                        st_m = mn;
+                        if (ylab >= col0 && ylab < col0 + nv) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (col0 + j == ylab) p.zlab[row] = __uint_as_float(r[j]);
+                        }
+                    }
                     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo + col0;
                     if (full_chunk) {
                         uint4* o4 = reinterpret_cast<uint4*>(o);
@@ -240,6 +270,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                     }
                 }
             }
+            if (stats) p.stats[static_cast<int64_t>(row) * p.stats_ld + tile_n(p, t)] = make_float2(st_m, st_s);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -317,7 +348,7 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     ok = ok && (d.b_mn_major
                     ? encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.K), d.ldb, 64)
                     : encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N), d.ldb, kBN));
-    if (ok && d.mode != kGemmOutBf16)
+    if (ok && (d.mode == kGemmOutF32 || d.mode == kGemmOutF32Acc))
         ok = encode_f32_out(&p.tmC, d.out, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.M), d.ldo);
     if (!ok) return cudaErrorInvalidValue;
     p.M = d.M;
@@ -333,6 +364,12 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     p.out = d.out;
     p.ldo = d.ldo;
     p.err = d.err;
+    p.labels = d.labels;
+    p.stats = d.stats;
+    p.stats_ld = d.stats_ld;
+    p.zlab = d.zlab;
+    if (d.mode == kGemmOutBf16Stats && (!d.labels || !d.stats || !d.zlab || d.stats_ld < p.tiles_n))
+        return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

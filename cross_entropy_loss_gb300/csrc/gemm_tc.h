@@ -10,6 +10,10 @@ enum GemmOut : int {
     kGemmOutBf16 = 0,    // C = A * B^T, stored as bf16
     kGemmOutF32 = 1,     // C = A * B^T, stored as fp32
     kGemmOutF32Acc = 2,  // C += A * B^T in fp32 (read-modify-write)
+    kGemmOutBf16Stats = 3,  // as kGemmOutBf16, plus per-(row, 256-column tile) softmax statistics of
+                            // the fp32 accumulator: stats[row * stats_ld + tile] = (max, sum exp(c - max))
+                            // over the tile's columns, and zlab[row] = C[row][labels[row]] when the
+                            // label is a column of the product (rows of C are the labels' rows)
 };
 
 // C[M x N] (+)= A[M x K] * B[N x K]^T, bf16 operands, fp32 accumulation.
@@ -28,7 +32,15 @@ struct GemmDesc {
     int64_t ldo;
     GemmOut mode;
     int32_t* err;  // device error word for wait timeouts (may be null)
+    // kGemmOutBf16Stats only
+    const int64_t* labels;
+    float2* stats;
+    int stats_ld;
+    float* zlab;
 };
+
+// Output tiles of the GEMM are kGemmTileN columns wide (the statistics' tile width).
+constexpr int kGemmTileN = 256;
 
 cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream);
 

@@ -45,10 +45,12 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
 cudaError_t launch_count_valid(const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, int64_t* n_valid,
                                int32_t* err, cudaStream_t stream);
 
+// g = *g_ptr, or g_host when g_ptr is null; D = *denom_dev when given, else
+// denom > 0 ? denom : the valid labels of labels[0, N).
 cudaError_t launch_ce_backward(int elem_bytes, void* dx, const void* x, int64_t ld,
                                const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index,
                                const float* lse, const float* g_ptr, float denom, int32_t* err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, float g_host = 1.f, const int64_t* denom_dev = nullptr);
 
 // Chunked linear + CE (linear_ce.cu): workspace bytes and the launch sequence.
 size_t linear_ce_workspace_bytes(int64_t N, int64_t V, int64_t chunk);

@@ -4,17 +4,25 @@
 // fms-acceleration-foak 0.7.4 page; "add chunked loss" in the TODO of
 // fms-acceleration PR #79).
 //
-// For each chunk of rows [r0, r0 + C):
-//   1. Z  = H_c W^T            tcgen05 GEMM, bf16 out (C x V scratch)
-//   2. dZ = CE fwd+bwd on Z    the fused row kernel, in place, dividing by the
-//                              batch's n_valid (counted over all N labels), so
-//                              the result does not depend on the chunk size
-//   3. dH_c = dZ W             tcgen05 GEMM, bf16 out into dH
-//   4. dW (+)= dZ^T H          tcgen05 GEMM, fp32 out, once per group of
+// The batch's n_valid is counted once up front (unless the caller gives denom), so
+// every chunk divides by the same D and the result does not depend on the chunk
+// size.  Then for each chunk of rows [r0, r0 + C):
+//   1. Z  = H_c W^T            tcgen05 GEMM, bf16 out (C x V scratch); its epilogue
+//                              also reduces each row of each 128 x 256 output tile
+//                              from the fp32 accumulator to (max, sum exp(z - max))
+//                              and keeps the logit at the row's label
+//   2. lse, row terms          one warp per row merges its tiles' pairs
+//   3. dZ = (exp(Z - lse) - onehot) g / D   the streaming backward kernel, in
+//                              place on Z (one read, one write, no row reduction)
+//   4. dH_c = dZ W             tcgen05 GEMM, bf16 out into dH
+//   5. dW (+)= dZ^T H          tcgen05 GEMM, fp32 out, once per group of
 //                              kDeferChunks chunks (stored by the first group,
 //                              added by TMA reduce for the others)
 // and finally one CTA sums the per-row loss terms of all N rows in float64, in
-// row order, over the denominator.  Only one group's Z lives at a time.
+// row order, over the denominator.  Only one group's Z lives at a time.  Steps 1-2
+// are the GEMM-1 epilogue statistics of the chunked loss; the softmax itself is
+// rebuilt from Z and lse by step 3 rather than inside the producers of steps 4-5,
+// whose operands would then each need an exponential at the tensor cores' rate.
 #include <algorithm>
 
 #include "common.cuh"
@@ -35,28 +43,37 @@ constexpr int64_t kDeferChunks = 2;
 inline size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct LinWs {
-    CeWsHeader* hdr;
-    float* row_loss;   // N
-    int32_t* chunk_err;  // one word per chunk's CE call, then one word for the GEMMs
-    float* chunk_loss;   // scratch loss output of the chunk CE calls
-    void* z;           // kDeferChunks chunks x ldz bf16
+    int64_t* n_valid;    // the batch's valid labels (the denominator unless denom > 0)
+    float* row_loss;     // N
+    int32_t* chunk_err;  // one word per chunk's dZ pass, then one word for the GEMMs
+    float2* stats;       // C x tiles per-tile (max, sum exp) of the chunk's rows
+    float* zlab;         // C logits at the labels
+    float* lse;          // C
+    void* z;             // kDeferChunks chunks x ldz bf16
     size_t bytes;
 };
+
+int64_t lin_tiles(int64_t V) { return (V + kGemmTileN - 1) / kGemmTileN; }
 
 LinWs lin_layout(void* base, int64_t N, int64_t V, int64_t chunk) {
     const int64_t nchunks = N > 0 ? (N + chunk - 1) / chunk : 0;
     const int64_t ldz = (V + 63) / 64 * 64;
+    const size_t crows = static_cast<size_t>(std::min(chunk, std::max<int64_t>(N, 1)));
     LinWs w = {};
     size_t off = 0;
     char* b = static_cast<char*>(base);
-    w.hdr = reinterpret_cast<CeWsHeader*>(b + off);
-    off += sizeof(CeWsHeader);
+    w.n_valid = reinterpret_cast<int64_t*>(b + off);
+    off += 256;
     w.row_loss = reinterpret_cast<float*>(b + off);
     off += round256(static_cast<size_t>(N) * 4);
     w.chunk_err = reinterpret_cast<int32_t*>(b + off);
     off += round256(static_cast<size_t>(nchunks + 1) * 4);
-    w.chunk_loss = reinterpret_cast<float*>(b + off);
-    off += 256;
+    w.stats = reinterpret_cast<float2*>(b + off);
+    off += round256(crows * static_cast<size_t>(lin_tiles(V)) * sizeof(float2));
+    w.zlab = reinterpret_cast<float*>(b + off);
+    off += round256(crows * 4);
+    w.lse = reinterpret_cast<float*>(b + off);
+    off += round256(crows * 4);
     w.z = b + off;
     off += round256(static_cast<size_t>(std::min(kDeferChunks * chunk, std::max<int64_t>(N, 1))) *
                     static_cast<size_t>(ldz) * 2);
@@ -93,6 +110,32 @@ __global__ void __launch_bounds__(kFinThreads) linear_ce_finalize(const float* _
     }
 }
 
+constexpr int kMergeThreads = 256;  // one warp per row
+
+// lse and the row term of each of a chunk's rows from its tiles' (max, sum exp) pairs.
+__global__ void __launch_bounds__(kMergeThreads) chunk_lse_kernel(const float2* __restrict__ stats, int tiles,
+                                                                  const float* __restrict__ zlab,
+                                                                  const int64_t* __restrict__ labels, int rows,
+                                                                  int64_t V, int64_t ignore_index,
+                                                                  float* __restrict__ lse, float* __restrict__ row_loss) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    float m = kNegInf, s = 0.f;
+    for (int t = lane; t < tiles; t += 32) {
+        const float2 st = stats[static_cast<int64_t>(row) * tiles + t];
+        ms_merge(m, s, st.x, st.y);
+    }
+    warp_ms_reduce(m, s);
+    if (lane == 0) {
+        const int64_t y = labels[row];
+        const bool valid = y != ignore_index && y >= 0 && y < V;
+        const float l = fmaf(lg2(s), kLn2, m);
+        lse[row] = valid ? l : 0.f;
+        row_loss[row] = valid ? l - zlab[row] : 0.f;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_rows_finalize(const float* row_loss, const int64_t* labels, int64_t N, int64_t V,
@@ -120,6 +163,14 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
         e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * static_cast<size_t>(D) * 4, stream);
         if (e != cudaSuccess) return e;
     }
+    // the batch's denominator, counted once for every chunk (unless the caller gives one)
+    const int64_t* denom_dev = nullptr;
+    if (!(denom > 0.f) && nchunks > 0) {
+        e = launch_count_valid(labels, N, V, ignore_index, ws.n_valid, nullptr, stream);
+        if (e != cudaSuccess) return e;
+        denom_dev = ws.n_valid;
+    }
+    const int tiles = static_cast<int>(lin_tiles(V));
     const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
     __nv_bfloat16* dHb = static_cast<__nv_bfloat16*>(dH);
     __nv_bfloat16* zbuf = static_cast<__nv_bfloat16*>(ws.z);
@@ -141,15 +192,24 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
         g1.K = static_cast<int>(D);
         g1.out = z;
         g1.ldo = ldz;
-        g1.mode = kGemmOutBf16;
+        g1.mode = kGemmOutBf16Stats;
         g1.err = gemm_err;
+        g1.labels = labels + r0;
+        g1.stats = ws.stats;
+        g1.stats_ld = tiles;
+        g1.zlab = ws.zlab;
         e = launch_gemm_bf16(g1, stream);
         if (e != cudaSuccess) return e;
-        // 2. dZ = (softmax(Z) - onehot) * g / D in place; row terms into the batch's row_loss
-        e = launch_ce_rows(true, 2, z, z, ldz, labels + r0, rows, V, ignore_index, g, denom, ws.chunk_loss,
-                           nullptr, ws.row_loss + r0, nullptr, ws.chunk_err + c, ws.hdr, stream, labels, N);
+        // 2. lse and row terms of the chunk's rows (into the batch's row_loss)
+        chunk_lse_kernel<<<(rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32), kMergeThreads, 0, stream>>>(
+            ws.stats, tiles, ws.zlab, labels + r0, rows, V, ignore_index, ws.lse, ws.row_loss + r0);
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        // 3. dH_c = dZ W     (W is [V][D]: MN-major as the [K][N] operand)
+        // 3. dZ = (softmax(Z) - onehot) * g / D in place
+        e = launch_ce_backward(2, z, z, ldz, labels + r0, rows, V, ignore_index, ws.lse, nullptr, denom,
+                               ws.chunk_err + c, stream, g, denom_dev);
+        if (e != cudaSuccess) return e;
+        // 4. dH_c = dZ W     (W is [V][D]: MN-major as the [K][N] operand)
         GemmDesc g2 = {};
         g2.a = z;
         g2.lda = ldz;
@@ -166,7 +226,7 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
         g2.err = gemm_err;
         e = launch_gemm_bf16(g2, stream);
         if (e != cudaSuccess) return e;
-        // 4. once the group is complete: dW (+)= dZ_g^T H_g over the group's rows
+        // 5. once the group is complete: dW (+)= dZ_g^T H_g over the group's rows
         //    (dZ_g is [rows_g][V] = [K][M], H_g is [rows_g][D] = [K][N])
         if (slot == kDeferChunks - 1 || c == nchunks - 1) {
             const int64_t g0 = (c - slot) * chunk;

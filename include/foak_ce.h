@@ -331,11 +331,12 @@ foak_status foak_rope_apply_qk(void* Q, int64_t Hq, int64_t ldq, void* K, int64_
                                int32_t inverse, int32_t* err, void* stream);
 
 /*
- * Bytes of device workspace foak_linear_ce_chunked needs: a 256-byte header, N
- * float32 per-row loss terms, a few error words and two chunks of bf16 logits
- * (min(2 chunk, N) x V, rows padded to 64 elements: dW is updated once per pair
- * of chunks).  Same rules as the CE workspace:
- * 256-byte aligned, zero-filled before first use, left reusable by every call.
+ * Bytes of device workspace foak_linear_ce_chunked needs: the batch's label
+ * count, N float32 per-row loss terms, a few error words, one chunk's per-tile
+ * softmax statistics (chunk x ceil(V / 256) float pairs), its label logits and
+ * log-sum-exps, and two chunks of bf16 logits (min(2 chunk, N) x V, rows padded
+ * to 64 elements: dW is updated once per pair of chunks).  256-byte aligned; its
+ * contents need no initialisation and every call may reuse it.
  */
 size_t foak_linear_ce_workspace_size(int64_t N, int64_t V, int64_t D, int64_t chunk);
 
@@ -343,7 +344,10 @@ size_t foak_linear_ce_workspace_size(int64_t N, int64_t V, int64_t D, int64_t ch
  * Chunked linear + cross-entropy: loss, dH and dW of CE(H W^T) computed chunk by
  * chunk (Z = H_c W^T, dZ = (softmax(Z) - onehot) g / D, dH_c = dZ W,
  * dW += dZ^T H_c) without materialising the N x V logits; the products run on the
- * tcgen05 tensor cores with fp32 accumulation, Z/dZ are kept in bf16.
+ * tcgen05 tensor cores with fp32 accumulation, Z/dZ are kept in bf16.  The Z
+ * product's epilogue reduces its fp32 accumulator to per-row, per-tile softmax
+ * statistics and the label's logit, so the loss and log-sum-exp come from the
+ * unrounded logits and dZ is one streaming pass over Z.
  *   H (device)        bf16 [N][D] row-major (hidden states), D % 8 == 0
  *   W (device)        bf16 [V][D] row-major (LM-head weight, no bias)
  *   labels (device)   int64[N]; ignore_index as for the CE calls
