@@ -614,22 +614,24 @@ def chunked_timing(ce, torch, dev, stream, steps=5, warmup=2):
                 "ms_per_step": ms_r, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm, "peak_source": hsrc,
                 "bytes": "Q and K read and written once, positions; the 4 MB cos/sin table stays in L2"})
     del q, k, cache
-    # the three products of one chunk, alone
+    # the three products of the call, alone, at the shapes it runs them (dW once per pair of chunks)
     Z = torch.empty(chunk, V, dtype=torch.bfloat16, device=dev)
-    Zs = torch.randn(chunk, V, device=dev).to(torch.bfloat16)
+    Zs = torch.randn(2 * chunk, V, device=dev).to(torch.bfloat16)
     Hc = H[:chunk]
+    Hp = H[:2 * chunk]
     dHc = torch.empty(chunk, D, dtype=torch.bfloat16, device=dev)
     shapes = [
-        ("Z = H_c W^T (M=1024, N=32000, K=4096, K/K-major)",
+        ("Z = H_c W^T (M=1024, N=32000, K=4096, K/K-major)", chunk,
          lambda: ce.foak_gemm_bf16(Hc, W, Z, mode=ce.FOAK_GEMM_BF16)),
-        ("dH_c = dZ W (M=1024, N=4096, K=32000, K/MN-major)",
-         lambda: ce.foak_gemm_bf16(Zs, W, dHc, b_mn_major=True, mode=ce.FOAK_GEMM_BF16)),
-        ("dW += dZ^T H_c (M=32000, N=4096, K=1024, MN/MN-major, fp32 RMW)",
-         lambda: ce.foak_gemm_bf16(Zs, Hc, dW, a_mn_major=True, b_mn_major=True, mode=ce.FOAK_GEMM_F32_ACC)),
+        ("dH_c = dZ W (M=1024, N=4096, K=32000, K/MN-major)", chunk,
+         lambda: ce.foak_gemm_bf16(Zs[:chunk], W, dHc, b_mn_major=True, mode=ce.FOAK_GEMM_BF16)),
+        ("dW += dZ_pair^T H_pair (M=32000, N=4096, K=2048, MN/MN-major, fp32 TMA reduce-add of the 524 MB dW)",
+         2 * chunk,
+         lambda: ce.foak_gemm_bf16(Zs, Hp, dW, a_mn_major=True, b_mn_major=True, mode=ce.FOAK_GEMM_F32_ACC)),
     ]
-    for name, fn in shapes:
+    for name, kk, fn in shapes:
         gms = timed(fn, 10, 3)
-        gtf = 2.0 * chunk * V * D / (gms * 1e-3) / 1e12
+        gtf = 2.0 * kk * V * D / (gms * 1e-3) / 1e12
         res.append({"path": "foak_gemm_bf16", "workload": name, "steps": 10, "ms_per_step": gms, "TFLOPs": gtf,
                     "frac": gtf / peak, "peak_source": src})
     del H, W, dH, dW, Z, Zs

@@ -1,24 +1,37 @@
 // Persistent bf16 GEMM on the fifth-generation tensor cores (tcgen05) for the
 // chunked linear + cross-entropy:  C (+)= A * B^T  with fp32 accumulation.
 //
-// One CTA per SM walks output tiles of 128 x 256.  The walk runs along the
-// shorter tile dimension first (M fastest when there are fewer M tiles than N
-// tiles, else N fastest), so the CTAs working at once share a few tiles of the
-// operand with many tiles and every operand tile is fetched from HBM about once:
-// for dW (250 x 16 tiles) an M-fastest walk re-read the 131 MB dZ operand once
-// per N tile.  Warp roles:
+// Two kernels share the warp roles and the epilogue:
+//   gemm_bf16_tc_kernel       one CTA per SM, output tiles of 128 x 256 (used when M
+//                             has a single 128-row tile);
+//   gemm_bf16_tc_pair_kernel  clusters of two CTAs whose tensor cores compute one
+//                             256 x 256 tile together (tcgen05 cta_group::2): each
+//                             CTA loads its own 128 rows of A and its own 128 rows of
+//                             B (plain TMA, no multicast), the even CTA issues the
+//                             M = 256 MMAs over both CTAs' shared memory, and each
+//                             CTA's TMEM receives its 128 rows of the accumulator.
+//                             Per CTA a 64-deep k-block is 32 KB instead of 48 KB, so
+//                             the ring holds 6 stages and each SM reads a third less
+//                             operand data from L2 per MMA.
+// Warp roles:
 //   warp 0     TMA producer: 2-D tiled loads (128-byte swizzle) of the A and B
-//              k-blocks (64 deep) into a 4-stage shared-memory ring;
+//              k-blocks into a shared-memory ring;
 //   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
-//              one thread issues tcgen05.mma (M=128, N=256, K=16) per 16-deep
-//              slice, committing each stage back to the producer and each
-//              finished accumulator to the epilogue;
+//              one thread issues tcgen05.mma per 16-deep slice, committing each
+//              stage back to the producer(s) and each finished accumulator to the
+//              epilogue(s);
 //   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter of the accumulator,
-//              then bf16 store, fp32 store or fp32 read-modify-write.
+//              then bf16 store (optionally with per-row softmax statistics of the
+//              tile), fp32 store or fp32 reduce-add through the TMA engine.
 // The accumulators are double-buffered, so a tile's epilogue overlaps the next
-// tile's main loop.  Either operand may be K-major (row-major [rows][K]) or
-// MN-major (row-major [K][rows]); the shared-memory descriptors and the
-// instruction descriptor's major bits say which.  All waits are bounded.
+// tile's main loop.  Tiles are walked along the shorter tile dimension first (M
+// fastest when there are fewer M tiles than N tiles, else N fastest), so the CTAs
+// working at once share a few tiles of the operand with many tiles and every
+// operand tile is fetched from HBM about once: for dW (250 x 16 tiles) an
+// M-fastest walk re-read the 131 MB dZ operand once per N tile.  Either operand
+// may be K-major (row-major [rows][K]) or MN-major (row-major [K][rows]); the
+// shared-memory descriptors and the instruction descriptor's major bits say
+// which.  All waits are bounded.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -32,17 +45,23 @@
 
 namespace foak {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr uint32_t kABytes = kBM * kBK * 2;            // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;            // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;    // 48 KB
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr uint32_t kABytes = kBM * kBK * 2;            // 16 KB: 128 rows of A
+constexpr uint32_t kBBytes = kBN * kBK * 2;            // 32 KB: 256 rows of B
+constexpr uint32_t kBHalfBytes = kBBytes / 2;          // a pair CTA's 128 rows of B
 constexpr uint32_t kMNBlock = 64 * kBK * 2;            // one 64 (MN) x 64 (K) box: 8 KB
+constexpr int kStages1 = 4;                            // single CTA: 48 KB stages
+constexpr int kStages2 = 6;                            // pair CTA: 32 KB stages
+constexpr uint32_t kStageBytes1 = kABytes + kBBytes;
+constexpr uint32_t kStageBytes2 = kABytes + kBHalfBytes;
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 2 * kBN;
 // fp32 outputs leave through shared memory: per epilogue warp two 32 x 32 fp32
 // staging boxes (4 KB each, 128-byte swizzle) written back by TMA store or reduce-add.
 constexpr uint32_t kStageOutBytes = 32 * 32 * 4;
-constexpr size_t kGemmSmem = kStages * kStageBytes + 4 * 2 * kStageOutBytes + 1024;  // + alignment slack
+constexpr uint32_t kOutStaging = 4 * 2 * kStageOutBytes;
+constexpr size_t kGemmSmem1 = kStages1 * kStageBytes1 + kOutStaging + 1024;  // + alignment slack
+constexpr size_t kGemmSmem2 = kStages2 * kStageBytes2 + kOutStaging + 1024;
 
 struct GemmParams {
     CUtensorMap tmA;
@@ -51,8 +70,8 @@ struct GemmParams {
     int M, N, K;
     int a_mn, b_mn;
     int mode;
-    int tiles_m, tiles_n;
-    int n_fast;  // tile walk: N index fastest (else M)
+    int units_m, tiles_n;  // output units: 128-row (single) or 256-row (pair) by 256 columns
+    int n_fast;            // unit walk: N index fastest (else M)
     uint32_t idesc;
     void* out;
     int64_t ldo;
@@ -64,14 +83,108 @@ struct GemmParams {
 };
 static_assert(kBN == kGemmTileN, "statistics tiles are the output tiles");
 
-// Output tiles walked along the shorter dimension first.
-__device__ __forceinline__ int tile_m(const GemmParams& p, int t) { return p.n_fast ? t / p.tiles_n : t % p.tiles_m; }
-__device__ __forceinline__ int tile_n(const GemmParams& p, int t) { return p.n_fast ? t % p.tiles_n : t / p.tiles_m; }
+// Output units walked along the shorter dimension first.
+__device__ __forceinline__ int unit_m(const GemmParams& p, int t) { return p.n_fast ? t / p.tiles_n : t % p.units_m; }
+__device__ __forceinline__ int unit_n(const GemmParams& p, int t) { return p.n_fast ? t % p.tiles_n : t / p.units_m; }
+
+// Epilogue of one accumulator for this warp: its 32 TMEM lanes are rows row_blk ..
+// row_blk + 31 of C, 256 columns from n0 (tile column tn).  bf16 store (statistics
+// mode: also the row's (max, sum exp) over the tile and its label's logit), or fp32
+// store / reduce-add through two staging boxes and the TMA engine.
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, int row_blk, int n0, int tn,
+                                              int lane, float* out_stage, uint32_t& out_it) {
+    const int row = row_blk + lane;
+    // statistics mode: this row's running (max, sum of exp(c - max)) over the tile's
+    // columns, in natural-log units, and its label (its logit is kept when it is a column here)
+    const bool stats = p.mode == kGemmOutBf16Stats && row < p.M;
+    float st_m = kNegInf, st_s = 0.f;
+    const int64_t ylab = stats ? __ldg(p.labels + row) : -1;
+    // TMEM -> registers one 32-column chunk ahead: chunk c + 1 is loading while
+    // chunk c is converted and stored (two register sets, loop unrolled)
+    uint32_t ra[32], rb[32];
+    tc_ld32(taddr, ra);
+#pragma unroll
+    for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t(&r)[32] = (c & 1) ? rb : ra;
+        uint32_t(&rn)[32] = (c & 1) ? ra : rb;
+        tc_wait_ld(r);
+        if (c + 1 < kBN / 32) tc_ld32(taddr + static_cast<uint32_t>((c + 1) * 32), rn);
+        const int col0 = n0 + c * 32;
+        if (col0 >= p.N) continue;
+        const bool full_chunk = col0 + 32 <= p.N;
+        if (p.mode == kGemmOutBf16 || p.mode == kGemmOutBf16Stats) {
+            if (row >= p.M) continue;
+            if (stats) {
+                const int nv = min(32, p.N - col0);
+                float cm = kNegInf;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < nv) cm = fmaxf(cm, __uint_as_float(r[j]));
+                const float mn = fmaxf(st_m, cm);
+                const float mb = mn * kLog2e;
+                float cs = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < nv) cs += ex2(fmaf(__uint_as_float(r[j]), kLog2e, -mb));
+                st_s = st_s * ex2(fmaf(st_m, kLog2e, -mb)) + cs;
+                st_m = mn;
+                if (ylab >= col0 && ylab < col0 + nv) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j == ylab) p.zlab[row] = __uint_as_float(r[j]);
+                }
+            }
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo + col0;
+            if (full_chunk) {
+                uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                    w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                    w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                    w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                    o4[v] = w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.N) o[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+            }
+        } else if (row_blk < p.M) {
+            // stage the 32 x 32 box (row = lane) with the 128-byte swizzle, then one
+            // TMA store or reduce-add writes it back; two boxes alternate per warp
+            float* sbuf = out_stage + (out_it & 1) * (kStageOutBytes / 4);
+            ++out_it;
+            if (lane == 0) bulk_wait_group_read_1();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4*>(sbuf + lane * 32 + ((j ^ (lane & 7)) * 4)) =
+                    make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (p.mode == kGemmOutF32Acc) tma_reduce_add_2d(&p.tmC, sbuf, col0, row_blk);
+                else tma_store_2d(&p.tmC, sbuf, col0, row_blk);
+                bulk_commit_group();
+            }
+        }
+    }
+    if (stats) p.stats[static_cast<int64_t>(row) * p.stats_ld + tn] = make_float2(st_m, st_s);
+}
+
+// Shared-memory descriptors of one 16-deep slice kk of a stage: K-major operands
+// advance 32 bytes inside the 128-byte swizzle row, MN-major ones 16 K-rows of 128 bytes.
+__device__ __forceinline__ uint64_t slice_desc(uint32_t base, int mn_major, int kk) {
+    return mn_major ? smem_desc_sw128(base + kk * 2048, kMNBlock, 1024) : smem_desc_sw128(base + kk * 32, 16, 1024);
+}
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+    __shared__ uint64_t full[kStages1], empty[kStages1], acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
 
@@ -79,7 +192,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     const int unit0 = static_cast<int>(blockIdx.x);
     const int unit_step = static_cast<int>(gridDim.x);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStages1; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -100,7 +213,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base_sh;
-    const int num_tiles = p.tiles_m * p.tiles_n;
+    const int num_units = p.units_m * p.tiles_n;
     const int nk = (p.K + kBK - 1) / kBK;
 
     auto give_up = [&]() {
@@ -112,14 +225,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = unit0; t < num_tiles && !abort_sh; t += unit_step) {
-                const int m0 = tile_m(p, t) * kBM, n0 = tile_n(p, t) * kBN;
+            for (int t = unit0; t < num_units && !abort_sh; t += unit_step) {
+                const int m0 = unit_m(p, t) * kBM, n0 = unit_n(p, t) * kBN;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) { give_up(); break; }
                     if (abort_sh) break;
-                    unsigned char* sA = smem + static_cast<size_t>(stage) * kStageBytes;
+                    unsigned char* sA = smem + static_cast<size_t>(stage) * kStageBytes1;
                     unsigned char* sB = sA + kABytes;
-                    mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                    mbar_arrive_expect_tx(&full[stage], kStageBytes1);
                     const int k0 = kb * kBK;
                     if (!p.a_mn) {
                         tma_load_2d(sA, &p.tmA, k0, m0, &full[stage]);
@@ -133,7 +246,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
 #pragma unroll
                         for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sB + j * kMNBlock, &p.tmB, n0 + 64 * j, k0, &full[stage]);
                     }
-                    if (++stage == kStages) {
+                    if (++stage == kStages1) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -144,27 +257,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         if (lane == 0) {
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            for (int t = unit0; t < num_tiles && !abort_sh; t += unit_step) {
+            for (int t = unit0; t < num_units && !abort_sh; t += unit_step) {
                 if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u)) { give_up(); break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tbase + static_cast<uint32_t>(acc * kBN);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&full[stage], phase)) { give_up(); break; }
                     tc_fence_after();
-                    const uint32_t sA = smem_u32(smem + static_cast<size_t>(stage) * kStageBytes);
+                    const uint32_t sA = smem_u32(smem + static_cast<size_t>(stage) * kStageBytes1);
                     const uint32_t sB = sA + kABytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // K-major: advance 32 bytes inside the 128-byte swizzle row;
-                        // MN-major: advance 16 K-rows of 128 bytes.
-                        const uint64_t ad = p.a_mn ? smem_desc_sw128(sA + kk * 2048, kMNBlock, 1024)
-                                                   : smem_desc_sw128(sA + kk * 32, 16, 1024);
-                        const uint64_t bd = p.b_mn ? smem_desc_sw128(sB + kk * 2048, kMNBlock, 1024)
-                                                   : smem_desc_sw128(sB + kk * 32, 16, 1024);
-                        tc_mma_bf16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc_mma_bf16(d_tmem, slice_desc(sA, p.a_mn, kk), slice_desc(sB, p.b_mn, kk), p.idesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
                     tc_commit(&empty[stage]);
-                    if (++stage == kStages) {
+                    if (++stage == kStages1) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -177,100 +284,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     } else {
         // epilogue warps 2..5: TMEM lane quarter = warp % 4
         const int q = warp & 3;
-        float* out_stage = reinterpret_cast<float*>(smem + kStages * kStageBytes) + q * 2 * (kStageOutBytes / 4);
+        float* out_stage = reinterpret_cast<float*>(smem + kStages1 * kStageBytes1) + q * 2 * (kStageOutBytes / 4);
         uint32_t out_it = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = unit0; t < num_tiles; t += unit_step) {
+        for (int t = unit0; t < num_units; t += unit_step) {
             const bool ok = !abort_sh && mbar_wait_bounded(&acc_full[acc], acc_phase);
             if (!ok) {
                 if (lane == 0) give_up();
                 break;
             }
             tc_fence_after();
-            const int m0 = tile_m(p, t) * kBM, n0 = tile_n(p, t) * kBN;
-            const int row_blk = m0 + q * 32;  // first row of this warp's 32
-            const int row = row_blk + lane;
-            // statistics mode: this row's running (max, sum of exp(c - max)) over the tile's
-            // columns, in natural-log units, and its label (its logit is kept when it is a column here)
-            const bool stats = p.mode == kGemmOutBf16Stats && row < p.M;
-            float st_m = kNegInf, st_s = 0.f;
-            const int64_t ylab = stats ? __ldg(p.labels + row) : -1;
-            // TMEM -> registers one 32-column chunk ahead: chunk c + 1 is loading while
-            // chunk c is converted and stored (two register sets, loop unrolled)
+            const int tn = unit_n(p, t);
             const uint32_t taddr = tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-            uint32_t ra[32], rb[32];
-            tc_ld32(taddr, ra);
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t(&r)[32] = (c & 1) ? rb : ra;
-                uint32_t(&rn)[32] = (c & 1) ? ra : rb;
-                tc_wait_ld(r);
-                if (c + 1 < kBN / 32) tc_ld32(taddr + static_cast<uint32_t>((c + 1) * 32), rn);
-                const int col0 = n0 + c * 32;
-                if (col0 >= p.N) continue;
-                const bool full_chunk = col0 + 32 <= p.N;
-                if (p.mode == kGemmOutBf16 || p.mode == kGemmOutBf16Stats) {
-                    if (row >= p.M) continue;
-                    if (stats) {
-                        const int nv = min(32, p.N - col0);
-                        float cm = kNegInf;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < nv) cm = fmaxf(cm, __uint_as_float(r[j]));
-                        const float mn = fmaxf(st_m, cm);
-                        const float mb = mn * kLog2e;
-                        float cs = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < nv) cs += ex2(fmaf(__uint_as_float(r[j]), kLog2e, -mb));
-                        st_s = st_s * ex2(fmaf(st_m, kLog2e, -mb)) + cs;
-                        st_m = mn;
-                        if (ylab >= col0 && ylab < col0 + nv) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (col0 + j == ylab) p.zlab[row] = __uint_as_float(r[j]);
-                        }
-                    }
-                    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.ldo + col0;
-                    if (full_chunk) {
-                        uint4* o4 = reinterpret_cast<uint4*>(o);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                            o4[v] = w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < p.N) o[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-                    }
-                } else if (row_blk < p.M) {
-                    // stage the 32 x 32 box (row = lane) with the 128-byte swizzle, then one
-                    // TMA store or reduce-add writes it back; two boxes alternate per warp
-                    float* sbuf = out_stage + (out_it & 1) * (kStageOutBytes / 4);
-                    ++out_it;
-                    if (lane == 0) bulk_wait_group_read_1();
-                    __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<float4*>(sbuf + lane * 32 + ((j ^ (lane & 7)) * 4)) =
-                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (p.mode == kGemmOutF32Acc) tma_reduce_add_2d(&p.tmC, sbuf, col0, row_blk);
-                        else tma_store_2d(&p.tmC, sbuf, col0, row_blk);
-                        bulk_commit_group();
-                    }
-                }
-            }
-            if (stats) p.stats[static_cast<int64_t>(row) * p.stats_ld + tile_n(p, t)] = make_float2(st_m, st_s);
+            epilogue_tile(p, taddr, unit_m(p, t) * kBM + q * 32, tn * kBN, tn, lane, out_stage, out_it);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -285,6 +312,158 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+// CTA pairs (clusters of 2) on 256 x 256 output units.  CTA rank r holds rows
+// m0 + 128r .. m0 + 128r + 127 of the unit's A and rows n0 + 128r .. of its B; the
+// even CTA's full barriers count both CTAs' bytes (the odd CTA's copies complete on
+// them), its MMA thread commits each stage to both CTAs' empty barriers and each
+// accumulator to both CTAs' acc_full barriers (one commit each, no multicast), and
+// both CTAs' epilogue warps arrive on the even CTA's acc_empty barriers.
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_pair_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t full[kStages2], empty[kStages2], acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool lead = rank == 0;
+    const int unit0 = static_cast<int>(blockIdx.x >> 1);
+    const int unit_step = static_cast<int>(gridDim.x >> 1);
+    if (tid == 0) {
+        for (int s = 0; s < kStages2; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 8);  // the four epilogue warps of each CTA
+        }
+        fence_mbar_init();
+        abort_sh = 0;
+        prefetch_tensormap(&p.tmA);
+        prefetch_tensormap(&p.tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&tmem_base_sh, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers and TMEM exist before any copy, commit or remote arrive
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_sh;
+    const int num_units = p.units_m * p.tiles_n;
+    const int nk = (p.K + kBK - 1) / kBK;
+
+    auto give_up = [&]() {
+        abort_sh = 1;
+        if (p.err) atomicOr(p.err, FOAK_ERRBIT_TIMEOUT);
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = unit0; t < num_units && !abort_sh; t += unit_step) {
+                const int m0 = unit_m(p, t) * (2 * kBM) + static_cast<int>(rank) * kBM;
+                const int nb0 = unit_n(p, t) * kBN + static_cast<int>(rank) * (kBN / 2);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) { give_up(); break; }
+                    if (abort_sh) break;
+                    unsigned char* sA = smem + static_cast<size_t>(stage) * kStageBytes2;
+                    unsigned char* sB = sA + kABytes;
+                    if (lead) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes2);
+                    const uint32_t bar = mapa_u32(&full[stage], 0);
+                    const int k0 = kb * kBK;
+                    if (!p.a_mn) {
+                        tma_load_2d_pair(sA, &p.tmA, k0, m0, bar);
+                    } else {
+                        tma_load_2d_pair(sA, &p.tmA, m0, k0, bar);
+                        tma_load_2d_pair(sA + kMNBlock, &p.tmA, m0 + 64, k0, bar);
+                    }
+                    if (!p.b_mn) {
+                        tma_load_2d_pair(sB, &p.tmB, k0, nb0, bar);
+                    } else {
+                        tma_load_2d_pair(sB, &p.tmB, nb0, k0, bar);
+                        tma_load_2d_pair(sB + kMNBlock, &p.tmB, nb0 + 64, k0, bar);
+                    }
+                    if (++stage == kStages2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && lead) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            for (int t = unit0; t < num_units && !abort_sh; t += unit_step) {
+                if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u)) { give_up(); break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tbase + static_cast<uint32_t>(acc * kBN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase)) { give_up(); break; }
+                    tc_fence_after();
+                    const uint32_t sA = smem_u32(smem + static_cast<size_t>(stage) * kStageBytes2);
+                    const uint32_t sB = sA + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc_mma_bf16_pair(d_tmem, slice_desc(sA, p.a_mn, kk), slice_desc(sB, p.b_mn, kk), p.idesc,
+                                         (kb | kk) != 0 ? 1u : 0u);
+                    tc_commit_pair(smem_u32(&empty[stage]));
+                    tc_commit_pair(mapa_u32(&empty[stage], 1));
+                    if (++stage == kStages2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit_pair(smem_u32(&acc_full[acc]));
+                tc_commit_pair(mapa_u32(&acc_full[acc], 1));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+    } else {
+        // epilogue warps 2..5 of each CTA: TMEM lane quarter = warp % 4 of this CTA's 128 rows
+        const int q = warp & 3;
+        float* out_stage = reinterpret_cast<float*>(smem + kStages2 * kStageBytes2) + q * 2 * (kStageOutBytes / 4);
+        uint32_t out_it = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const uint32_t lead_acc_empty0 = mapa_u32(&acc_empty[0], 0);
+        const uint32_t lead_acc_empty1 = mapa_u32(&acc_empty[1], 0);
+        for (int t = unit0; t < num_units; t += unit_step) {
+            const bool ok = !abort_sh && mbar_wait_bounded(&acc_full[acc], acc_phase);
+            if (!ok) {
+                if (lane == 0) give_up();
+                break;
+            }
+            tc_fence_after();
+            const int tn = unit_n(p, t);
+            const uint32_t taddr = tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+            epilogue_tile(p, taddr, unit_m(p, t) * (2 * kBM) + static_cast<int>(rank) * kBM + q * 32, tn * kBN, tn,
+                          lane, out_stage, out_it);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc == 0 ? lead_acc_empty0 : lead_acc_empty1);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    if (warp >= 2 && lane == 0) bulk_wait_group_0();  // staged fp32 boxes fully written
+    tc_fence_before();
+    __syncthreads();
+    // no CTA frees its TMEM or leaves while the pair's MMAs, copies or arrivals may still reach it
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tbase, kTmemCols);
     }
 }
 
@@ -342,12 +521,16 @@ bool g_gemm_attr[64] = {false};
 cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     if (d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaSuccess;
     GemmParams p = {};
-    // K-major [rows][K]: inner K, boxes of 64 x rows-tile; MN-major [K][rows]: inner rows, 64 x 64 boxes.
+    const int tiles_m = (d.M + kBM - 1) / kBM;
+    // CTA pairs whenever M has at least two 128-row tiles
+    const bool pair = tiles_m >= 2;
+    // K-major [rows][K]: inner K, boxes of 64 x (the CTA's rows); MN-major [K][rows]: inner rows, 64 x 64 boxes.
     bool ok = d.a_mn_major ? encode_bf16(&p.tmA, d.a, static_cast<uint64_t>(d.M), static_cast<uint64_t>(d.K), d.lda, 64)
                            : encode_bf16(&p.tmA, d.a, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.M), d.lda, kBM);
     ok = ok && (d.b_mn_major
                     ? encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.K), d.ldb, 64)
-                    : encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N), d.ldb, kBN));
+                    : encode_bf16(&p.tmB, d.b, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N), d.ldb,
+                                  pair ? kBN / 2 : kBN));
     if (ok && (d.mode == kGemmOutF32 || d.mode == kGemmOutF32Acc))
         ok = encode_f32_out(&p.tmC, d.out, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.M), d.ldo);
     if (!ok) return cudaErrorInvalidValue;
@@ -357,10 +540,10 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     p.a_mn = d.a_mn_major ? 1 : 0;
     p.b_mn = d.b_mn_major ? 1 : 0;
     p.mode = d.mode;
-    p.tiles_m = (d.M + kBM - 1) / kBM;
+    p.units_m = pair ? (tiles_m + 1) / 2 : tiles_m;
     p.tiles_n = (d.N + kBN - 1) / kBN;
-    p.n_fast = p.tiles_m > p.tiles_n ? 1 : 0;
-    p.idesc = idesc_bf16_f32(kBM, kBN, p.a_mn, p.b_mn);
+    p.n_fast = p.units_m > p.tiles_n ? 1 : 0;
+    p.idesc = idesc_bf16_f32(pair ? 2 * kBM : kBM, kBN, p.a_mn, p.b_mn);
     p.out = d.out;
     p.ldo = d.ldo;
     p.err = d.err;
@@ -374,19 +557,48 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static int max_pairs[64] = {0};
     {
         std::lock_guard<std::mutex> lock(g_gemm_mu);
         if (!g_gemm_attr[dev]) {
             e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kGemmSmem));
+                                     static_cast<int>(kGemmSmem1));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gemm_bf16_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kGemmSmem2));
             if (e != cudaSuccess) return e;
             g_gemm_attr[dev] = true;
         }
     }
-    const int tiles = p.tiles_m * p.tiles_n;
-    const int grid = std::min(tiles, device_sm_count());
-    gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(p);
-    return cudaGetLastError();
+    const int units = p.units_m * p.tiles_n;
+    if (!pair) {
+        const int grid = std::min(units, device_sm_count());
+        gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem1, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmem2;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    {
+        std::lock_guard<std::mutex> lock(g_gemm_mu);
+        if (max_pairs[dev] == 0) {
+            cfg.gridDim = dim3(2, 1, 1);
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_pair_kernel, &cfg);
+            if (e != cudaSuccess) return e;
+            max_pairs[dev] = std::max(1, n);
+        }
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(units, max_pairs[dev])), 1, 1);
+    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_pair_kernel, p);
 }
 
 }  // namespace foak
