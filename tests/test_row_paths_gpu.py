@@ -170,3 +170,29 @@ def test_independent_warps_region_edges(cuda_lib, row_path, V):
     assert_loss_close(f["loss"].item(), ref["loss"], dtype)
     valid = ref["state"] == oracle.VALID
     np.testing.assert_allclose(to_f64(f["lse"])[valid], ref["lse"][valid], rtol=2e-6, atol=2e-6)
+
+
+@pytest.mark.parametrize("row_path", [WARPS], indirect=True)
+def test_independent_warps_wait_timeout(cuda_lib, row_path, monkeypatch):
+    """A row load that never happens makes the independent-warp kernel's waits run out
+    (fused and forward): the call reports FOAK_ERRBIT_TIMEOUT without faulting, every
+    warp winds down, and the next call is correct."""
+    ce = cuda_lib
+    x, y = _rand(400, 4096, wl.BF16, seed=19, n_ignore=20)
+    row = int(np.nonzero(y != -100)[0][200])
+    try:
+        ce.lib.foak_test_set_wait_limit_ns(100_000_000)
+        ce.lib.foak_test_skip_row_load(row)
+        out = ce.foak_ce_fwd_bwd(to_device(x, wl.BF16), torch.from_numpy(y).cuda())
+        f = ce.foak_ce_forward(to_device(x, wl.BF16), torch.from_numpy(y).cuda())
+        torch.cuda.synchronize()
+        assert out["err"].item() & ce.FOAK_ERRBIT_TIMEOUT
+        assert f["err"].item() & ce.FOAK_ERRBIT_TIMEOUT
+    finally:
+        ce.lib.foak_test_skip_row_load(-1)
+        ce.lib.foak_test_set_wait_limit_ns(0)
+    _check_fused(cuda_lib, x, y, 4096, wl.BF16)
+    f = ce.foak_ce_forward(to_device(x, wl.BF16), torch.from_numpy(y).cuda())
+    torch.cuda.synchronize()
+    assert f["err"].item() == 0
+    assert_loss_close(f["loss"].item(), oracle.ce(x, y, 4096)["loss"], wl.BF16)
