@@ -48,6 +48,15 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     __shared__ int iscratch[2 * kRowWarps];
     __shared__ double dred[kRowWarps];
     __shared__ int s_abort, s_last;
+    // Single-CTA rows: the batch's valid rows from row tail0 on, in row order (the
+    // same list in every CTA), handed out one at a time through the workspace
+    // header's counter, and the row and label whose copy went into each stage.
+    constexpr int kTail = THREADS >= 512 ? kTailMax : 1;
+    __shared__ int2 s_tail[kTail];  // (row, label): labels of valid rows fit 32 bits
+    __shared__ int s_ntail;
+    __shared__ int s_scan[kRowWarps];  // the tail scan's warp totals (count_labels has its own scratch)
+    __shared__ int s_qrow[kRowMaxStages];
+    __shared__ int64_t s_qlab[kRowMaxStages];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = p.k;
@@ -55,6 +64,15 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     const int64_t cid = K > 1 ? cluster_id_x() : blockIdx.x;
     const int64_t ncl = K > 1 ? cluster_count_x() : gridDim.x;
     const int64_t n_it = p.N > cid ? (p.N - 1 - cid) / ncl + 1 : 0;
+    // With a tail, this CTA's round-robin rows are those below tail0; the rest are
+    // shared.  Whether the call takes a tail is decided once the labels are counted
+    // (below); until then only rows that are round-robin either way are touched.
+    const bool dyn_ok = K == 1 && kTail > 1 && p.tail_rounds >= 0;
+    const int64_t tail_lo = dyn_ok ? static_cast<int64_t>(p.tail_rounds) * ncl : p.N;
+    const int64_t n_stat_lo = tail_lo > cid ? (tail_lo - 1 - cid) / ncl + 1 : 0;
+    bool dyn = dyn_ok;
+    int64_t tail0 = tail_lo;
+    int64_t n_stat = n_stat_lo;
     const int64_t row_bytes = p.ld * ES;
     const int tail_tid = K == 1 ? 32 : 0;
     const int64_t v0 = static_cast<int64_t>(rank) * p.per;
@@ -73,41 +91,73 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     // Producer state (thread 0): next row iteration to look at, valid rows issued.
     int64_t p_it = 0;
     uint32_t p_v = 0;
-    bool lab_cached = false;
+    int64_t lab_lim = 0;  // labels s_lab[0, lab_lim) are valid for this thread
     auto label_of = [&](int64_t it) -> int64_t {
-        return (lab_cached && it < kLabCache) ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
+        return it < lab_lim ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
     };
     // Fused kernel: the next load is found (label scan, address, size) before
     // the row's barrier and only issued after it, so thread 0's warp leaves the
     // barrier with little extra work and does not hold up the next one.
     const char* q_src = nullptr;
     uint32_t q_bytes = 0;
+    int64_t q_row = 0, q_lab = 0;
     int q_state = 0;  // 0 nothing prepared, 1 a load, 2 a skipped load (test hook), 3 no rows left
+    // Tail claims: the counter is bumped one claim ahead, so the atomic's latency is
+    // hidden behind a row instead of delaying thread 0 at a row barrier.
+    unsigned claim = 0;
+    bool claim_out = false;
+    bool ended = false;  // the end of the row sequence has been marked in s_qrow
+    auto claim_ahead = [&]() {
+        if (dyn && !claim_out) {
+            claim = atomicAdd(&p.ws->next, 1u);
+            claim_out = true;
+        }
+    };
+    // The next valid row of this CTA: its round-robin rows, then claimed tail rows.
+    auto next_row = [&](int64_t& row, int64_t& y) -> bool {
+        while (p_it < n_stat) {
+            row = cid + p_it * ncl;
+            y = label_of(p_it);
+            ++p_it;
+            if (dyn && p_it + 1 >= n_stat) claim_ahead();
+            if (y == p.ignore_index || y < 0 || y >= p.V) continue;
+            return true;
+        }
+        if (!dyn) return false;
+        claim_ahead();
+        const unsigned k = claim;
+        claim_out = false;
+        if (k >= static_cast<unsigned>(s_ntail)) return false;
+        const int2 e = s_tail[k];
+        row = e.x;
+        y = e.y;
+        claim_ahead();  // the next claim, already on its way
+        return true;
+    };
     auto prepare = [&]() {
         if (q_state != 0) return;
-        while (p_it < n_it) {
-            const int64_t row = cid + p_it * ncl;
-            const int64_t y = label_of(p_it);
-            ++p_it;
-            if (y == p.ignore_index || y < 0 || y >= p.V) continue;
-            if (row == p.skip_load_row) {  // test hook: the stage's barrier is never completed
-                q_state = 2;
-                return;
-            }
-            const char* rowp = p.x + row * row_bytes;
-            const RowGeom gm = AL ? RowGeom{0, p.V / EPV, 0} : row_geom<ES>(rowp, p.V);
-            int64_t nl = gm.nb - v0;
-            nl = nl < 0 ? 0 : (nl > p.per ? p.per : nl);
-            q_bytes = static_cast<uint32_t>(nl) * 16u;
-            q_src = rowp + static_cast<int64_t>(gm.h) * ES + v0 * 16;
-            q_state = 1;
+        int64_t row, y;
+        if (!next_row(row, y)) {
+            q_state = 3;
             return;
         }
-        q_state = 3;
+        q_row = row;
+        q_lab = y;
+        if (row == p.skip_load_row) {  // test hook: the stage's barrier is never completed
+            q_state = 2;
+            return;
+        }
+        const char* rowp = p.x + row * row_bytes;
+        const RowGeom gm = AL ? RowGeom{0, p.V / EPV, 0} : row_geom<ES>(rowp, p.V);
+        int64_t nl = gm.nb - v0;
+        nl = nl < 0 ? 0 : (nl > p.per ? p.per : nl);
+        q_bytes = static_cast<uint32_t>(nl) * 16u;
+        q_src = rowp + static_cast<int64_t>(gm.h) * ES + v0 * 16;
+        q_state = 1;
     };
     auto fire = [&]() {
+        const int st = static_cast<int>(p_v % static_cast<uint32_t>(p.stages));
         if (q_state == 1) {
-            const int st = static_cast<int>(p_v % static_cast<uint32_t>(p.stages));
             uint64_t* bar = &bars[st];
             mbar_arrive_expect_tx(bar, q_bytes);
             unsigned char* dst = smem + static_cast<size_t>(st) * p.stage_bytes;
@@ -115,54 +165,97 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
                 bulk_g2s(dst + off, q_src + off, min(kBulkChunk, q_bytes - off), bar);
         }
         if (q_state == 1 || q_state == 2) {
+            s_qrow[st] = static_cast<int>(q_row);
+            s_qlab[st] = q_lab;
             ++p_v;
             q_state = 0;
-        }
-    };
-    // Forward kernel: find and issue in one go after the barrier (measured faster there).
-    auto issue_direct = [&]() {
-        while (p_it < n_it) {
-            const int64_t row = cid + p_it * ncl;
-            const int64_t y = label_of(p_it);
-            ++p_it;
-            if (y == p.ignore_index || y < 0 || y >= p.V) continue;
-            if (row == p.skip_load_row) {  // test hook: the stage's barrier is never completed
-                ++p_v;
-                return;
-            }
-            const char* rowp = p.x + row * row_bytes;
-            const RowGeom gm = AL ? RowGeom{0, p.V / EPV, 0} : row_geom<ES>(rowp, p.V);
-            int64_t nl = gm.nb - v0;
-            nl = nl < 0 ? 0 : (nl > p.per ? p.per : nl);
-            const uint32_t bytes = static_cast<uint32_t>(nl) * 16u;
-            const int st = static_cast<int>(p_v % static_cast<uint32_t>(p.stages));
-            ++p_v;
-            uint64_t* bar = &bars[st];
-            mbar_arrive_expect_tx(bar, bytes);
-            const char* src = rowp + static_cast<int64_t>(gm.h) * ES + v0 * 16;
-            unsigned char* dst = smem + static_cast<size_t>(st) * p.stage_bytes;
-            for (uint32_t off = 0; off < bytes; off += kBulkChunk)
-                bulk_g2s(dst + off, src + off, min(kBulkChunk, bytes - off), bar);
-            return;
+        } else if (q_state == 3 && dyn && !ended) {
+            s_qrow[st] = -1;  // the consumers stop at this stage
+            ended = true;
         }
     };
     auto issue_next = [&]() {
-        if constexpr (GRAD) {
-            prepare();
-            fire();
-        } else {
-            issue_direct();
-        }
+        prepare();
+        fire();
     };
-    if (tid == 0)
-        for (int s = 0; s < p.stages; ++s) issue_next();
+    // Start-up order matters: every CTA reads all N labels (the count) and its own
+    // rows' labels, and if the first copies of all CTAs (three 64 KB rows each) went
+    // out first, those small reads would queue behind ~29 MB of row data.  So warp 0
+    // fetches the first 32 labels together, thread 0 issues the first row's copy,
+    // all label reads follow, and then the remaining copies.  A copy that would need
+    // a claimed tail row waits until the tail list exists.
+    const int64_t n_lab0 = min(n_stat_lo, static_cast<int64_t>(32));
+    if (warp == 0) {
+        if (lane < n_lab0) s_lab[lane] = __ldg(p.labels + cid + lane * ncl);
+        __syncwarp();
+        lab_lim = n_lab0;
+    }
+    int n_early = 0;
+    if (tid == 0) {
+        bool have = !dyn;
+        for (int64_t i = p_it; i < n_stat && !have; ++i) {
+            const int64_t y = label_of(i);
+            have = y != p.ignore_index && y >= 0 && y < p.V;
+        }
+        if (have) {
+            issue_next();
+            n_early = 1;
+        }
+    }
 
     int n_valid = 0, n_bad = 0;
     count_labels(p.count_labels, p.count_N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
     const float D = row_denominator(p, n_valid);
     const float scale = p.g / D;
-    // Labels of this CTA's first rows, for the row loop and the producer.
-    for (int64_t it = tid; it < n_it && it < kLabCache; it += blockDim.x) s_lab[it] = __ldg(p.labels + cid + it * ncl);
+    // The shared tail pays only when the round-robin split is uneven, i.e. when many
+    // rows are ignored (they take no load): measured on 8192-row padding-free batches
+    // (45% ignored) 148 -> 141 us, while on the Mistral batch (0.1% ignored) the tail's
+    // extra start-up costs 3 us.  Every CTA counts the same labels, so all agree; a
+    // call whose count covers other rows than its own (a chunk of a larger batch) keeps
+    // the round-robin split.
+    if (dyn_ok && (p.count_labels != p.labels || (p.N - n_valid) * static_cast<int64_t>(kTailIgnoredDiv) < p.N)) {
+        dyn = false;
+        tail0 = p.N;
+        n_stat = n_it;
+    }
+    // Labels of this CTA's rows (round-robin ones, then its share of the tail: rows
+    // tail0 + cid + j * ncl, which it zero-fills when they are ignored); warp 0
+    // already holds the first n_lab0.
+    const int64_t n_mine = dyn ? (p.N > tail0 + cid ? (p.N - 1 - tail0 - cid) / ncl + 1 : 0) : 0;
+    for (int64_t it = n_lab0 + tid; it < n_stat + n_mine && it < kLabCache; it += blockDim.x)
+        s_lab[it] = __ldg(p.labels + (it < n_stat ? cid + it * ncl : tail0 + cid + (it - n_stat) * ncl));
+    // The shared tail's valid rows, in row order: every thread counts a block of
+    // labels, a CTA scan gives each block its place, and each block writes its rows.
+    if (dyn) {
+        const int64_t T = p.N - tail0;  // at most kTailMax (the host sizes tail_rounds so)
+        constexpr int kPer = (kTail + kRowThreads - 1) / kRowThreads;
+        const int per_t = static_cast<int>((T + kRowThreads - 1) / kRowThreads);
+        const int64_t b0 = tail0 + static_cast<int64_t>(tid) * per_t;
+        int64_t yb[kPer];  // this thread's block of labels, loaded together
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            yb[k] = (k < per_t && b0 + k < p.N) ? __ldg(p.labels + b0 + k) : p.ignore_index;
+            cnt += (yb[k] != p.ignore_index && yb[k] >= 0 && yb[k] < p.V) ? 1 : 0;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) s_scan[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += s_scan[w];
+        int pos = base + incl - cnt;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            if (yb[k] != p.ignore_index && yb[k] >= 0 && yb[k] < p.V)
+                s_tail[pos++] = make_int2(static_cast<int>(b0 + k), static_cast<int>(yb[k]));
+        }
+        if (tid == kRowThreads - 1) s_ntail = base + incl;
+    }
     if constexpr (AL) {
         // -inf in every stage slot past this CTA's slice (the copies never write there)
         int64_t nl0 = p.V / EPV - v0;
@@ -174,7 +267,11 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
         }
     }
     __syncthreads();
-    lab_cached = true;
+    lab_lim = kLabCache;
+    // the remaining copies; the barrier publishes what thread 0 recorded for them
+    if (tid == 0)
+        for (int s = n_early; s < p.stages; ++s) issue_next();
+    __syncthreads();
 
     // Gradient constants: for scale > 0 the scale is folded into the exponent,
     // 2^(x*log2e - lse2 + log2(scale)); otherwise the exponential is multiplied by it.
@@ -186,9 +283,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     uint32_t c_v = 0;      // valid rows consumed
     uint32_t c_ok = 0;     // valid rows whose load was seen complete (a prefix)
     bool aborted = false;
-    for (int64_t it = 0; it < n_it; ++it) {
-        const int64_t row = cid + it * ncl;
-        const int64_t y = label_of(it);
+    auto do_row = [&](const int64_t row, const int64_t y) {
         const bool valid = y != p.ignore_index && y >= 0 && y < p.V;
         const char* rowp = p.x + row * row_bytes;
         const RowGeom gm = AL ? RowGeom{0, p.V / EPV, 0} : row_geom<ES>(rowp, p.V);
@@ -215,7 +310,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
                 p.row_loss[row] = 0.f;
                 if (p.lse) p.lse[row] = 0.f;
             }
-            continue;
+            return;
         }
 
         // Who owns the label column: the thread holding the head or tail scalar it
@@ -361,6 +456,29 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
             }
         }
         if (rank == 0 && tid == 0 && p.lse && !aborted) p.lse[row] = lse;
+    };
+
+    // One loop, one copy of the row code: this CTA's round-robin rows; then its share
+    // of the tail's ignored rows (only written: +0.0 and zero row terms); then the
+    // tail's valid rows it claimed, in the order their copies were issued, until the
+    // stage marked as the end (written by thread 0 at least one row barrier before
+    // any thread reads it).
+    for (int64_t it = 0;; ++it) {
+        int64_t row, y;
+        if (it < n_stat) {
+            row = cid + it * ncl;
+            y = label_of(it);
+        } else if (it < n_stat + n_mine) {
+            row = tail0 + cid + (it - n_stat) * ncl;
+            y = it < kLabCache ? s_lab[it] : __ldg(p.labels + row);
+            if (y != p.ignore_index && y >= 0 && y < p.V) continue;  // a tail row for the claims
+        } else {
+            if (!dyn || aborted) break;
+            row = s_qrow[c_st];
+            if (row < 0) break;
+            y = s_qlab[c_st];
+        }
+        do_row(row, y);
     }
 
     // Loads still in flight exist only after an abort: those issued past the
@@ -490,6 +608,16 @@ cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t s
     if (e != cudaSuccess) return e;
     const int64_t want = std::max<int64_t>(1, std::min<int64_t>(ncl, base.N));
     CeRowParams prm = base;
+    // Single-CTA rows: about 80% of the rows go round-robin and the valid rows of the
+    // rest are handed out at run time, so the CTAs (whose speed and share of valid
+    // rows differ) finish together; the shared tail is at most kTailMax rows.
+    prm.tail_rounds = -1;
+    if (pl.k == 1 && THREADS >= 512) {
+        const int64_t rounds = base.N / want;
+        int64_t tr = rounds * 8 / 10;
+        tr = std::max<int64_t>(tr, (base.N - kTailMax + want - 1) / want);
+        prm.tail_rounds = static_cast<int>(std::min<int64_t>(std::max<int64_t>(tr, 0), rounds));
+    }
     prm.k = pl.k;
     prm.per = pl.per;
     prm.stages = pl.stages;

@@ -74,11 +74,14 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
         s_abort = 0;
         s_last = 0;
     }
+    // the first 32 labels fetched together, so no producer waits on one round trip per row
+    const int64_t n_lab0 = min(n_it, static_cast<int64_t>(32));
+    if (warp == 0 && lane < n_lab0) s_lab[lane] = __ldg(p.labels + cid + lane * ncl);
     __syncthreads();
 
-    bool lab_cached = false;
+    int64_t lab_lim = n_lab0;  // s_lab[0, lab_lim) holds labels
     auto label_of = [&](int64_t it) -> int64_t {
-        return (lab_cached && it < kLabCache) ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
+        return it < lab_lim ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
     };
     bool aborted = false;
     auto check_abort = [&]() {
@@ -145,11 +148,15 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
         }
         ++s_iss[st];  // one issuer per stage at a time: the release protocol orders them
     };
+    // One chunk's copy first, then the label reads (which would otherwise queue behind
+    // every CTA's first S chunks of data), then the remaining S - 1 copies.
+    uint32_t k_init = 0;
     if (lane == 0) {
         advance();
-        for (uint32_t k = 0; k < S && p_has; ++k) {
-            if (warp == 0) issue(k);
+        if (p_has) {
+            if (warp == 0) issue(0);
             advance();
+            k_init = 1;
         }
     }
 
@@ -159,7 +166,13 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
     const float scale = p.g / D;
     for (int64_t it = tid; it < n_it && it < kLabCache; it += THREADS) s_lab[it] = __ldg(p.labels + cid + it * ncl);
     __syncthreads();
-    lab_cached = true;
+    lab_lim = kLabCache;
+    if (lane == 0) {
+        for (uint32_t k = k_init; k < S && p_has; ++k) {
+            if (warp == 0) issue(k);
+            advance();
+        }
+    }
 
     // For scale > 0 the scale is folded into the exponent; otherwise multiplied.
     const bool mul = !(scale > 0.f);

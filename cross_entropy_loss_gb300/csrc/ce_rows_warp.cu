@@ -103,14 +103,17 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
                     reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * kWStageBytes)[lv] = pad;
         }
     }
+    // the first 32 labels fetched together, so no warp waits on one round trip per row
+    const int n_lab0 = min(n_it, 32);
+    if (warp == 0 && lane < n_lab0) s_lab[lane] = __ldg(p.labels + cid + lane * ncl);
     __syncthreads();
 
     // Producer state of this warp (lane 0): next row iteration to scan, valid rows issued.
     int q_it = 0;
     uint32_t q_v = 0;
-    bool lab_cached = false;
+    int lab_lim = n_lab0;  // s_lab[0, lab_lim) holds labels
     auto label_of = [&](int it) -> int64_t {
-        return (lab_cached && it < kLabCache) ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
+        return it < lab_lim ? s_lab[it] : __ldg(p.labels + cid + it * ncl);
     };
     auto is_valid = [&](int64_t y) { return y != p.ignore_index && y >= 0 && y < p.V; };
     // Copy this warp's region of the next valid row into its stage (lane 0).
@@ -131,8 +134,9 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
             return;
         }
     };
-    if (lane == 0)
-        for (int s = 0; s < kWStages; ++s) issue_next();
+    // One row's copies first, then the label reads (which would otherwise queue behind
+    // every CTA's three rows of data), then the remaining copies.
+    if (lane == 0) issue_next();
 
     int n_valid = 0, n_bad = 0;
     count_labels(p.count_labels, p.count_N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
@@ -140,7 +144,9 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
     const float scale = p.g / D;
     for (int it = tid; it < n_it && it < kLabCache; it += kWThreads) s_lab[it] = __ldg(p.labels + cid + it * ncl);
     __syncthreads();
-    lab_cached = true;
+    lab_lim = kLabCache;
+    if (lane == 0)
+        for (int s = 1; s < kWStages; ++s) issue_next();
 
     // Gradient constants: for scale > 0 the scale is folded into the exponent,
     // 2^(x*log2e - lse2 + log2(scale)); otherwise the exponential is multiplied by it.
@@ -270,7 +276,8 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
         for (uint32_t k = c_ok; k < q_v; ++k)
             (void)mbar_wait_bounded(&full[k % kWStages], (k / kWStages) & 1u, p.wait_ns);
     }
-    rows_finish<kWThreads>(p, aborted, n_valid, n_bad, &s_last, dred);
+    __syncthreads();  // an abort seen by any warp is reported
+    rows_finish<kWThreads>(p, aborted || s_abort != 0, n_valid, n_bad, &s_last, dred);
 }
 
 // ------------------------------------------------------------------ host side

@@ -296,11 +296,20 @@ __device__ __forceinline__ void count_labels(const int64_t* __restrict__ labels,
                                              int64_t ignore_index, int* scratch, int& n_valid,
                                              int& n_bad) {
     int cv = 0, cb = 0;
-    for (int64_t i = threadIdx.x; i < N; i += blockDim.x) {
-        const int64_t y = __ldg(labels + i);
-        if (y != ignore_index) {
-            if (y >= 0 && y < V) ++cv;
-            else ++cb;
+    // eight independent loads in flight per thread, not one round trip per label
+    for (int64_t i0 = threadIdx.x; i0 < N; i0 += 8 * static_cast<int64_t>(blockDim.x)) {
+        int64_t y[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t i = i0 + static_cast<int64_t>(k) * blockDim.x;
+            y[k] = i < N ? __ldg(labels + i) : ignore_index;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (y[k] != ignore_index) {
+                if (y[k] >= 0 && y[k] < V) ++cv;
+                else ++cb;
+            }
         }
     }
     cv = __reduce_add_sync(0xffffffffu, cv);

@@ -8,11 +8,14 @@ namespace foak {
 
 // Header at the start of a CE workspace.  `done` counts finished CTAs of the
 // running call (the last one reduces the loss and sets it back to 0); `err`
-// collects error bits of the running call (read and cleared by that last CTA).
+// collects error bits of the running call (read and cleared by that last CTA);
+// `next` hands out the shared tail rows of the running call (reset to 0 by that
+// last CTA too).
 struct CeWsHeader {
     unsigned int done;
     unsigned int err;
-    unsigned int pad[62];
+    unsigned int next;
+    unsigned int pad[61];
 };
 static_assert(sizeof(CeWsHeader) == 256, "workspace header is 256 bytes");
 

@@ -17,7 +17,9 @@ constexpr int kRowMaxCluster = 8;
 constexpr int kMaxScalars = 7;                        // head or tail: < 16 bytes of bf16
 constexpr uint32_t kBulkChunk = 32768;
 constexpr int kLabCache = 1024;                       // labels of a CTA's first rows kept in smem
-constexpr size_t kSmemBudget = 227 * 1024 - 10 * 1024; // dynamic smem left after static use
+constexpr int kTailMax = 2048;                        // shared tail rows handed out at run time
+constexpr int kTailIgnoredDiv = 16;                   // ... when at least N / 16 rows are ignored
+constexpr size_t kSmemBudget = 227 * 1024 - 28 * 1024; // dynamic smem left after static use
 
 struct CeRowParams {
     const char* x;
@@ -38,6 +40,8 @@ struct CeRowParams {
     uint64_t wait_ns;        // limit of every shared-memory barrier wait
     int64_t skip_load_row;   // test hook: this row's slice is never loaded (-1: none)
     int l2_hint;             // two-pass kernel: 0 none, 1 pass 1 evict_last + pass 2 evict_first, 2 pass 2 evict_first
+    int tail_rounds;     // single-CTA rows: rows below tail_rounds * gridDim.x go round-robin, the
+                         // valid rows from there on are handed out one at a time; -1: all round-robin
     int k;               // CTAs per row (cluster size)
     int per;             // vectors per CTA slice
     int stages;          // rows in flight per CTA
@@ -236,6 +240,7 @@ __device__ __forceinline__ void rows_finish(const CeRowParams& p, bool aborted, 
         unsigned e = atomicExch(&p.ws->err, 0u);
         if (n_bad > 0) e |= FOAK_ERRBIT_LABEL_RANGE;
         if (p.err) *p.err = static_cast<int32_t>(e);
+        atomicExch(&p.ws->next, 0u);
         atomicExch(&p.ws->done, 0u);
     }
 }
