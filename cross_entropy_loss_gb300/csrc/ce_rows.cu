@@ -85,8 +85,22 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
         s_abort = 0;
         s_last = 0;
     }
+    if constexpr (AL) {
+        // -inf in every stage slot past this CTA's slice (the copies never write there)
+        int64_t nl0 = p.V / EPV - v0;
+        nl0 = nl0 < 0 ? 0 : (nl0 > p.per ? p.per : nl0);
+        const uint4 pad = RowMath<ES>::pad();
+        for (int s = 0; s < p.stages; ++s) {
+            uint4* sb = reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
+            for (int i = static_cast<int>(nl0) + tid; i < VPT * kRowThreads; i += kRowThreads) sb[i] = pad;
+        }
+    }
     __syncthreads();
     if (K > 1) cluster_sync();  // every CTA's exchange barriers exist before the first st.async
+    // Up to here only shared memory was touched: under a programmatic launch this
+    // set-up overlaps the end of the previous kernel, and everything below waits for it.
+    griddep_launch_dependents();
+    griddep_wait();
 
     // Producer state (thread 0): next row iteration to look at, valid rows issued.
     int64_t p_it = 0;
@@ -213,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     // extra start-up costs 3 us.  Every CTA counts the same labels, so all agree; a
     // call whose count covers other rows than its own (a chunk of a larger batch) keeps
     // the round-robin split.
-    if (dyn_ok && (p.count_labels != p.labels || (p.N - n_valid) * static_cast<int64_t>(kTailIgnoredDiv) < p.N)) {
+    if (dyn_ok && (p.count_labels != p.labels || p.count_N != p.N || (p.N - n_valid) * static_cast<int64_t>(kTailIgnoredDiv) < p.N)) {
         dyn = false;
         tail0 = p.N;
         n_stat = n_it;
@@ -255,16 +269,6 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
                 s_tail[pos++] = make_int2(static_cast<int>(b0 + k), static_cast<int>(yb[k]));
         }
         if (tid == kRowThreads - 1) s_ntail = base + incl;
-    }
-    if constexpr (AL) {
-        // -inf in every stage slot past this CTA's slice (the copies never write there)
-        int64_t nl0 = p.V / EPV - v0;
-        nl0 = nl0 < 0 ? 0 : (nl0 > p.per ? p.per : nl0);
-        const uint4 pad = RowMath<ES>::pad();
-        for (int s = 0; s < p.stages; ++s) {
-            uint4* sb = reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
-            for (int i = static_cast<int>(nl0) + tid; i < VPT * kRowThreads; i += kRowThreads) sb[i] = pad;
-        }
     }
     __syncthreads();
     lab_lim = kLabCache;
@@ -627,13 +631,14 @@ cudaError_t launch_typed(const CeRowParams& base, const Plan& pl, cudaStream_t s
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = static_cast<unsigned>(pl.k);
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(pl.k);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();  // the shared-memory set-up may overlap the previous kernel's end
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, ce_rows_kernel<ES, GRAD, THREADS, AL>, prm);
 }
 

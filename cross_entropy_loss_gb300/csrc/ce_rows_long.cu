@@ -74,6 +74,9 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
         s_abort = 0;
         s_last = 0;
     }
+    // shared memory only up to here (see ce_rows_kernel); global accesses wait below
+    griddep_launch_dependents();
+    griddep_wait();
     // the first 32 labels fetched together, so no producer waits on one round trip per row
     const int64_t n_lab0 = min(n_it, static_cast<int64_t>(32));
     if (warp == 0 && lane < n_lab0) s_lab[lane] = __ldg(p.labels + cid + lane * ncl);
@@ -393,8 +396,15 @@ cudaError_t launch_long_typed(const CeRowParams& base, cudaStream_t stream) {
     prm.stage_bytes = static_cast<uint32_t>(THREADS * VPT * 16);
     prm.stages = static_cast<int>(std::min<size_t>(kLongMaxStages, kSmemBudget / prm.stage_bytes));
     const size_t smem = static_cast<size_t>(prm.stages) * prm.stage_bytes;
-    ce_rows_long_kernel<ES, GRAD, THREADS, VPT><<<static_cast<unsigned>(grid), THREADS, smem, stream>>>(prm);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr = pdl_attribute();
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ce_rows_long_kernel<ES, GRAD, THREADS, VPT>, prm);
 }
 
 template <int ES, bool GRAD>

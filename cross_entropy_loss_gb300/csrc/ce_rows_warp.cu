@@ -103,6 +103,10 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
                     reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * kWStageBytes)[lv] = pad;
         }
     }
+    // shared memory only up to here: under a programmatic launch this overlaps the end
+    // of the previous kernel, and every global access below waits for it
+    griddep_launch_dependents();
+    griddep_wait();
     // the first 32 labels fetched together, so no warp waits on one round trip per row
     const int n_lab0 = min(n_it, 32);
     if (warp == 0 && lane < n_lab0) s_lab[lane] = __ldg(p.labels + cid + lane * ncl);
@@ -315,13 +319,14 @@ static cudaError_t launch_warp_typed(const CeRowParams& prm, cudaStream_t stream
     cfg.blockDim = dim3(kWThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 1;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, ce_rows_warp_kernel<ES, GRAD>, prm);
 }
 

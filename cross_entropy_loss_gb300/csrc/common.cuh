@@ -27,6 +27,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// A kernel launched with the programmatic-serialization attribute may start while the
+// previous kernel in its stream is still running; griddep_wait() returns once that
+// kernel has completed and its writes are visible, so no global memory may be touched
+// before it.  Without the attribute it returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next such kernel in the stream be scheduled (it still waits in griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

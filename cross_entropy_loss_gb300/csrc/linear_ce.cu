@@ -92,8 +92,18 @@ __global__ void __launch_bounds__(kFinThreads) linear_ce_finalize(const float* _
     __shared__ double dred[kFinThreads / 32];
     int n_valid = 0, n_bad = 0;
     count_labels(labels, N, V, ignore_index, iscratch, n_valid, n_bad);
+    // eight loads in flight per thread, then the additions in the same row order
     double acc = 0.0;
-    for (int64_t i = threadIdx.x; i < N; i += kFinThreads) acc += static_cast<double>(row_loss[i]);
+    for (int64_t i0 = threadIdx.x; i0 < N; i0 += 8 * kFinThreads) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t i = i0 + static_cast<int64_t>(k) * kFinThreads;
+            v[k] = i < N ? row_loss[i] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc += static_cast<double>(v[k]);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off);
     if ((threadIdx.x & 31) == 0) dred[threadIdx.x >> 5] = acc;
