@@ -17,8 +17,8 @@
 // Rows whose address is not 16-byte aligned are split into a scalar head (< 16
 // bytes), a run of 16-byte vectors and a scalar tail; the scalars are handled by
 // one thread each.  n_valid is counted by every CTA from the labels (64 KB at
-// N = 8192, an L2-resident read), and the mean loss is reduced in float64, in
-// row order, by whichever CTA finishes last.
+// N = 8192, an L2-resident read), and the mean loss is reduced (a double-float
+// sum in a fixed order) by whichever CTA finishes last.
 #include <algorithm>
 #include <cstdlib>
 #include <map>
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
     __shared__ uint64_t xbar[2];                  // completes when all K pairs of a row arrived
     __shared__ int64_t s_lab[kLabCache];
     __shared__ int iscratch[2 * kRowWarps];
-    __shared__ double dred[kRowWarps];
+    __shared__ DFloat dred[kRowWarps];
     __shared__ int s_abort, s_last;
     // Single-CTA rows: the batch's valid rows from row tail0 on, in row order (the
     // same list in every CTA), handed out one at a time through the workspace

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(THREADS, 1) ce_rows_long_kernel(const CeRowPar
     __shared__ float2 red_ms[2][WARPS];
     __shared__ int64_t s_lab[kLabCache];
     __shared__ int iscratch[2 * WARPS];
-    __shared__ double dred[WARPS];
+    __shared__ DFloat dred[WARPS];
     __shared__ int s_abort, s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

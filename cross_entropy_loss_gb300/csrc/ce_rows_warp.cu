@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
     __shared__ float2 pairs[kWPairSlots][kWWarps];
     __shared__ int64_t s_lab[kLabCache];
     __shared__ int iscratch[2 * kWWarps];
-    __shared__ double dred[kWWarps];
+    __shared__ DFloat dred[kWWarps];
     __shared__ volatile int s_abort;
     __shared__ int s_last;
 

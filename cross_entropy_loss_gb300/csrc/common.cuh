@@ -36,6 +36,74 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 // Lets the next such kernel in the stream be scheduled (it still waits in griddep_wait).
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// ------------------------------------------------ double-float sums of float terms
+// A value carried as hi + lo in two floats.  Additions take Knuth's TwoSum (an exact
+// error-free transform: s + e == a + b) and renormalise with Dekker's Fast2Sum, so a
+// sum of float terms keeps about 48 significant bits on the FP32 pipe; the FP64 pipe
+// of this part is narrow enough that a few dozen dependent float64 additions and a
+// division at the end of a kernel cost microseconds.  Non-finite sums propagate as
+// in plain float arithmetic.
+struct DFloat {
+    float hi, lo;
+};
+
+__device__ __forceinline__ DFloat df_add(DFloat x, float b) {
+    const float s = __fadd_rn(x.hi, b);
+    if (!isfinite(s)) return DFloat{s, 0.f};
+    const float bp = __fsub_rn(s, x.hi);
+    const float e = __fadd_rn(__fadd_rn(__fsub_rn(x.hi, __fsub_rn(s, bp)), __fsub_rn(b, bp)), x.lo);
+    const float hi = __fadd_rn(s, e);
+    return DFloat{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ DFloat df_add(DFloat x, DFloat y) {
+    DFloat r = df_add(x, y.hi);
+    if (!isfinite(r.hi)) return r;
+    const float hi = __fadd_rn(r.hi, y.lo);
+    return DFloat{hi, __fadd_rn(r.lo, __fsub_rn(y.lo, __fsub_rn(hi, r.hi)))};
+}
+
+// (hi + lo) / d as a float: the quotient of hi, corrected by the remainder hi - q d,
+// which an FMA gives exactly for a correctly rounded q, plus lo.
+__device__ __forceinline__ float df_div(DFloat x, float d) {
+    const float q = __fdiv_rn(x.hi, d);
+    if (!isfinite(q)) return q;
+    const float r = fmaf(-q, d, x.hi);
+    return __fadd_rn(q, __fdiv_rn(__fadd_rn(r, x.lo), d));
+}
+
+// Sum of v[0, n) over a CTA of THREADS threads, in a fixed order: thread t adds
+// v[t], v[t + THREADS], ... (eight loads in flight before their additions), then a
+// shuffle tree per warp and warp 0's partials in warp order.  `red` holds THREADS/32
+// values; the result is valid in thread 0.  Loads bypass L1 (the terms were written
+// by other CTAs of the same kernel).
+template <int THREADS>
+__device__ __forceinline__ DFloat block_sum_terms(const float* v, int64_t n, DFloat* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    DFloat acc{0.f, 0.f};
+    for (int64_t i0 = tid; i0 < n; i0 += 8 * THREADS) {
+        float t[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t i = i0 + static_cast<int64_t>(k) * THREADS;
+            t[k] = i < n ? __ldcg(v + i) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = df_add(acc, t[k]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const DFloat o{__shfl_down_sync(0xffffffffu, acc.hi, off), __shfl_down_sync(0xffffffffu, acc.lo, off)};
+        acc = df_add(acc, o);
+    }
+    if (lane == 0) red[warp] = acc;
+    __syncthreads();
+    DFloat tot{0.f, 0.f};
+    if (tid == 0)
+        for (int w = 0; w < THREADS / 32; ++w) tot = df_add(tot, red[w]);
+    return tot;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

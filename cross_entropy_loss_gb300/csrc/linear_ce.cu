@@ -18,8 +18,8 @@
 //   5. dW (+)= dZ^T H          tcgen05 GEMM, fp32 out, once per group of
 //                              kDeferChunks chunks (stored by the first group,
 //                              added by TMA reduce for the others)
-// and finally one CTA sums the per-row loss terms of all N rows in float64, in
-// row order, over the denominator.  Only one group's Z lives at a time.  Steps 1-2
+// and finally one CTA sums the per-row loss terms of all N rows (double-float, a
+// fixed order) over the denominator.  Only one group's Z lives at a time.  Steps 1-2
 // are the GEMM-1 epilogue statistics of the chunked loss; the softmax itself is
 // rebuilt from Z and lse by step 3 rather than inside the producers of steps 4-5,
 // whose operands would then each need an exponential at the tensor cores' rate.
@@ -81,7 +81,7 @@ LinWs lin_layout(void* base, int64_t N, int64_t V, int64_t chunk) {
     return w;
 }
 
-// loss = (sum of row terms, float64, row order) / D; n_valid; error word.
+// loss = (double-float sum of the row terms, fixed order) / D; n_valid; error word.
 __global__ void __launch_bounds__(kFinThreads) linear_ce_finalize(const float* __restrict__ row_loss,
                                                                   const int64_t* __restrict__ labels, int64_t N,
                                                                   int64_t V, int64_t ignore_index, float denom,
@@ -89,30 +89,13 @@ __global__ void __launch_bounds__(kFinThreads) linear_ce_finalize(const float* _
                                                                   float* loss, int32_t* n_valid_out,
                                                                   int32_t* err_out) {
     __shared__ int iscratch[2 * (kFinThreads / 32)];
-    __shared__ double dred[kFinThreads / 32];
+    __shared__ DFloat dred[kFinThreads / 32];
     int n_valid = 0, n_bad = 0;
     count_labels(labels, N, V, ignore_index, iscratch, n_valid, n_bad);
-    // eight loads in flight per thread, then the additions in the same row order
-    double acc = 0.0;
-    for (int64_t i0 = threadIdx.x; i0 < N; i0 += 8 * kFinThreads) {
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int64_t i = i0 + static_cast<int64_t>(k) * kFinThreads;
-            v[k] = i < N ? row_loss[i] : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc += static_cast<double>(v[k]);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off);
-    if ((threadIdx.x & 31) == 0) dred[threadIdx.x >> 5] = acc;
-    __syncthreads();
+    // the same 512-thread tree as the fused kernel's last CTA
+    const DFloat tot = block_sum_terms<kFinThreads>(row_loss, N, dred);
     if (threadIdx.x == 0) {
-        double tot = 0.0;
-        for (int w = 0; w < kFinThreads / 32; ++w) tot += dred[w];
-        const double D = denom > 0.f ? static_cast<double>(denom) : static_cast<double>(n_valid);
-        *loss = static_cast<float>(tot / D);
+        *loss = df_div(tot, denom > 0.f ? denom : static_cast<float>(n_valid));
         if (n_valid_out) *n_valid_out = n_valid;
         int32_t e = n_bad > 0 ? FOAK_ERRBIT_LABEL_RANGE : 0;
         for (int64_t c = 0; c < nchunks; ++c) e |= chunk_err[c];

@@ -1,7 +1,7 @@
 // Pieces shared by the row-wise cross-entropy kernels (one CTA or one cluster
 // per row, and one CTA streaming a long row in two passes): launch parameters,
 // row geometry for rows that do not start on a 16-byte boundary, the packed
-// per-thread arithmetic, and the last-CTA float64 loss reduction.
+// per-thread arithmetic, and the last-CTA loss reduction.
 #pragma once
 
 #include "common.cuh"
@@ -216,12 +216,12 @@ cudaError_t launch_ce_rows_long(bool grad, int elem_bytes, const CeRowParams& ba
 bool ce_rows_warp_fits(int elem_bytes, int64_t V);
 cudaError_t launch_ce_rows_warp(bool grad, int elem_bytes, const CeRowParams& base, cudaStream_t stream);
 
-// End of a row kernel: every CTA counts itself done; the last one reduces the
-// row loss terms in row order in float64 over D, publishes n_valid and the
+// End of a row kernel: every CTA counts itself done; the last one sums the row
+// loss terms (block_sum_terms: double-float, a fixed order) over D, publishes n_valid and the
 // error word, and resets the workspace header for the next call.
 template <int THREADS>
 __device__ __forceinline__ void rows_finish(const CeRowParams& p, bool aborted, int n_valid, int n_bad,
-                                            int* s_last, double* dred) {
+                                            int* s_last, DFloat* dred) {
     constexpr int WARPS = THREADS / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __syncthreads();
@@ -234,29 +234,9 @@ __device__ __forceinline__ void rows_finish(const CeRowParams& p, bool aborted, 
     __syncthreads();
     if (!*s_last) return;
     __threadfence();
-    // Eight loads in flight per thread before the additions (a dependent round trip per
-    // term took ~6 us for 4096 rows); each thread still adds its rows tid, tid + THREADS,
-    // ... in order, and a missing term adds +0.0, which leaves the sum unchanged.
-    double acc = 0.0;
-    for (int64_t i0 = tid; i0 < p.N; i0 += 8 * THREADS) {
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int64_t i = i0 + static_cast<int64_t>(k) * THREADS;
-            v[k] = i < p.N ? __ldcg(p.row_loss + i) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc += static_cast<double>(v[k]);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off);
-    if (lane == 0) dred[warp] = acc;
-    __syncthreads();
+    const DFloat tot = block_sum_terms<THREADS>(p.row_loss, p.N, dred);
     if (tid == 0) {
-        double tot = 0.0;
-        for (int w = 0; w < WARPS; ++w) tot += dred[w];
-        const double Dd = static_cast<double>(row_denominator(p, n_valid));
-        *p.loss = static_cast<float>(tot / Dd);
+        *p.loss = df_div(tot, row_denominator(p, n_valid));
         if (p.n_valid) *p.n_valid = n_valid;
         unsigned e = atomicExch(&p.ws->err, 0u);
         if (n_bad > 0) e |= FOAK_ERRBIT_LABEL_RANGE;

@@ -42,7 +42,9 @@
  *   last kernel of the call.  With n_valid == 0 and denom <= 0 the loss is 0/0 =
  *   NaN (as torch's mean reduction gives) and every gradient row is +0.0.
  * - The result is deterministic for a given input and device: the loss is the
- *   float64 sum of per-row float32 terms in row order, reduced by a fixed tree.
+ *   sum of the per-row float32 terms in a fixed order (each of 512 threads adds
+ *   rows t, t + 512, ...; then a fixed tree) carried as a double-float (hi + lo,
+ *   about 48 significant bits, Knuth's TwoSum), divided by D and rounded to float.
  */
 #ifndef FOAK_CE_H
 #define FOAK_CE_H
@@ -190,8 +192,8 @@ size_t foak_ce_host_workspace_size(int64_t N);
  * the labels and then the logits to the device in row chunks on a copy stream of
  * its own and runs the fused kernel of foak_ce_fwd_bwd on each chunk as soon as it
  * has landed (on `stream`), so the arithmetic hides under the host-to-device copy;
- * every chunk divides by the n_valid of all N rows (or denom), and one float64
- * reduction in row order over all N rows gives the loss, as in foak_ce_fwd_bwd.
+ * every chunk divides by the n_valid of all N rows (or denom), and one reduction
+ * over all N rows in the same order as foak_ce_fwd_bwd's gives the loss.
  * This is the same mean-reduced cross-entropy and in-place gradient as the
  * FastCrossEntropyLoss kernel of the FOAK pages (fms-acceleration PR #79,
  * Description item 4); the pages fix no host interface, so this one is ours.

@@ -370,3 +370,36 @@ def test_many_rows_per_cta(cuda_lib):
     N, V = 160_000, 64
     x, y = _rand(N, V, wl.F32, seed=12, n_ignore=N // 10)
     _check_fused(cuda_lib, x, y, V, wl.F32)
+
+
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
+def test_loss_sum_within_one_ulp_of_exact(cuda_lib, dtype):
+    """The loss is the exact sum of the kernel's own row terms (lse - x_y in float32,
+    reproduced here from the returned lse) over D, to within one float ulp.  Row 0's
+    label logit is -1000 (a term near 1e3), every other row's +25 (terms near 2e-6,
+    each below half an ulp of the running total): together the small terms move the
+    sum by over a hundred ulps, which a float accumulation would lose entirely.  bf16
+    takes the one-CTA row kernel, fp32 (125 KB rows) the two-pass one."""
+    N, V = 4096, 32000
+    x = wl.normal_matrix(N, V, seed=77, sigma=2.0, dtype=dtype)
+    y = wl.uniform_labels(N, V, seed=77)
+    r = np.arange(N)
+    val = np.where(r == 0, -1000.0, 25.0)
+    x[r, y] = wl.f64_to_bf16_bits(val) if dtype == wl.BF16 else val.astype(np.float32)
+    y[wl.pick_rows(N, 50, seed=77, exclude=(0,))] = -100
+    out = cuda_lib.foak_ce_fwd_bwd(to_device(x, dtype), torch.from_numpy(y).cuda(), want_lse=True)
+    lse = out["lse"].cpu().numpy()
+    valid = y != -100
+    xy = x[r[valid], y[valid]]
+    xy = wl.bf16_bits_to_f64(xy).astype(np.float32) if dtype == wl.BF16 else xy
+    terms = lse[valid] - xy  # float32 arithmetic, as in the kernel
+    n = int(valid.sum())
+    want = np.float32(math.fsum(terms.astype(np.float64)) / n)
+    got = np.float32(out["loss"].item())
+    assert out["n_valid"].item() == n
+    assert abs(int(got.view(np.int32)) - int(want.view(np.int32))) <= 1, (got, want)
+    # the same terms accumulated in float32 from row 0 on land far from the exact value
+    naive = np.float32(0.0)
+    for t in terms:
+        naive = np.float32(naive + t)
+    assert abs(int(np.float32(naive / np.float32(n)).view(np.int32)) - int(want.view(np.int32))) > 50

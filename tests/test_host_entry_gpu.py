@@ -5,7 +5,7 @@ Bars: the same as the fused call against the oracle (loss 1e-5 / 2e-3 relative,
 dlogits one bf16 ulp or 1e-6, ignored rows +0.0, n_valid and error word exact);
 against foak_ce_fwd_bwd on the same inputs the results are bit-identical (each
 row is computed the same way whatever the chunking, and the loss is the same
-float64 row-order sum).
+reduction in the same order).
 """
 import math
 
