@@ -225,24 +225,32 @@ __device__ __forceinline__ void rows_finish(const CeRowParams& p, bool aborted, 
     constexpr int WARPS = THREADS / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __syncthreads();
+    unsigned e = 0;
     if (tid == 0) {
         if (aborted) atomicOr(&p.ws->err, static_cast<unsigned>(FOAK_ERRBIT_TIMEOUT));
         __threadfence();
         const unsigned t = atomicAdd(&p.ws->done, 1u);
-        *s_last = t == gridDim.x - 1;
+        const bool last = t == gridDim.x - 1;
+        *s_last = last;
+        if (last) {
+            // Every other CTA has published its row terms and error bits and made its
+            // last claim: this fence orders the reads below after theirs (the barrier
+            // extends it to the CTA's other threads), and the header is taken and reset
+            // now, its atomics' latency hidden under the sum.
+            __threadfence();
+            e = atomicExch(&p.ws->err, 0u);
+            atomicExch(&p.ws->next, 0u);
+            atomicExch(&p.ws->done, 0u);
+        }
     }
     __syncthreads();
     if (!*s_last) return;
-    __threadfence();
     const DFloat tot = block_sum_terms<THREADS>(p.row_loss, p.N, dred);
     if (tid == 0) {
         *p.loss = df_div(tot, row_denominator(p, n_valid));
         if (p.n_valid) *p.n_valid = n_valid;
-        unsigned e = atomicExch(&p.ws->err, 0u);
         if (n_bad > 0) e |= FOAK_ERRBIT_LABEL_RANGE;
         if (p.err) *p.err = static_cast<int32_t>(e);
-        atomicExch(&p.ws->next, 0u);
-        atomicExch(&p.ws->done, 0u);
     }
 }
 
