@@ -145,11 +145,16 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
     // every CTA's three rows of data), then the remaining copies.
     if (lane == 0) issue_next();
 
+    // The forward needs the denominator only for the loss: when the call counts its own
+    // labels, each CTA counts those of its rows on the way and the last CTA adds them up
+    // (no read of all N labels by every CTA at start-up).  The fused sweep scales every
+    // gradient by g / D, so it counts first.
+    const bool late_count = !GRAD && p.count_labels == p.labels && p.count_N == p.N;
     int n_valid = 0, n_bad = 0;
-    count_labels(p.count_labels, p.count_N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
+    if (!late_count) count_labels(p.count_labels, p.count_N, p.V, p.ignore_index, iscratch, n_valid, n_bad);
     const float D = row_denominator(p, n_valid);
     const float scale = p.g / D;
-    for (int it = tid; it < n_it && it < kLabCache; it += kWThreads) s_lab[it] = __ldg(p.labels + cid + it * ncl);
+    for (int it = n_lab0 + tid; it < n_it && it < kLabCache; it += kWThreads) s_lab[it] = __ldg(p.labels + cid + it * ncl);
     __syncthreads();
     lab_lim = kLabCache;
     if (lane == 0)
@@ -226,6 +231,10 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
     for (int it = 0; it < n_it; ++it) {
         const int row = cid + it * ncl;
         const int64_t y = label_of(it);
+        if (late_count && tid == 0) {
+            if (is_valid(y)) ++n_valid;
+            else if (y != p.ignore_index) ++n_bad;
+        }
         if (!is_valid(y)) {
             if constexpr (GRAD) {
                 if (!aborted) {
@@ -291,7 +300,7 @@ __global__ void __launch_bounds__(kWThreads, 1) ce_rows_warp_kernel(const CeRowP
             (void)mbar_wait_bounded(&full[k % kWStages], (k / kWStages) & 1u, p.wait_ns);
     }
     __syncthreads();  // an abort seen by any warp is reported
-    rows_finish<kWThreads>(p, aborted || s_abort != 0, n_valid, n_bad, &s_last, dred);
+    rows_finish<kWThreads>(p, aborted || s_abort != 0, n_valid, n_bad, &s_last, dred, late_count);
 }
 
 // ------------------------------------------------------------------ host side

@@ -15,7 +15,9 @@ struct CeWsHeader {
     unsigned int done;
     unsigned int err;
     unsigned int next;
-    unsigned int pad[61];
+    unsigned int nvalid;  // label counts added by each CTA when they are counted on the way
+    unsigned int nbad;
+    unsigned int pad[59];
 };
 static_assert(sizeof(CeWsHeader) == 256, "workspace header is 256 bytes");
 

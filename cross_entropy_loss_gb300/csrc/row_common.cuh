@@ -218,15 +218,21 @@ cudaError_t launch_ce_rows_warp(bool grad, int elem_bytes, const CeRowParams& ba
 
 // End of a row kernel: every CTA counts itself done; the last one sums the row
 // loss terms (block_sum_terms: double-float, a fixed order) over D, publishes n_valid and the
-// error word, and resets the workspace header for the next call.
+// error word, and resets the workspace header for the next call.  With local_counts,
+// n_valid and n_bad (thread 0's) are this CTA's counts of the labels of its own rows,
+// added to the header before the CTA counts itself done; the last CTA takes the totals.
 template <int THREADS>
 __device__ __forceinline__ void rows_finish(const CeRowParams& p, bool aborted, int n_valid, int n_bad,
-                                            int* s_last, DFloat* dred) {
+                                            int* s_last, DFloat* dred, bool local_counts = false) {
     constexpr int WARPS = THREADS / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __syncthreads();
     unsigned e = 0;
     if (tid == 0) {
+        if (local_counts) {
+            if (n_valid) atomicAdd(&p.ws->nvalid, static_cast<unsigned>(n_valid));
+            if (n_bad) atomicAdd(&p.ws->nbad, static_cast<unsigned>(n_bad));
+        }
         if (aborted) atomicOr(&p.ws->err, static_cast<unsigned>(FOAK_ERRBIT_TIMEOUT));
         __threadfence();
         const unsigned t = atomicAdd(&p.ws->done, 1u);
@@ -239,6 +245,10 @@ __device__ __forceinline__ void rows_finish(const CeRowParams& p, bool aborted, 
             // now, its atomics' latency hidden under the sum.
             __threadfence();
             e = atomicExch(&p.ws->err, 0u);
+            if (local_counts) {
+                n_valid = static_cast<int>(atomicExch(&p.ws->nvalid, 0u));
+                n_bad = static_cast<int>(atomicExch(&p.ws->nbad, 0u));
+            }
             atomicExch(&p.ws->next, 0u);
             atomicExch(&p.ws->done, 0u);
         }
