@@ -66,6 +66,7 @@ SIGNATURES = {
     "foak_ce_fwd_bwd_noalloc": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
                                        _vp]),
     "foak_gemm_bf16": (_i32, [_vp, _i64, _i32, _vp, _i64, _i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _vp]),
+    "foak_gemm_bf16_group": (_i32, [_vp, _i32, _vp, _vp]),
     "foak_linear_ce_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
     "foak_linear_ce_chunked": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _sz, _vp]),
@@ -364,6 +365,46 @@ def foak_gemm_bf16(a, b, out, *, a_mn_major: bool = False, b_mn_major: bool = Fa
                             _ptr(out), out.stride(0), int(mode), _ptr(err), _stream(out.device, stream))
     _check(st, "foak_gemm_bf16")
     return out
+
+
+class _GemmProblem(ctypes.Structure):
+    """foak_gemm_problem of the C header."""
+    _fields_ = [("a", ctypes.c_void_p), ("lda", ctypes.c_int64), ("a_mn_major", ctypes.c_int32),
+                ("b", ctypes.c_void_p), ("ldb", ctypes.c_int64), ("b_mn_major", ctypes.c_int32),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("out", ctypes.c_void_p), ("ldo", ctypes.c_int64), ("out_mode", ctypes.c_int32)]
+
+
+FOAK_GEMM_GROUP_MAX = 3
+
+
+def foak_gemm_bf16_group(problems, *, err=None, stream=None):
+    """Several independent products out (+)= A @ B^T in one persistent launch.
+
+    problems: sequence of dicts with keys a, b, out and optionally a_mn_major, b_mn_major,
+    mode, M, N, K -- each as for foak_gemm_bf16.  No product may write what another reads.
+    """
+    if len(problems) > FOAK_GEMM_GROUP_MAX:
+        raise ValueError(f"at most {FOAK_GEMM_GROUP_MAX} products")
+    arr = (_GemmProblem * max(1, len(problems)))()
+    dev = None
+    for i, q in enumerate(problems):
+        a, b, out = q["a"], q["b"], q["out"]
+        for t in (a, b, out):
+            if t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda:
+                raise ValueError("operands must be 2-D CUDA tensors with unit column stride")
+        if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+            raise TypeError("a and b must be bfloat16")
+        amn, bmn = bool(q.get("a_mn_major", False)), bool(q.get("b_mn_major", False))
+        M = q.get("M", a.shape[1] if amn else a.shape[0])
+        K = q.get("K", a.shape[0] if amn else a.shape[1])
+        N = q.get("N", b.shape[1] if bmn else b.shape[0])
+        arr[i] = _GemmProblem(_ptr(a), a.stride(0), int(amn), _ptr(b), b.stride(0), int(bmn), M, N, K, _ptr(out),
+                              out.stride(0), int(q.get("mode", FOAK_GEMM_BF16)))
+        dev = out.device
+    st = lib.foak_gemm_bf16_group(ctypes.cast(arr, ctypes.c_void_p), len(problems), _ptr(err),
+                                  _stream(dev, stream) if dev is not None else None)
+    _check(st, "foak_gemm_bf16_group")
 
 
 def foak_linear_ce_workspace_size(N: int, V: int, D: int, chunk: int) -> int:

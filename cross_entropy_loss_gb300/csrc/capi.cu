@@ -202,6 +202,47 @@ NormLinWs norm_lin_layout(void* base, int64_t N, int64_t V, int64_t D, int64_t c
     return w;
 }
 
+// Argument checks of one product (foak_gemm_bf16 / foak_gemm_bf16_group).
+foak_status check_gemm(const foak_gemm_problem& q) {
+    if (q.M < 0 || q.N < 0 || q.K < 0 || q.M > 0x7fffffffLL || q.N > 0x7fffffffLL || q.K > 0x7fffffffLL)
+        return FOAK_ERR_INVALID_ARG;
+    if (q.out_mode != FOAK_GEMM_BF16 && q.out_mode != FOAK_GEMM_F32 && q.out_mode != FOAK_GEMM_F32_ACC)
+        return FOAK_ERR_INVALID_ARG;
+    if (q.M == 0 || q.N == 0) return FOAK_OK;
+    const int oes = q.out_mode == FOAK_GEMM_BF16 ? 2 : 4;
+    if (!q.a || !q.b || !q.out || !aligned(q.a, 16) || !aligned(q.b, 16) || !aligned(q.out, 16))
+        return FOAK_ERR_INVALID_ARG;
+    if ((q.lda * 2) % 16 || (q.ldb * 2) % 16 || (q.ldo * oes) % 16 || q.ldo < q.N) return FOAK_ERR_INVALID_ARG;
+    if (q.lda < (q.a_mn_major ? q.M : q.K) || q.ldb < (q.b_mn_major ? q.N : q.K)) return FOAK_ERR_INVALID_ARG;
+    return FOAK_OK;
+}
+
+// An empty contraction: C = 0 (or unchanged when accumulating).
+cudaError_t gemm_empty_k(const foak_gemm_problem& q, cudaStream_t s) {
+    if (q.M == 0 || q.N == 0 || q.out_mode == FOAK_GEMM_F32_ACC) return cudaSuccess;
+    const int oes = q.out_mode == FOAK_GEMM_BF16 ? 2 : 4;
+    return cudaMemset2DAsync(q.out, static_cast<size_t>(q.ldo) * oes, 0, static_cast<size_t>(q.N) * oes,
+                             static_cast<size_t>(q.M), s);
+}
+
+GemmDesc gemm_desc(const foak_gemm_problem& q, int32_t* err) {
+    GemmDesc d = {};
+    d.a = q.a;
+    d.lda = q.lda;
+    d.a_mn_major = q.a_mn_major != 0;
+    d.b = q.b;
+    d.ldb = q.ldb;
+    d.b_mn_major = q.b_mn_major != 0;
+    d.M = static_cast<int>(q.M);
+    d.N = static_cast<int>(q.N);
+    d.K = static_cast<int>(q.K);
+    d.out = q.out;
+    d.ldo = q.ldo;
+    d.mode = static_cast<GemmOut>(q.out_mode);
+    d.err = err;
+    return d;
+}
+
 }  // namespace
 }  // namespace foak
 
@@ -445,42 +486,39 @@ foak_status foak_rope_apply_qk(void* Q, int64_t Hq, int64_t ldq, void* K, int64_
     return finish(e, err, s);
 }
 
-foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const void* b, int64_t ldb,
-                           int32_t b_mn_major, int64_t M, int64_t N, int64_t K, void* out, int64_t ldo,
-                           int32_t out_mode, int32_t* err, void* stream) {
-    if (M < 0 || N < 0 || K < 0 || M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL)
-        return FOAK_ERR_INVALID_ARG;
-    if (out_mode != FOAK_GEMM_BF16 && out_mode != FOAK_GEMM_F32 && out_mode != FOAK_GEMM_F32_ACC)
-        return FOAK_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return FOAK_OK;
-    const int oes = out_mode == FOAK_GEMM_BF16 ? 2 : 4;
-    if (!a || !b || !out || !aligned(a, 16) || !aligned(b, 16) || !aligned(out, 16)) return FOAK_ERR_INVALID_ARG;
-    if ((lda * 2) % 16 || (ldb * 2) % 16 || (ldo * oes) % 16 || ldo < N) return FOAK_ERR_INVALID_ARG;
-    if (lda < (a_mn_major ? M : K) || ldb < (b_mn_major ? N : K)) return FOAK_ERR_INVALID_ARG;
+foak_status foak_gemm_bf16_group(const foak_gemm_problem* problems, int32_t n, int32_t* err, void* stream) {
+    if (n < 0 || n > FOAK_GEMM_GROUP_MAX || (n > 0 && !problems)) return FOAK_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i) {
+        const foak_status st = check_gemm(problems[i]);
+        if (st != FOAK_OK) return st;
+    }
     if (err && !aligned(err, 4)) return FOAK_ERR_INVALID_ARG;
     if (take_injected_failure()) return FOAK_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) {  // empty contraction: C = 0 (or unchanged when accumulating)
-        if (out_mode == FOAK_GEMM_F32_ACC) return FOAK_OK;
-        cudaError_t e = cudaMemset2DAsync(out, static_cast<size_t>(ldo) * oes, 0, static_cast<size_t>(N) * oes,
-                                          static_cast<size_t>(M), s);
-        return finish(e, nullptr, s);
+    GemmDesc d[FOAK_GEMM_GROUP_MAX];
+    int nd = 0;
+    cudaError_t e = cudaSuccess;
+    for (int32_t i = 0; i < n && e == cudaSuccess; ++i) {
+        const foak_gemm_problem& q = problems[i];
+        if (q.M == 0 || q.N == 0) continue;
+        if (q.K == 0) e = gemm_empty_k(q, s);
+        else d[nd++] = gemm_desc(q, err);
     }
-    GemmDesc d = {};
-    d.a = a;
-    d.lda = lda;
-    d.a_mn_major = a_mn_major != 0;
-    d.b = b;
-    d.ldb = ldb;
-    d.b_mn_major = b_mn_major != 0;
-    d.M = static_cast<int>(M);
-    d.N = static_cast<int>(N);
-    d.K = static_cast<int>(K);
-    d.out = out;
-    d.ldo = ldo;
-    d.mode = static_cast<GemmOut>(out_mode);
-    d.err = err;
-    return finish(launch_gemm_bf16(d, s), err, s);
+    if (e == cudaSuccess) e = launch_gemm_bf16_group(d, nd, s);
+    return finish(e, err, s);
+}
+
+foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const void* b, int64_t ldb,
+                           int32_t b_mn_major, int64_t M, int64_t N, int64_t K, void* out, int64_t ldo,
+                           int32_t out_mode, int32_t* err, void* stream) {
+    const foak_gemm_problem q = {a, lda, a_mn_major, b, ldb, b_mn_major, M, N, K, out, ldo, out_mode};
+    const foak_status st = check_gemm(q);
+    if (st != FOAK_OK || M == 0 || N == 0) return st;
+    if (err && !aligned(err, 4)) return FOAK_ERR_INVALID_ARG;
+    if (take_injected_failure()) return FOAK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return finish(gemm_empty_k(q, s), nullptr, s);
+    return finish(launch_gemm_bf16(gemm_desc(q, err), s), err, s);
 }
 
 size_t foak_ce_host_workspace_size(int64_t N) { return N < 0 ? 0 : host_ws_bytes(N); }

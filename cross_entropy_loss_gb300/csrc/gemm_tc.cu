@@ -36,7 +36,10 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <map>
 #include <mutex>
+#include <type_traits>
+#include <vector>
 
 #include "foak_ce.h"
 #include "gemm_tc.h"
@@ -82,6 +85,20 @@ struct GemmParams {
     float* zlab;
 };
 static_assert(kBN == kGemmTileN, "statistics tiles are the output tiles");
+
+// Several independent products in one launch of the pair kernel: cluster c takes the
+// (problem, unit) entries ent[start[c] .. start[c + 1]) in that order, a list the host
+// balances by estimated cost (k-blocks plus the epilogue), longest units first.
+constexpr int kGroupMax = 3;
+constexpr int kGroupMaxClusters = 128;
+constexpr int kGroupMaxUnits = 8192;
+constexpr int kGroupUnitBits = 14;  // entry = (problem << 14) | unit
+struct GemmGroup {
+    GemmParams prob[kGroupMax];
+    int nprob;
+    uint16_t start[kGroupMaxClusters + 1];
+    uint16_t ent[kGroupMaxUnits];
+};
 
 // Output units walked along the shorter dimension first.
 __device__ __forceinline__ int unit_m(const GemmParams& p, int t) { return p.n_fast ? t / p.tiles_n : t % p.units_m; }
@@ -321,7 +338,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
 // them), its MMA thread commits each stage to both CTAs' empty barriers and each
 // accumulator to both CTAs' acc_full barriers (one commit each, no multicast), and
 // both CTAs' epilogue warps arrive on the even CTA's acc_empty barriers.
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_pair_kernel(const __grid_constant__ GemmParams p) {
+// GROUPED: the kernel's argument is a GemmGroup and each cluster walks its entries;
+// otherwise one GemmParams whose units the clusters take round-robin.
+template <bool GROUPED>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_tc_pair_kernel(const __grid_constant__ typename std::conditional<GROUPED, GemmGroup, GemmParams>::type g) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t full[kStages2], empty[kStages2], acc_full[2], acc_empty[2];
@@ -331,8 +352,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_pair_kernel(cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const bool lead = rank == 0;
-    const int unit0 = static_cast<int>(blockIdx.x >> 1);
-    const int unit_step = static_cast<int>(gridDim.x >> 1);
+    const int cl = static_cast<int>(blockIdx.x >> 1);
+    const int ncl = static_cast<int>(gridDim.x >> 1);
+    // this cluster's units: how many, and the i-th one's problem and unit index
+    int n_my;
+    if constexpr (GROUPED) {
+        n_my = g.start[cl + 1] - g.start[cl];
+    } else {
+        const int units = g.units_m * g.tiles_n;
+        n_my = cl < units ? (units - 1 - cl) / ncl + 1 : 0;
+    }
+    auto unit_at = [&](int i, int& t) -> const GemmParams& {
+        if constexpr (GROUPED) {
+            const unsigned e = g.ent[g.start[cl] + i];
+            t = static_cast<int>(e & ((1u << kGroupUnitBits) - 1u));
+            return g.prob[e >> kGroupUnitBits];
+        } else {
+            t = cl + i * ncl;
+            return g;
+        }
+    };
+    int32_t* err_word;
+    if constexpr (GROUPED) err_word = g.prob[0].err;
+    else err_word = g.err;
     if (tid == 0) {
         for (int s = 0; s < kStages2; ++s) {
             mbar_init(&full[s], 1);
@@ -344,8 +386,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_pair_kernel(cons
         }
         fence_mbar_init();
         abort_sh = 0;
-        prefetch_tensormap(&p.tmA);
-        prefetch_tensormap(&p.tmB);
+        if constexpr (GROUPED) {
+            for (int q = 0; q < g.nprob; ++q) {
+                prefetch_tensormap(&g.prob[q].tmA);
+                prefetch_tensormap(&g.prob[q].tmB);
+            }
+        } else {
+            prefetch_tensormap(&g.tmA);
+            prefetch_tensormap(&g.tmB);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(&tmem_base_sh, kTmemCols);
@@ -356,19 +405,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_pair_kernel(cons
     cluster_sync();  // both CTAs' barriers and TMEM exist before any copy, commit or remote arrive
     tc_fence_after();
     const uint32_t tbase = tmem_base_sh;
-    const int num_units = p.units_m * p.tiles_n;
-    const int nk = (p.K + kBK - 1) / kBK;
 
     auto give_up = [&]() {
         abort_sh = 1;
-        if (p.err) atomicOr(p.err, FOAK_ERRBIT_TIMEOUT);
+        if (err_word) atomicOr(err_word, FOAK_ERRBIT_TIMEOUT);
     };
 
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = unit0; t < num_units && !abort_sh; t += unit_step) {
+            for (int i = 0; i < n_my && !abort_sh; ++i) {
+                int t;
+                const GemmParams& p = unit_at(i, t);
+                const int nk = (p.K + kBK - 1) / kBK;
                 const int m0 = unit_m(p, t) * (2 * kBM) + static_cast<int>(rank) * kBM;
                 const int nb0 = unit_n(p, t) * kBN + static_cast<int>(rank) * (kBN / 2);
                 for (int kb = 0; kb < nk; ++kb) {
@@ -402,7 +452,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_pair_kernel(cons
         if (lane == 0 && lead) {
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            for (int t = unit0; t < num_units && !abort_sh; t += unit_step) {
+            for (int i = 0; i < n_my && !abort_sh; ++i) {
+                int t;
+                const GemmParams& p = unit_at(i, t);
+                const int nk = (p.K + kBK - 1) / kBK;
                 if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u)) { give_up(); break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tbase + static_cast<uint32_t>(acc * kBN);
@@ -437,7 +490,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_pair_kernel(cons
         uint32_t acc_phase = 0;
         const uint32_t lead_acc_empty0 = mapa_u32(&acc_empty[0], 0);
         const uint32_t lead_acc_empty1 = mapa_u32(&acc_empty[1], 0);
-        for (int t = unit0; t < num_units; t += unit_step) {
+        for (int i = 0; i < n_my; ++i) {
+            int t;
+            const GemmParams& p = unit_at(i, t);
             const bool ok = !abort_sh && mbar_wait_bounded(&acc_full[acc], acc_phase);
             if (!ok) {
                 if (lane == 0) give_up();
@@ -518,12 +573,14 @@ bool g_gemm_attr[64] = {false};
 
 }  // namespace
 
-cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
-    if (d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaSuccess;
-    GemmParams p = {};
+namespace {
+
+// Kernel parameters of one product; pair = CTA pairs on 256-row units (M has at least two
+// 128-row tiles).  False when a tensor map cannot be encoded or the description is invalid.
+bool make_params(const GemmDesc& d, GemmParams& p, bool& pair) {
+    p = GemmParams{};
     const int tiles_m = (d.M + kBM - 1) / kBM;
-    // CTA pairs whenever M has at least two 128-row tiles
-    const bool pair = tiles_m >= 2;
+    pair = tiles_m >= 2;
     // K-major [rows][K]: inner K, boxes of 64 x (the CTA's rows); MN-major [K][rows]: inner rows, 64 x 64 boxes.
     bool ok = d.a_mn_major ? encode_bf16(&p.tmA, d.a, static_cast<uint64_t>(d.M), static_cast<uint64_t>(d.K), d.lda, 64)
                            : encode_bf16(&p.tmA, d.a, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.M), d.lda, kBM);
@@ -533,7 +590,7 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
                                   pair ? kBN / 2 : kBN));
     if (ok && (d.mode == kGemmOutF32 || d.mode == kGemmOutF32Acc))
         ok = encode_f32_out(&p.tmC, d.out, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.M), d.ldo);
-    if (!ok) return cudaErrorInvalidValue;
+    if (!ok) return false;
     p.M = d.M;
     p.N = d.N;
     p.K = d.K;
@@ -551,54 +608,181 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     p.stats = d.stats;
     p.stats_ld = d.stats_ld;
     p.zlab = d.zlab;
-    if (d.mode == kGemmOutBf16Stats && (!d.labels || !d.stats || !d.zlab || d.stats_ld < p.tiles_n))
-        return cudaErrorInvalidValue;
+    return !(d.mode == kGemmOutBf16Stats && (!d.labels || !d.stats || !d.zlab || d.stats_ld < p.tiles_n));
+}
+
+int g_max_pairs[64] = {0};
+
+// Kernel attributes once per device, and the number of CTA pairs resident at once.
+cudaError_t gemm_setup(int* max_pairs) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    static int max_pairs[64] = {0};
-    {
-        std::lock_guard<std::mutex> lock(g_gemm_mu);
-        if (!g_gemm_attr[dev]) {
-            e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kGemmSmem1));
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(gemm_bf16_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmem2));
-            if (e != cudaSuccess) return e;
-            g_gemm_attr[dev] = true;
-        }
+    std::lock_guard<std::mutex> lock(g_gemm_mu);
+    if (!g_gemm_attr[dev]) {
+        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGemmSmem1));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_bf16_tc_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kGemmSmem2));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_bf16_tc_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kGemmSmem2));
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kGemmThreads, 1, 1);
+        cfg.dynamicSmemBytes = kGemmSmem2;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_pair_kernel<false>, &cfg);
+        if (e != cudaSuccess) return e;
+        g_max_pairs[dev] = std::max(1, n);
+        g_gemm_attr[dev] = true;
     }
-    const int units = p.units_m * p.tiles_n;
-    if (!pair) {
-        const int grid = std::min(units, device_sm_count());
-        gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem1, stream>>>(p);
-        return cudaGetLastError();
-    }
+    *max_pairs = g_max_pairs[dev];
+    return cudaSuccess;
+}
+
+template <typename Arg>
+cudaError_t launch_pair(const Arg& arg, int clusters, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = kGemmSmem2;
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    {
-        std::lock_guard<std::mutex> lock(g_gemm_mu);
-        if (max_pairs[dev] == 0) {
-            cfg.gridDim = dim3(2, 1, 1);
-            int n = 0;
-            e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_pair_kernel, &cfg);
-            if (e != cudaSuccess) return e;
-            max_pairs[dev] = std::max(1, n);
-        }
+    if constexpr (std::is_same<Arg, GemmGroup>::value)
+        return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_pair_kernel<true>, arg);
+    else
+        return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_pair_kernel<false>, arg);
+}
+
+// Estimated cost of one unit in k-blocks: its main loop plus about 8 k-blocks of
+// epilogue not hidden behind the next unit (from the measured per-unit times of the
+// chunked products: 500 k-blocks 195 us, 64 k-blocks + statistics 28 us, 32 k-blocks +
+// fp32 reduce-add 15 us on one pair).
+int unit_cost(const GemmParams& p) { return (p.K + kBK - 1) / kBK + 8; }
+
+struct Schedule {
+    int clusters;
+    std::vector<uint16_t> start, ent;
+};
+
+// Longest units first, each to the cluster with the least estimated work so far (ties:
+// the lowest cluster); units of one problem keep their walk order, so clusters working
+// at the same time share operand tiles as in a single product.
+Schedule build_schedule(const GemmParams* ps, int n, int max_pairs) {
+    struct U {
+        int cost, prob, t;
+    };
+    std::vector<U> us;
+    for (int q = 0; q < n; ++q)
+        for (int t = 0; t < ps[q].units_m * ps[q].tiles_n; ++t) us.push_back({unit_cost(ps[q]), q, t});
+    std::stable_sort(us.begin(), us.end(), [](const U& a, const U& b) { return a.cost > b.cost; });
+    Schedule s;
+    s.clusters = std::max(1, std::min(std::min(max_pairs, kGroupMaxClusters), static_cast<int>(us.size())));
+    std::vector<int64_t> load(static_cast<size_t>(s.clusters), 0);
+    std::vector<std::vector<uint16_t>> lists(static_cast<size_t>(s.clusters));
+    for (const U& u : us) {
+        int best = 0;
+        for (int c = 1; c < s.clusters; ++c)
+            if (load[static_cast<size_t>(c)] < load[static_cast<size_t>(best)]) best = c;
+        load[static_cast<size_t>(best)] += u.cost;
+        lists[static_cast<size_t>(best)].push_back(static_cast<uint16_t>((u.prob << kGroupUnitBits) | u.t));
     }
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(units, max_pairs[dev])), 1, 1);
-    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_pair_kernel, p);
+    s.start.push_back(0);
+    for (const auto& l : lists) {
+        s.ent.insert(s.ent.end(), l.begin(), l.end());
+        s.start.push_back(static_cast<uint16_t>(s.ent.size()));
+    }
+    return s;
+}
+
+std::mutex g_sched_mu;
+std::map<std::vector<int>, Schedule> g_sched;  // by (pairs, per problem: K, mode, units_m, tiles_n)
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
+    if (d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaSuccess;
+    GemmParams p;
+    bool pair = false;
+    if (!make_params(d, p, pair)) return cudaErrorInvalidValue;
+    int max_pairs = 0;
+    cudaError_t e = gemm_setup(&max_pairs);
+    if (e != cudaSuccess) return e;
+    const int units = p.units_m * p.tiles_n;
+    if (!pair) {
+        const int grid = std::min(units, device_sm_count());
+        gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem1, stream>>>(p);
+        return cudaGetLastError();
+    }
+    return launch_pair(p, std::min(units, max_pairs), stream);
+}
+
+cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream) {
+    // the non-empty products
+    const GemmDesc* live[kGroupMax];
+    int nl = 0;
+    for (int i = 0; i < n; ++i) {
+        if (d[i].M <= 0 || d[i].N <= 0 || d[i].K <= 0) continue;
+        if (nl == kGroupMax) return cudaErrorInvalidValue;
+        live[nl++] = &d[i];
+    }
+    if (nl == 0) return cudaSuccess;
+    // the grouped kernel arguments (about 18 KB: kept off the stack of the caller's thread)
+    thread_local GemmGroup grp;
+    int total = 0;
+    bool all_pair = true, small = true;
+    for (int q = 0; q < nl; ++q) {
+        bool pair = false;
+        if (!make_params(*live[q], grp.prob[q], pair)) return cudaErrorInvalidValue;
+        const int u = grp.prob[q].units_m * grp.prob[q].tiles_n;
+        all_pair = all_pair && pair;
+        small = small && u < (1 << kGroupUnitBits);
+        total += u;
+    }
+    // one product, a product of single-CTA tiles, or too many units: separate launches, in order
+    if (nl == 1 || !all_pair || !small || total > kGroupMaxUnits) {
+        for (int q = 0; q < nl; ++q) {
+            const cudaError_t e = launch_gemm_bf16(*live[q], stream);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    int max_pairs = 0;
+    cudaError_t e = gemm_setup(&max_pairs);
+    if (e != cudaSuccess) return e;
+    std::vector<int> key = {max_pairs, nl};
+    for (int q = 0; q < nl; ++q) {
+        const GemmParams& p = grp.prob[q];
+        key.insert(key.end(), {p.K, p.mode, p.units_m, p.tiles_n});
+    }
+    const Schedule* s = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_sched_mu);
+        auto it = g_sched.find(key);
+        if (it == g_sched.end()) it = g_sched.emplace(key, build_schedule(grp.prob, nl, max_pairs)).first;
+        s = &it->second;
+    }
+    grp.nprob = nl;
+    std::copy(s->start.begin(), s->start.end(), grp.start);
+    std::copy(s->ent.begin(), s->ent.end(), grp.ent);
+    return launch_pair(grp, s->clusters, stream);
 }
 
 }  // namespace foak

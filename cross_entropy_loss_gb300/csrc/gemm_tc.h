@@ -44,4 +44,11 @@ constexpr int kGemmTileN = 256;
 
 cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream);
 
+// Up to three independent products in one persistent launch of the CTA-pair kernel
+// (every product with M > 128): the clusters take a list of (product, output unit)
+// entries balanced by estimated cost, longest first.  No product may write what another
+// reads.  Other cases are launched one product after another, in order.  The error word
+// of the first product receives every timeout.
+cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream);
+
 }  // namespace foak

@@ -19,7 +19,10 @@
 //                              kDeferChunks chunks (stored by the first group,
 //                              added by TMA reduce for the others)
 // and finally one CTA sums the per-row loss terms of all N rows (double-float, a
-// fixed order) over the denominator.  Only one group's Z lives at a time.  Steps 1-2
+// fixed order) over the denominator.  Step 4 of a chunk runs in one launch with step
+// 1 of the next (two independent products on one persistent grid, see
+// launch_gemm_bf16_group): dH's 4 x 16 output units of 256 x 256 would leave 12 of the
+// 76 SM pairs idle for its whole run.  Only one group's Z lives at a time.  Steps 1-2
 // are the GEMM-1 epilogue statistics of the chunked loss; the softmax itself is
 // rebuilt from Z and lse by step 3 rather than inside the producers of steps 4-5,
 // whose operands would then each need an exponential at the tensor cores' rate.
@@ -167,6 +170,10 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
     const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
     __nv_bfloat16* dHb = static_cast<__nv_bfloat16*>(dH);
     __nv_bfloat16* zbuf = static_cast<__nv_bfloat16*>(ws.z);
+    // dH of a chunk goes out with the next chunk's Z in one launch (the 64 units of dH
+    // alone leave 12 of the 76 SM pairs idle), and the last one with the last dW
+    GemmDesc pend_dh = {};
+    bool have_dh = false;
     for (int64_t c = 0; c < nchunks; ++c) {
         const int64_t r0 = c * chunk;
         const int rows = static_cast<int>(std::min(chunk, N - r0));
@@ -191,8 +198,11 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
         g1.stats = ws.stats;
         g1.stats_ld = tiles;
         g1.zlab = ws.zlab;
-        e = launch_gemm_bf16(g1, stream);
-        if (e != cudaSuccess) return e;
+        {
+            const GemmDesc grp[2] = {g1, pend_dh};  // Z(c) writes the other Z slot than dH(c-1) reads
+            e = launch_gemm_bf16_group(grp, have_dh ? 2 : 1, stream);
+            if (e != cudaSuccess) return e;
+        }
         // 2. lse and row terms of the chunk's rows (into the batch's row_loss)
         chunk_lse_kernel<<<(rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32), kMergeThreads, 0, stream>>>(
             ws.stats, tiles, ws.zlab, labels + r0, rows, V, ignore_index, ws.lse, ws.row_loss + r0);
@@ -202,8 +212,9 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
         e = launch_ce_backward(2, z, z, ldz, labels + r0, rows, V, ignore_index, ws.lse, nullptr, denom,
                                ws.chunk_err + c, stream, g, denom_dev);
         if (e != cudaSuccess) return e;
-        // 4. dH_c = dZ W     (W is [V][D]: MN-major as the [K][N] operand)
-        GemmDesc g2 = {};
+        // 4. dH_c = dZ W     (W is [V][D]: MN-major as the [K][N] operand), launched later
+        GemmDesc& g2 = pend_dh;
+        g2 = GemmDesc{};
         g2.a = z;
         g2.lda = ldz;
         g2.a_mn_major = false;
@@ -217,8 +228,7 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
         g2.ldo = D;
         g2.mode = kGemmOutBf16;
         g2.err = gemm_err;
-        e = launch_gemm_bf16(g2, stream);
-        if (e != cudaSuccess) return e;
+        have_dh = true;
         // 5. once the group is complete: dW (+)= dZ_g^T H_g over the group's rows
         //    (dZ_g is [rows_g][V] = [K][M], H_g is [rows_g][D] = [K][N])
         if (slot == kDeferChunks - 1 || c == nchunks - 1) {
@@ -238,7 +248,13 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
             g3.ldo = D;
             g3.mode = g0 == 0 ? kGemmOutF32 : kGemmOutF32Acc;
             g3.err = gemm_err;
-            e = launch_gemm_bf16(g3, stream);
+            if (c == nchunks - 1) {
+                const GemmDesc fin[2] = {pend_dh, g3};
+                e = launch_gemm_bf16_group(fin, 2, stream);
+                have_dh = false;
+            } else {
+                e = launch_gemm_bf16(g3, stream);
+            }
             if (e != cudaSuccess) return e;
         }
     }

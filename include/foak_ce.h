@@ -389,6 +389,36 @@ foak_status foak_gemm_bf16(const void* a, int64_t lda, int32_t a_mn_major, const
                            int32_t out_mode, int32_t* err, void* stream);
 
 /*
+ * Up to FOAK_GEMM_GROUP_MAX independent products of foak_gemm_bf16's form in one
+ * persistent launch: the SM pairs take a list of (product, 256 x 256 output unit)
+ * entries balanced by estimated cost, longest units first, so a product with fewer
+ * units than the GPU has SM pairs (dH of the chunked call: 4 x 16 units on 76 pairs)
+ * shares the machine with another instead of leaving pairs idle.  This is how the
+ * chunked call issues its dH products (with the next chunk's logits product).
+ *   problems (host)   n descriptors, fields and rules as for foak_gemm_bf16; read
+ *                     before the call returns.  No product may write memory that
+ *                     another one reads or writes.
+ *   n                 0 .. FOAK_GEMM_GROUP_MAX
+ *   err (device)      as for foak_gemm_bf16, shared by the products
+ * Products with M <= 128 (single-CTA tiles), or more than 8192 output units in all,
+ * are launched one after another in the order given, with the same results.
+ */
+#define FOAK_GEMM_GROUP_MAX 3
+typedef struct foak_gemm_problem {
+    const void* a;
+    int64_t lda;
+    int32_t a_mn_major;
+    const void* b;
+    int64_t ldb;
+    int32_t b_mn_major;
+    int64_t M, N, K;
+    void* out;
+    int64_t ldo;
+    int32_t out_mode;
+} foak_gemm_problem;
+foak_status foak_gemm_bf16_group(const foak_gemm_problem* problems, int32_t n, int32_t* err, void* stream);
+
+/*
  * Largest N that foak_ce_fwd_bwd_noalloc accepts (its fixed scratch holds one
  * float per row: 1 MiB plus a 256-byte header on every device that loads the
  * library, kept until the process exits).

@@ -204,3 +204,31 @@ def test_rope_entries_argument_errors(so):
         L.foak_rope_apply_qk(Q, 2, 256, K, 1, ldk, 1, 4, 128, FAKE, FAKE, 16, 0, None, None))
     assert qk(K=None) == E.FOAK_ERR_INVALID_ARG
     assert qk(ldk=64) == E.FOAK_ERR_INVALID_ARG
+
+
+def test_gemm_group_argument_errors(so):
+    """foak_gemm_bf16_group rejects a bad count or a bad product before any launch; an
+    empty group (or only empty products) is a no-op."""
+    E = so
+    L = so.lib
+
+    def prob(**kw):
+        f = dict(a=FAKE, lda=64, a_mn_major=0, b=FAKE, ldb=64, b_mn_major=0, M=256, N=256, K=64, out=FAKE, ldo=256,
+                 out_mode=E.FOAK_GEMM_BF16)
+        f.update(kw)
+        return E._GemmProblem(**f)
+
+    def group(*ps, n=None):
+        arr = (E._GemmProblem * max(1, len(ps)))(*ps)
+        return L.foak_gemm_bf16_group(ctypes.cast(arr, ctypes.c_void_p), len(ps) if n is None else n, None, None)
+
+    assert group(n=-1) == E.FOAK_ERR_INVALID_ARG
+    assert group(prob(), prob(), prob(), prob()) == E.FOAK_ERR_INVALID_ARG  # more than FOAK_GEMM_GROUP_MAX
+    assert L.foak_gemm_bf16_group(None, 1, None, None) == E.FOAK_ERR_INVALID_ARG
+    assert group(prob(), prob(out_mode=7)) == E.FOAK_ERR_INVALID_ARG
+    assert group(prob(lda=32)) == E.FOAK_ERR_INVALID_ARG                   # lda < K
+    assert group(prob(), prob(a=FAKE + 8)) == E.FOAK_ERR_INVALID_ARG       # 16-byte alignment
+    assert group(prob(ldo=100)) == E.FOAK_ERR_INVALID_ARG                  # ldo < N
+    assert group(prob(K=-1)) == E.FOAK_ERR_INVALID_ARG
+    assert group(n=0) == E.FOAK_OK
+    assert group(prob(M=0), prob(N=0, ldo=0)) == E.FOAK_OK
