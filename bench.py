@@ -625,20 +625,27 @@ def chunked_timing(ce, torch, dev, stream, steps=10, warmup=3):
                 "ms_per_step": ms_r, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm, "peak_source": hsrc,
                 "bytes": "Q and K read and written once, positions; the 4 MB cos/sin table stays in L2"})
     del q, k, cache
-    # the three products of the call, alone, at the shapes it runs them (dW once per pair of chunks)
+    # the products of the call at the shapes it runs them: a chunk's logits product and the
+    # previous chunk's dH, alone and in the one grouped launch the call makes of them, and dW
+    # once per group of four chunks
+    G = 4
     Z = torch.empty(chunk, V, dtype=torch.bfloat16, device=dev)
-    Zs = torch.randn(2 * chunk, V, device=dev).to(torch.bfloat16)
+    Zs = torch.randn(G * chunk, V, device=dev).to(torch.bfloat16)
     Hc = H[:chunk]
-    Hp = H[:2 * chunk]
+    Hg = H[:G * chunk]
     dHc = torch.empty(chunk, D, dtype=torch.bfloat16, device=dev)
     shapes = [
         ("Z = H_c W^T (M=1024, N=32000, K=4096, K/K-major)", chunk,
          lambda: ce.foak_gemm_bf16(Hc, W, Z, mode=ce.FOAK_GEMM_BF16)),
         ("dH_c = dZ W (M=1024, N=4096, K=32000, K/MN-major)", chunk,
          lambda: ce.foak_gemm_bf16(Zs[:chunk], W, dHc, b_mn_major=True, mode=ce.FOAK_GEMM_BF16)),
-        ("dW += dZ_pair^T H_pair (M=32000, N=4096, K=2048, MN/MN-major, fp32 TMA reduce-add of the 524 MB dW)",
-         2 * chunk,
-         lambda: ce.foak_gemm_bf16(Zs, Hp, dW, a_mn_major=True, b_mn_major=True, mode=ce.FOAK_GEMM_F32_ACC)),
+        ("Z(c) and dH(c-1) in one grouped launch (foak_gemm_bf16_group; the two shapes above)", 2 * chunk,
+         lambda: ce.foak_gemm_bf16_group([dict(a=Hc, b=W, out=Z, mode=ce.FOAK_GEMM_BF16),
+                                          dict(a=Zs[:chunk], b=W, out=dHc, b_mn_major=True,
+                                               mode=ce.FOAK_GEMM_BF16)])),
+        ("dW += dZ_g^T H_g (M=32000, N=4096, K=4096, MN/MN-major, fp32 TMA reduce-add of the 524 MB dW)",
+         G * chunk,
+         lambda: ce.foak_gemm_bf16(Zs, Hg, dW, a_mn_major=True, b_mn_major=True, mode=ce.FOAK_GEMM_F32_ACC)),
     ]
     for name, kk, fn in shapes:
         gms = timed(fn, 10, 3)
