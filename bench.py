@@ -233,9 +233,9 @@ def _stated_bytes(cfg):
 
 # ----------------------------------------------------------------------------- ours
 
-def _ring(torch, x_dev, count):
+def _ring(torch, x_dev, count, ring_max=None):
     size = x_dev.numel() * x_dev.element_size()
-    r = max(2, min(count, RING_BUDGET_BYTES // max(size, 1)))
+    r = max(2, min(count, RING_BUDGET_BYTES // max(size, 1), ring_max or count))
     bufs = [torch.empty_like(x_dev) for _ in range(r)]
     return bufs
 
@@ -265,13 +265,13 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def fused_timing(cfg, steps, warmup, record_clocks, use_dist=True, call=None):
+    def fused_timing(cfg, steps, warmup, record_clocks, use_dist=True, call=None, ring_max=None):
         call = call or ce.foak_ce_fwd_bwd
         x = upload(cfg["logits"], cfg["dtype"])
         y = torch.from_numpy(cfg["labels"]).to(dev)
         N = x.shape[0]
         ws = ce.workspace(N, dev)
-        bufs = _ring(torch, x, steps + warmup)
+        bufs = _ring(torch, x, steps + warmup, ring_max)
         _fill(bufs, x)
         del x
         for i in range(warmup):
@@ -481,8 +481,10 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
     peak, peak_src = _peak_hbm()
     for name in ("packed", "llama3", "llama3_f32"):
         cfg = _make(name)
-        k, w = 10, 3
-        ms, loss, err, _ = fused_timing(cfg, k, w, False, use_dist=False)
+        # enough calls that the first one's launch after the synchronise is amortised; every
+        # buffer is larger than L2, so eight of them in turn leave nothing cached between uses
+        k, w = 50, 3
+        ms, loss, err, reused = fused_timing(cfg, k, w, False, use_dist=False, ring_max=8)
         algo = _algo_bytes(cfg)
         gbs = algo / (ms * 1e-3) / 1e9
         out.append({"key": name, "workload_key": f"{name}: N={cfg['logits'].shape[0]} V={cfg['V']}",
@@ -490,7 +492,9 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
                     "steps": k, "ms_per_step": ms,
                     "tokens_per_s": cfg["logits"].shape[0] / (ms * 1e-3), "GBps_algorithmic": gbs,
                     "GBps_stated_2NVs": _stated_bytes(cfg) / (ms * 1e-3) / 1e9, "frac": gbs / peak,
-                    "peak": peak, "peak_source": peak_src, "loss": loss, "err": err})
+                    "peak": peak, "peak_source": peak_src, "loss": loss, "err": err,
+                    "l2": "distinct logits buffers in turn (8 at most), each larger than L2"
+                          + (" (reused)" if reused else "")})
         del cfg
     # separate forward and backward on the headline workload
     cfg = _make(args.workload)
@@ -498,8 +502,8 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
     y = torch.from_numpy(cfg["labels"]).to(dev)
     N = x.shape[0]
     ws = ce.workspace(N, dev)
-    k, w = 20, 3
-    bufs = _ring(torch, x, k + w)
+    k, w = 100, 3
+    bufs = _ring(torch, x, k + w, 16)  # 262 MB buffers in turn: none is in L2 when it comes back
     _fill(bufs, x)
     dl = [torch.empty_like(x) for _ in range(2)]
     for i in range(w):
