@@ -74,7 +74,7 @@ __device__ __forceinline__ float df_div(DFloat x, float d) {
 
 // Sum of v[0, n) over a CTA of THREADS threads, in a fixed order: thread t adds
 // v[t], v[t + THREADS], ... (eight loads in flight before their additions), then a
-// shuffle tree per warp and warp 0's partials in warp order.  `red` holds THREADS/32
+// shuffle tree per warp and the same tree over the warps' partials in warp 0.  `red` holds THREADS/32
 // values; the result is valid in thread 0.  Loads bypass L1 (the terms were written
 // by other CTAs of the same kernel).
 template <int THREADS>
@@ -98,10 +98,27 @@ __device__ __forceinline__ DFloat block_sum_terms(const float* v, int64_t n, DFl
     }
     if (lane == 0) red[warp] = acc;
     __syncthreads();
+    // the warp partials by warp 0: the same shuffle tree over lanes 0 .. THREADS/32 - 1
     DFloat tot{0.f, 0.f};
-    if (tid == 0)
-        for (int w = 0; w < THREADS / 32; ++w) tot = df_add(tot, red[w]);
+    if (warp == 0) {
+        static_assert(THREADS / 32 <= 32, "one partial per lane");
+        tot = lane < THREADS / 32 ? red[lane] : DFloat{0.f, 0.f};
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const DFloat o{__shfl_down_sync(0xffffffffu, tot.hi, off), __shfl_down_sync(0xffffffffu, tot.lo, off)};
+            tot = df_add(tot, o);
+        }
+    }
     return tot;
+}
+
+// Fetch-and-add with release and acquire semantics at GPU scope: earlier writes of this
+// thread (and those it has seen) are visible before the add, and later reads see what
+// the threads whose adds it follows had written.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 // ---------------------------------------------------------------- mbarrier

@@ -234,16 +234,17 @@ __device__ __forceinline__ void rows_finish(const CeRowParams& p, bool aborted, 
             if (n_bad) atomicAdd(&p.ws->nbad, static_cast<unsigned>(n_bad));
         }
         if (aborted) atomicOr(&p.ws->err, static_cast<unsigned>(FOAK_ERRBIT_TIMEOUT));
-        __threadfence();
-        const unsigned t = atomicAdd(&p.ws->done, 1u);
+        // The ticket releases this CTA's row terms, counts and error bits (the CTA
+        // barrier above puts its other threads' writes before it) and, for the last
+        // CTA, acquires everyone else's.
+        const unsigned t = atom_add_acq_rel_gpu(&p.ws->done, 1u);
         const bool last = t == gridDim.x - 1;
         *s_last = last;
         if (last) {
             // Every other CTA has published its row terms and error bits and made its
-            // last claim: this fence orders the reads below after theirs (the barrier
-            // extends it to the CTA's other threads), and the header is taken and reset
-            // now, its atomics' latency hidden under the sum.
-            __threadfence();
+            // last claim (the barrier below extends the acquire to the CTA's other
+            // threads); the header is taken and reset now, its atomics' latency hidden
+            // under the sum.
             e = atomicExch(&p.ws->err, 0u);
             if (local_counts) {
                 n_valid = static_cast<int>(atomicExch(&p.ws->nvalid, 0u));
