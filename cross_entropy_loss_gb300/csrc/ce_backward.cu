@@ -47,6 +47,8 @@ __device__ __forceinline__ void bwd_store_scalar(char* p, float v) {
 
 template <int ES>
 __global__ void __launch_bounds__(kBwdThreads) ce_backward_kernel(const CeBwdParams p) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     constexpr int EPV = 16 / ES;
     __shared__ int iscratch[2 * (kBwdThreads / 32)];
     const int tid = threadIdx.x;
@@ -179,11 +181,8 @@ cudaError_t launch_ce_backward(int elem_bytes, void* dx, const void* x, int64_t 
     const int64_t items = N * prm.nseg;
     const int64_t full = static_cast<int64_t>(device_sm_count()) * kBwdBlocksPerSm;
     const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(full, items)));
-    if (elem_bytes == 2)
-        ce_backward_kernel<2><<<grid, kBwdThreads, 0, stream>>>(prm);
-    else
-        ce_backward_kernel<4><<<grid, kBwdThreads, 0, stream>>>(prm);
-    return cudaGetLastError();
+    return elem_bytes == 2 ? launch_dependent(ce_backward_kernel<2>, dim3(grid), dim3(kBwdThreads), 0, stream, prm)
+                           : launch_dependent(ce_backward_kernel<4>, dim3(grid), dim3(kBwdThreads), 0, stream, prm);
 }
 
 }  // namespace foak

@@ -17,6 +17,8 @@ constexpr int kCountThreads = 1024;
 __global__ void __launch_bounds__(kCountThreads) ce_count_valid_kernel(const int64_t* __restrict__ labels, int64_t N,
                                                                        int64_t V, int64_t ignore_index,
                                                                        int64_t* n_valid, int32_t* err) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     __shared__ int scratch[2 * (kCountThreads / 32)];
     int nv = 0, nb = 0;
     count_labels(labels, N, V, ignore_index, scratch, nv, nb);
@@ -28,8 +30,8 @@ __global__ void __launch_bounds__(kCountThreads) ce_count_valid_kernel(const int
 
 cudaError_t launch_count_valid(const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index, int64_t* n_valid,
                                int32_t* err, cudaStream_t stream) {
-    ce_count_valid_kernel<<<1, kCountThreads, 0, stream>>>(labels, N, V, ignore_index, n_valid, err);
-    return cudaGetLastError();
+    return launch_dependent(ce_count_valid_kernel, dim3(1), dim3(kCountThreads), 0, stream, labels, N, V, ignore_index,
+                            n_valid, err);
 }
 
 }  // namespace foak

@@ -92,6 +92,8 @@ __global__ void __launch_bounds__(kFinThreads) linear_ce_finalize(const float* _
                                                                   const int32_t* chunk_err, int64_t nchunks,
                                                                   float* loss, int32_t* n_valid_out,
                                                                   int32_t* err_out) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     __shared__ int iscratch[2 * (kFinThreads / 32)];
     __shared__ DFloat dred[kFinThreads / 32];
     int n_valid = 0, n_bad = 0;
@@ -115,6 +117,8 @@ __global__ void __launch_bounds__(kMergeThreads) chunk_lse_kernel(const float2* 
                                                                   const int64_t* __restrict__ labels, int rows,
                                                                   int64_t V, int64_t ignore_index,
                                                                   float* __restrict__ lse, float* __restrict__ row_loss) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
@@ -138,9 +142,8 @@ __global__ void __launch_bounds__(kMergeThreads) chunk_lse_kernel(const float2* 
 cudaError_t launch_rows_finalize(const float* row_loss, const int64_t* labels, int64_t N, int64_t V,
                                  int64_t ignore_index, float denom, const int32_t* chunk_err, int64_t nerr,
                                  float* loss, int32_t* n_valid, int32_t* err, cudaStream_t stream) {
-    linear_ce_finalize<<<1, kFinThreads, 0, stream>>>(row_loss, labels, N, V, ignore_index, denom, chunk_err, nerr,
-                                                      loss, n_valid, err);
-    return cudaGetLastError();
+    return launch_dependent(linear_ce_finalize, dim3(1), dim3(kFinThreads), 0, stream, row_loss, labels, N, V,
+                            ignore_index, denom, chunk_err, nerr, loss, n_valid, err);
 }
 
 size_t linear_ce_workspace_bytes(int64_t N, int64_t V, int64_t chunk) {
@@ -205,9 +208,9 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
             if (e != cudaSuccess) return e;
         }
         // 2. lse and row terms of the chunk's rows (into the batch's row_loss)
-        chunk_lse_kernel<<<(rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32), kMergeThreads, 0, stream>>>(
-            ws.stats, tiles, ws.zlab, labels + r0, rows, V, ignore_index, ws.lse, ws.row_loss + r0);
-        e = cudaGetLastError();
+        e = launch_dependent(chunk_lse_kernel, dim3((rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32)),
+                             dim3(kMergeThreads), 0, stream, ws.stats, tiles, ws.zlab, labels + r0, rows, V,
+                             ignore_index, ws.lse, ws.row_loss + r0);
         if (e != cudaSuccess) return e;
         // 3. dZ = (softmax(Z) - onehot) * g / D in place
         e = launch_ce_backward(2, z, z, ldz, labels + r0, rows, V, ignore_index, ws.lse, nullptr, denom,
@@ -259,9 +262,8 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
             if (e != cudaSuccess) return e;
         }
     }
-    linear_ce_finalize<<<1, kFinThreads, 0, stream>>>(ws.row_loss, labels, N, V, ignore_index, denom, ws.chunk_err,
-                                                      nchunks + 1, loss, n_valid, err);
-    return cudaGetLastError();
+    return launch_dependent(linear_ce_finalize, dim3(1), dim3(kFinThreads), 0, stream, ws.row_loss, labels, N, V,
+                            ignore_index, denom, ws.chunk_err, nchunks + 1, loss, n_valid, err);
 }
 
 }  // namespace foak

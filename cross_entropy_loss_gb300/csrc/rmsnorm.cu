@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const char* _
                                                                    const char* __restrict__ gamma, int64_t N,
                                                                    int64_t D, float eps, char* __restrict__ Y,
                                                                    int64_t ldy, float* __restrict__ rstd) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     constexpr int EPV = 16 / ES;
     const int lane = threadIdx.x & 31;
     const int64_t nvec = D / EPV;
@@ -98,12 +100,65 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const char* _
     }
 }
 
+// Rows of at most 32 * VPL vectors: the warp holds its row in registers (lane l has
+// vectors l, l + 32, ...), so every load of the row is in flight at once and the row
+// is read from memory once; same arithmetic, in the same order, as rmsnorm_fwd_kernel.
+template <int ES, int VPL>
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_reg_kernel(const char* __restrict__ X, int64_t ldx,
+                                                                       const char* __restrict__ gamma, int64_t N,
+                                                                       int64_t D, float eps, char* __restrict__ Y,
+                                                                       int64_t ldy, float* __restrict__ rstd) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
+    constexpr int EPV = 16 / ES;
+    const int lane = threadIdx.x & 31;
+    const int nvec = static_cast<int>(D / EPV);
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kNormThreads / 32);
+    for (int64_t row = blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); row < N; row += warps) {
+        const uint4* x = reinterpret_cast<const uint4*>(X + row * ldx * ES);
+        uint4 v[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int j = lane + 32 * i;
+            v[i] = j < nvec ? ld_global_v4(x + j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            if (lane + 32 * i < nvec) {
+                float f[EPV];
+                unpack<ES>(v[i], f);
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) ss = fmaf(f[k], f[k], ss);
+            }
+        }
+        ss = warp_sum(ss);
+        const float r = rsqrtf(ss / static_cast<float>(D) + eps);
+        char* y = Y + row * ldy * ES;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int j = lane + 32 * i;
+            if (j < nvec) {
+                float f[EPV], gm[EPV];
+                unpack<ES>(v[i], f);
+                load8<ES>(gamma + static_cast<int64_t>(j) * 16, gm);
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) f[k] = f[k] * r * gm[k];
+                store8<ES>(y + static_cast<int64_t>(j) * 16, f);
+            }
+        }
+        if (lane == 0 && rstd) rstd[row] = r;
+    }
+}
+
 template <int ES>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_bwd_kernel(const char* __restrict__ dY, int64_t lddy,
                                                                    const char* __restrict__ X, int64_t ldx,
                                                                    const char* __restrict__ gamma,
                                                                    const float* __restrict__ rstd, int64_t N,
                                                                    int64_t D, char* __restrict__ dX, int64_t lddx) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     constexpr int EPV = 16 / ES;
     const int lane = threadIdx.x & 31;
     const int64_t nvec = D / EPV;
@@ -142,6 +197,8 @@ __global__ void __launch_bounds__(kGammaThreads) rmsnorm_dgamma_kernel(const cha
                                                                        const char* __restrict__ X, int64_t ldx,
                                                                        const float* __restrict__ rstd, int64_t N,
                                                                        int64_t D, float* __restrict__ part) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     constexpr int EPV = 16 / ES;
     const int64_t v = static_cast<int64_t>(blockIdx.x) * kGammaThreads + threadIdx.x;  // vector of columns
     if (v * EPV >= D) return;
@@ -178,6 +235,8 @@ __global__ void __launch_bounds__(1024) rmsnorm_bwd_fused_kernel(const char* __r
                                                                  const float* __restrict__ rstd, int64_t N,
                                                                  int64_t D, char* __restrict__ dX, int64_t lddx,
                                                                  float* __restrict__ part) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     constexpr int EPV = 16 / ES;
     __shared__ float red[2][kFuseRows][32];
     const int v = threadIdx.x, lane = v & 31, warp = v >> 5, warps = blockDim.x >> 5;
@@ -238,12 +297,15 @@ __global__ void __launch_bounds__(1024) rmsnorm_bwd_fused_kernel(const char* __r
     }
 }
 
-// dgamma[j] = sum of part[g][j] over g < G, in a fixed order: 8 slices of 64
-// columns per CTA, slice sl summing g = sl, sl + 8, ... (four interleaved running
-// sums), then slice 0 adding the 8 slice sums in slice order.
-constexpr int kRedCols = 64, kRedSlices = 8;
+// dgamma[j] = sum of part[g][j] over g < G, in a fixed order: 32 slices of 32
+// columns per CTA, slice sl summing g = sl, sl + 32, ... (four interleaved running
+// sums), then slice 0 adding the 32 slice sums in slice order.  (8 slices of 64
+// columns, 64 CTAs for D = 4096, took 7.8 us: each thread walked ~38 partials.)
+constexpr int kRedCols = 32, kRedSlices = 32;
 __global__ void __launch_bounds__(kRedCols * kRedSlices) rmsnorm_dgamma_reduce(const float* __restrict__ part, int G,
                                                                              int64_t D, float* __restrict__ dgamma) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     __shared__ float ss[kRedSlices][kRedCols];
     const int c = threadIdx.x % kRedCols, sl = threadIdx.x / kRedCols;
     const int64_t j = static_cast<int64_t>(blockIdx.x) * kRedCols + c;
@@ -279,74 +341,61 @@ int norm_grid(int64_t N) {
 cudaError_t launch_rmsnorm_fwd(int es, const void* X, int64_t ldx, const void* gamma, int64_t N, int64_t D,
                                float eps, void* Y, int64_t ldy, float* rstd, cudaStream_t s) {
     if (N == 0) return cudaSuccess;
-    const int grid = norm_grid(N);
-    if (es == 2)
-        rmsnorm_fwd_kernel<2><<<grid, kNormThreads, 0, s>>>(static_cast<const char*>(X), ldx,
-                                                            static_cast<const char*>(gamma), N, D, eps,
-                                                            static_cast<char*>(Y), ldy, rstd);
-    else
-        rmsnorm_fwd_kernel<4><<<grid, kNormThreads, 0, s>>>(static_cast<const char*>(X), ldx,
-                                                            static_cast<const char*>(gamma), N, D, eps,
-                                                            static_cast<char*>(Y), ldy, rstd);
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned>(norm_grid(N))), block(kNormThreads);
+    const char* x = static_cast<const char*>(X);
+    const char* g = static_cast<const char*>(gamma);
+    char* y = static_cast<char*>(Y);
+    // rows of at most 512 vectors in registers (D <= 4096 bf16 / 2048 fp32)
+    const int64_t nvec = D / (16 / es);
+    if (nvec <= 128)
+        return es == 2 ? launch_dependent(rmsnorm_fwd_reg_kernel<2, 4>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd)
+                       : launch_dependent(rmsnorm_fwd_reg_kernel<4, 4>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd);
+    if (nvec <= 512)
+        return es == 2 ? launch_dependent(rmsnorm_fwd_reg_kernel<2, 16>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd)
+                       : launch_dependent(rmsnorm_fwd_reg_kernel<4, 16>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd);
+    return es == 2 ? launch_dependent(rmsnorm_fwd_kernel<2>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd)
+                   : launch_dependent(rmsnorm_fwd_kernel<4>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd);
 }
 
 cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void* X, int64_t ldx, const void* gamma,
                                const float* rstd, int64_t N, int64_t D, void* dX, int64_t lddx, float* part,
                                float* dgamma, cudaStream_t s) {
     const int64_t nvec = D / (16 / es);
+    const char* dy = static_cast<const char*>(dY);
+    const char* x = static_cast<const char*>(X);
+    const char* g = static_cast<const char*>(gamma);
+    char* dx = static_cast<char*>(dX);
+    const dim3 rgrid(static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols))),
+        rblock(kRedCols * kRedSlices);
+    cudaError_t e = cudaSuccess;
     if (dgamma && N > 0 && nvec <= 1024) {
         // one pass: dX and the dgamma partials of each CTA, then the fixed-order reduce
-        const int threads = static_cast<int>((nvec + 31) / 32 * 32);
+        const dim3 block(static_cast<unsigned>((nvec + 31) / 32 * 32));
         const int grid = static_cast<int>(std::min<int64_t>(
             {(N + kFuseRows - 1) / kFuseRows, static_cast<int64_t>(device_sm_count()) * 2, kFuseMaxGrid}));
-        if (es == 2)
-            rmsnorm_bwd_fused_kernel<2><<<grid, threads, 0, s>>>(static_cast<const char*>(dY), lddy,
-                                                                 static_cast<const char*>(X), ldx,
-                                                                 static_cast<const char*>(gamma), rstd, N, D,
-                                                                 static_cast<char*>(dX), lddx, part);
-        else
-            rmsnorm_bwd_fused_kernel<4><<<grid, threads, 0, s>>>(static_cast<const char*>(dY), lddy,
-                                                                 static_cast<const char*>(X), ldx,
-                                                                 static_cast<const char*>(gamma), rstd, N, D,
-                                                                 static_cast<char*>(dX), lddx, part);
-        cudaError_t e = cudaGetLastError();
+        e = es == 2 ? launch_dependent(rmsnorm_bwd_fused_kernel<2>, dim3(grid), block, 0, s, dy, lddy, x, ldx, g, rstd, N,
+                                       D, dx, lddx, part)
+                    : launch_dependent(rmsnorm_bwd_fused_kernel<4>, dim3(grid), block, 0, s, dy, lddy, x, ldx, g, rstd, N,
+                                       D, dx, lddx, part);
         if (e != cudaSuccess) return e;
-        rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols)), kRedCols * kRedSlices, 0, s>>>(part, grid, D,
-                                                                                                       dgamma);
-        return cudaGetLastError();
+        return launch_dependent(rmsnorm_dgamma_reduce, rgrid, rblock, 0, s, part, grid, D, dgamma);
     }
     if (N > 0) {
-        const int grid = norm_grid(N);
-        if (es == 2)
-            rmsnorm_bwd_kernel<2><<<grid, kNormThreads, 0, s>>>(static_cast<const char*>(dY), lddy,
-                                                                static_cast<const char*>(X), ldx,
-                                                                static_cast<const char*>(gamma), rstd, N, D,
-                                                                static_cast<char*>(dX), lddx);
-        else
-            rmsnorm_bwd_kernel<4><<<grid, kNormThreads, 0, s>>>(static_cast<const char*>(dY), lddy,
-                                                                static_cast<const char*>(X), ldx,
-                                                                static_cast<const char*>(gamma), rstd, N, D,
-                                                                static_cast<char*>(dX), lddx);
-        cudaError_t e = cudaGetLastError();
+        const dim3 grid(static_cast<unsigned>(norm_grid(N))), block(kNormThreads);
+        e = es == 2 ? launch_dependent(rmsnorm_bwd_kernel<2>, grid, block, 0, s, dy, lddy, x, ldx, g, rstd, N, D, dx, lddx)
+                    : launch_dependent(rmsnorm_bwd_kernel<4>, grid, block, 0, s, dy, lddy, x, ldx, g, rstd, N, D, dx, lddx);
         if (e != cudaSuccess) return e;
     }
     if (!dgamma) return cudaSuccess;
     const int epv = 16 / es;
     const dim3 ggrid(static_cast<unsigned>((D / epv + kGammaThreads - 1) / kGammaThreads), kRmsGammaGroups);
-    if (es == 2)
-        rmsnorm_dgamma_kernel<2><<<ggrid, kGammaThreads, 0, s>>>(static_cast<const char*>(dY), lddy,
-                                                                 static_cast<const char*>(X), ldx, rstd, N, D,
-                                                                 part);
-    else
-        rmsnorm_dgamma_kernel<4><<<ggrid, kGammaThreads, 0, s>>>(static_cast<const char*>(dY), lddy,
-                                                                 static_cast<const char*>(X), ldx, rstd, N, D,
-                                                                 part);
-    cudaError_t e = cudaGetLastError();
+    e = es == 2 ? launch_dependent(rmsnorm_dgamma_kernel<2>, ggrid, dim3(kGammaThreads), 0, s, dy, lddy, x, ldx, rstd, N,
+                                   D, part)
+                : launch_dependent(rmsnorm_dgamma_kernel<4>, ggrid, dim3(kGammaThreads), 0, s, dy, lddy, x, ldx, rstd, N,
+                                   D, part);
     if (e != cudaSuccess) return e;
-    rmsnorm_dgamma_reduce<<<static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols)), kRedCols * kRedSlices, 0, s>>>(
-        part, kRmsGammaGroups, D, dgamma);
-    return cudaGetLastError();
+    return launch_dependent(rmsnorm_dgamma_reduce, rgrid, rblock, 0, s, part, static_cast<int>(kRmsGammaGroups), D,
+                            dgamma);
 }
 
 }  // namespace foak

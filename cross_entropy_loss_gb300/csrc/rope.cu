@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_apply_kernel(const RopeTens
                                                                   const float* __restrict__ cos_t,
                                                                   const float* __restrict__ sin_t, int64_t P,
                                                                   float sign, int32_t* err) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
     constexpr int EPV = 16 / ES;
     const int half = d / 2;
     const int per_head = half / EPV;  // vector pairs per head
@@ -166,11 +168,10 @@ cudaError_t launch_rope_apply(int es, void* X, int64_t T, int H, int64_t ldt, vo
         static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + kRopeThreads - 1) / kRopeThreads,
                                                                 static_cast<int64_t>(device_sm_count()) * 8)));
     const float sign = inverse ? -1.f : 1.f;
-    if (es == 2)
-        rope_apply_kernel<2><<<grid, kRopeThreads, 0, s>>>(a, T, d, positions, cos_t, sin_t, max_pos, sign, err);
-    else
-        rope_apply_kernel<4><<<grid, kRopeThreads, 0, s>>>(a, T, d, positions, cos_t, sin_t, max_pos, sign, err);
-    return cudaGetLastError();
+    return es == 2 ? launch_dependent(rope_apply_kernel<2>, dim3(grid), dim3(kRopeThreads), 0, s, a, T, d, positions,
+                                      cos_t, sin_t, max_pos, sign, err)
+                   : launch_dependent(rope_apply_kernel<4>, dim3(grid), dim3(kRopeThreads), 0, s, a, T, d, positions,
+                                      cos_t, sin_t, max_pos, sign, err);
 }
 
 }  // namespace foak
