@@ -96,6 +96,7 @@ constexpr int kGroupUnitBits = 14;  // entry = (problem << 14) | unit
 struct GemmGroup {
     GemmParams prob[kGroupMax];
     int nprob;
+    GemmSideDz side;  // side.rows == 0: none
     uint16_t start[kGroupMaxClusters + 1];
     uint16_t ent[kGroupMaxUnits];
 };
@@ -343,6 +344,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
 // them), its MMA thread commits each stage to both CTAs' empty barriers and each
 // accumulator to both CTAs' acc_full barriers (one commit each, no multicast), and
 // both CTAs' epilogue warps arrive on the even CTA's acc_empty barriers.
+// The side job of a grouped launch for one epilogue warp (gw of nw): work items are
+// (row, 256-vector segment); lane l takes vectors l, l + 32, ... of the segment, all
+// eight loads first, then the gradient and 16-byte streaming stores.
+__device__ __forceinline__ void side_dz(const GemmSideDz& s, int gw, int nw, int lane) {
+    const int nvec = s.V / 8;
+    const int nseg = (nvec + 255) / 256;
+    const float Dd = s.denom_dev ? static_cast<float>(__ldg(s.denom_dev)) : s.denom;
+    const float scale = s.g / Dd;
+    const int items = s.rows * nseg;
+    for (int it = gw; it < items; it += nw) {
+        const int r = it / nseg, sg = it - r * nseg;
+        const int64_t y = __ldg(s.labels + r);
+        const bool valid = y != s.ignore_index && y >= 0 && y < s.V;
+        uint4* zr = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(s.z) + static_cast<int64_t>(r) * s.ldz);
+        const int v0 = sg * 256;
+        if (!valid) {
+            if (sg == 0 && lane == 0 && y != s.ignore_index && s.err) atomicOr(s.err, FOAK_ERRBIT_LABEL_RANGE);
+            const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int v = v0 + lane + 32 * i;
+                if (v < nvec) st_global_cs_v4(zr + v, zero);
+            }
+            continue;
+        }
+        const float c = __ldg(s.lse + r) * kLog2e;
+        const int yv = static_cast<int>(y >> 3), ye = static_cast<int>(y & 7);
+        uint4 x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int v = v0 + lane + 32 * i;
+            if (v < nvec) x[i] = ld_global_v4(zr + v);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int v = v0 + lane + 32 * i;
+            if (v < nvec) {
+                const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+                float d[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    d[2 * k] = ex2(fmaf(bf16_lo(w[k]), kLog2e, -c)) * scale;
+                    d[2 * k + 1] = ex2(fmaf(bf16_hi(w[k]), kLog2e, -c)) * scale;
+                }
+                if (v == yv) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (e == ye) d[e] -= scale;
+                }
+                st_global_cs_v4(zr + v, make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
+                                                   pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7])));
+            }
+        }
+    }
+}
+
 // GROUPED: the kernel's argument is a GemmGroup and each cluster walks its entries;
 // otherwise one GemmParams whose units the clusters take round-robin.
 template <bool GROUPED>
@@ -500,6 +557,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t acc_phase = 0;
         const uint32_t lead_acc_empty0 = mapa_u32(&acc_empty[0], 0);
         const uint32_t lead_acc_empty1 = mapa_u32(&acc_empty[1], 0);
+        if constexpr (GROUPED) {
+            // idle until the first accumulator is ready: the side job first
+            if (g.side.rows > 0) side_dz(g.side, static_cast<int>(blockIdx.x) * 4 + q, static_cast<int>(gridDim.x) * 4, lane);
+        }
         for (int i = 0; i < n_my; ++i) {
             int t;
             const GemmParams& p = unit_at(i, t);
@@ -746,7 +807,21 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     return launch_pair(p, std::min(units, max_pairs), stream);
 }
 
-cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream) {
+bool gemm_group_fits(const GemmDesc* d, int n) {
+    int total = 0, live = 0;
+    for (int i = 0; i < n; ++i) {
+        if (d[i].M <= 0 || d[i].N <= 0 || d[i].K <= 0) continue;
+        const int tiles_m = (d[i].M + kBM - 1) / kBM;
+        if (tiles_m < 2) return false;
+        const int u = (tiles_m + 1) / 2 * ((d[i].N + kBN - 1) / kBN);
+        if (u >= (1 << kGroupUnitBits)) return false;
+        total += u;
+        ++live;
+    }
+    return live <= kGroupMax && total <= kGroupMaxUnits;
+}
+
+cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream, const GemmSideDz* side) {
     // the non-empty products
     const GemmDesc* live[kGroupMax];
     int nl = 0;
@@ -768,8 +843,12 @@ cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream
         small = small && u < (1 << kGroupUnitBits);
         total += u;
     }
+    const bool has_side = side && side->rows > 0;
+    if (has_side && (!all_pair || !small || total > kGroupMaxUnits || side->V % 8 != 0 || side->ldz % 8 != 0 ||
+                     reinterpret_cast<uintptr_t>(side->z) % 16 != 0))
+        return cudaErrorInvalidValue;  // the caller checks gemm_group_fits and runs the job by itself otherwise
     // one product, a product of single-CTA tiles, or too many units: separate launches, in order
-    if (nl == 1 || !all_pair || !small || total > kGroupMaxUnits) {
+    if ((nl == 1 && !has_side) || !all_pair || !small || total > kGroupMaxUnits) {
         for (int q = 0; q < nl; ++q) {
             const cudaError_t e = launch_gemm_bf16(*live[q], stream);
             if (e != cudaSuccess) return e;
@@ -792,6 +871,7 @@ cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream
         s = &it->second;
     }
     grp.nprob = nl;
+    grp.side = has_side ? *side : GemmSideDz{};
     std::copy(s->start.begin(), s->start.end(), grp.start);
     std::copy(s->ent.begin(), s->ent.end(), grp.ent);
     return launch_pair(grp, s->clusters, stream);

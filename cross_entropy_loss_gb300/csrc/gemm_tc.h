@@ -44,11 +44,35 @@ constexpr int kGemmTileN = 256;
 
 cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream);
 
+// Streaming work the epilogue warps of a grouped launch do before their first
+// accumulator is ready (they are idle then): the cross-entropy gradient of a chunk's
+// bf16 logits in place, z <- (exp(z - lse_row) - [col == label_row]) * g / D, rows of
+// ignored labels (or labels outside [0, V), which set FOAK_ERRBIT_LABEL_RANGE in err)
+// zero-filled.  V % 8 == 0 and 16-byte aligned rows (gemm_side_fits).  The same
+// arithmetic, element for element, as the separate backward kernel.
+struct GemmSideDz {
+    void* z;                   // bf16 [rows][ldz]
+    int64_t ldz;
+    const int64_t* labels;     // [rows]
+    const float* lse;          // [rows], natural log
+    int rows;
+    int V;
+    int64_t ignore_index;
+    float g;
+    float denom;               // used when denom_dev is null
+    const int64_t* denom_dev;  // the denominator as an int64 in device memory, or null
+    int32_t* err;              // OR-ed with FOAK_ERRBIT_LABEL_RANGE; may be null
+};
+
 // Up to three independent products in one persistent launch of the CTA-pair kernel
 // (every product with M > 128): the clusters take a list of (product, output unit)
 // entries balanced by estimated cost, longest first.  No product may write what another
 // reads.  Other cases are launched one product after another, in order.  The error word
 // of the first product receives every timeout.
-cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream);
+cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream, const GemmSideDz* side = nullptr);
+
+// Whether launch_gemm_bf16_group runs these products as one grouped launch (and so can
+// take a side job): every product on CTA pairs (M > 128), at most 8192 units.
+bool gemm_group_fits(const GemmDesc* d, int n);
 
 }  // namespace foak

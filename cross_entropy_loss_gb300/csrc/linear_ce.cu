@@ -6,26 +6,28 @@
 //
 // The batch's n_valid is counted once up front (unless the caller gives denom), so
 // every chunk divides by the same D and the result does not depend on the chunk
-// size.  Then for each chunk of rows [r0, r0 + C):
+// size.  Per chunk of rows [r0, r0 + C):
 //   1. Z  = H_c W^T            tcgen05 GEMM, bf16 out (C x V scratch); its epilogue
 //                              also reduces each row of each 128 x 256 output tile
 //                              from the fp32 accumulator to (max, sum exp(z - max))
 //                              and keeps the logit at the row's label
 //   2. lse, row terms          one warp per row merges its tiles' pairs
-//   3. dZ = (exp(Z - lse) - onehot) g / D   the streaming backward kernel, in
-//                              place on Z (one read, one write, no row reduction)
+//   3. dZ = (exp(Z - lse) - onehot) g / D   in place on Z, one streaming read and
+//                              write per element (no row reduction)
 //   4. dH_c = dZ W             tcgen05 GEMM, bf16 out into dH
 //   5. dW (+)= dZ^T H          tcgen05 GEMM, fp32 out, once per group of
 //                              kDeferChunks chunks (stored by the first group,
 //                              added by TMA reduce for the others)
 // and finally one CTA sums the per-row loss terms of all N rows (double-float, a
-// fixed order) over the denominator.  Step 4 of a chunk runs in one launch with step
-// 1 of the next (two independent products on one persistent grid, see
-// launch_gemm_bf16_group): dH's 4 x 16 output units of 256 x 256 would leave 12 of the
-// 76 SM pairs idle for its whole run.  Only one group's Z lives at a time.  Steps 1-2
-// are the GEMM-1 epilogue statistics of the chunked loss; the softmax itself is
-// rebuilt from Z and lse by step 3 rather than inside the producers of steps 4-5,
-// whose operands would then each need an exponential at the tensor cores' rate.
+// fixed order) over the denominator.  The GEMMs run as grouped launches
+// (launch_gemm_bf16_group): launch c holds step 1 of chunk c and step 4 of chunk
+// c - 2 on one persistent grid, and its epilogue warps, idle until their first
+// accumulator is ready, do step 3 of chunk c - 1 first (dH's 4 x 16 output units of
+// 256 x 256 alone would leave 12 of the 76 SM pairs idle, and a separate dZ pass
+// took 19 us per chunk).  Two groups' logits are resident.  Steps 1-2 are the GEMM-1
+// epilogue statistics of the chunked loss; the softmax itself is rebuilt from Z and
+// lse by step 3 rather than inside the producers of steps 4-5, whose operands would
+// then each need an exponential at the tensor cores' rate.
 #include <algorithm>
 
 #include "common.cuh"
@@ -53,7 +55,7 @@ struct LinWs {
     float2* stats;       // C x tiles per-tile (max, sum exp) of the chunk's rows
     float* zlab;         // C logits at the labels
     float* lse;          // C
-    void* z;             // kDeferChunks chunks x ldz bf16
+    void* z;             // 2 kDeferChunks chunks x ldz bf16 (two dW groups)
     size_t bytes;
 };
 
@@ -79,7 +81,7 @@ LinWs lin_layout(void* base, int64_t N, int64_t V, int64_t chunk) {
     w.lse = reinterpret_cast<float*>(b + off);
     off += round256(crows * 4);
     w.z = b + off;
-    off += round256(static_cast<size_t>(std::min(kDeferChunks * chunk, std::max<int64_t>(N, 1))) *
+    off += round256(static_cast<size_t>(std::min(2 * kDeferChunks * chunk, std::max<int64_t>(N, 1))) *
                     static_cast<size_t>(ldz) * 2);
     w.bytes = off;
     return w;
@@ -157,7 +159,8 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
     const int64_t ldz = (V + 63) / 64 * 64;
     const int64_t nchunks = N > 0 ? (N + chunk - 1) / chunk : 0;
     int32_t* gemm_err = ws.chunk_err + nchunks;  // GEMM timeouts are OR-ed in here
-    cudaError_t e = cudaMemsetAsync(gemm_err, 0, sizeof(int32_t), stream);
+    // every error word starts at 0: the chunks' dZ passes and the GEMMs OR into theirs
+    cudaError_t e = cudaMemsetAsync(ws.chunk_err, 0, static_cast<size_t>(nchunks + 1) * sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
     if (nchunks == 0) {
         e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * static_cast<size_t>(D) * 4, stream);
@@ -174,93 +177,123 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
     const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
     __nv_bfloat16* dHb = static_cast<__nv_bfloat16*>(dH);
     __nv_bfloat16* zbuf = static_cast<__nv_bfloat16*>(ws.z);
-    // dH of a chunk goes out with the next chunk's Z in one launch (the 64 units of dH
-    // alone leave 12 of the 76 SM pairs idle), and the last one with the last dW
-    GemmDesc pend_dh = {};
-    bool have_dh = false;
+    auto rows_of = [&](int64_t c) { return static_cast<int>(std::min(chunk, N - c * chunk)); };
+    // chunk c's logits live in slot c % (2 kDeferChunks): a dW group's chunks are adjacent
+    auto z_of = [&](int64_t c) { return zbuf + (c % (2 * kDeferChunks)) * chunk * ldz; };
+    auto z_desc = [&](int64_t c) {  // 1. Z = H_c W^T, with the epilogue statistics
+        GemmDesc d = {};
+        d.a = Hb + c * chunk * D;
+        d.lda = D;
+        d.b = W;
+        d.ldb = D;
+        d.M = rows_of(c);
+        d.N = static_cast<int>(V);
+        d.K = static_cast<int>(D);
+        d.out = z_of(c);
+        d.ldo = ldz;
+        d.mode = kGemmOutBf16Stats;
+        d.err = gemm_err;
+        d.labels = labels + c * chunk;
+        d.stats = ws.stats;
+        d.stats_ld = tiles;
+        d.zlab = ws.zlab;
+        return d;
+    };
+    auto dh_desc = [&](int64_t c) {  // 4. dH_c = dZ_c W (W is [V][D]: MN-major as the [K][N] operand)
+        GemmDesc d = {};
+        d.a = z_of(c);
+        d.lda = ldz;
+        d.b = W;
+        d.ldb = D;
+        d.b_mn_major = true;
+        d.M = rows_of(c);
+        d.N = static_cast<int>(D);
+        d.K = static_cast<int>(V);
+        d.out = dHb + c * chunk * D;
+        d.ldo = D;
+        d.mode = kGemmOutBf16;
+        d.err = gemm_err;
+        return d;
+    };
+    auto dw_desc = [&](int64_t c_last) {  // 5. dW (+)= dZ_g^T H_g over the group ending at c_last
+        const int64_t c0 = c_last - c_last % kDeferChunks;
+        GemmDesc d = {};
+        d.a = z_of(c0);  // dZ_g is [rows_g][V] = [K][M], H_g is [rows_g][D] = [K][N]
+        d.lda = ldz;
+        d.a_mn_major = true;
+        d.b = Hb + c0 * chunk * D;
+        d.ldb = D;
+        d.b_mn_major = true;
+        d.M = static_cast<int>(V);
+        d.N = static_cast<int>(D);
+        d.K = static_cast<int>(c_last * chunk + rows_of(c_last) - c0 * chunk);
+        d.out = dW;
+        d.ldo = D;
+        d.mode = c0 == 0 ? kGemmOutF32 : kGemmOutF32Acc;
+        d.err = gemm_err;
+        return d;
+    };
+    auto side_of = [&](int64_t c) {  // 3. dZ_c = (softmax(Z_c) - onehot) * g / D in place
+        GemmSideDz s = {};
+        s.z = z_of(c);
+        s.ldz = ldz;
+        s.labels = labels + c * chunk;
+        s.lse = ws.lse;
+        s.rows = rows_of(c);
+        s.V = static_cast<int>(V);
+        s.ignore_index = ignore_index;
+        s.g = g;
+        s.denom = denom;
+        s.denom_dev = denom_dev;
+        s.err = ws.chunk_err + c;
+        return s;
+    };
+    auto dz_alone = [&](int64_t c) {
+        return launch_ce_backward(2, z_of(c), z_of(c), ldz, labels + c * chunk, rows_of(c), V, ignore_index, ws.lse,
+                                  nullptr, denom, ws.chunk_err + c, stream, g, denom_dev);
+    };
+    // Launch c holds Z(c) and dH(c - 2), and its epilogue warps turn Z(c - 1) into dZ(c - 1)
+    // before their first accumulator (they are idle then); the three touch three different
+    // slots.  The lse of chunk c - 1 is in ws.lse from the kernel after launch c - 1.
     for (int64_t c = 0; c < nchunks; ++c) {
-        const int64_t r0 = c * chunk;
-        const int rows = static_cast<int>(std::min(chunk, N - r0));
-        const int64_t slot = c % kDeferChunks;  // this chunk's place in the group's Z buffer
-        __nv_bfloat16* z = zbuf + slot * chunk * ldz;
-        // 1. Z = H_c W^T
-        GemmDesc g1 = {};
-        g1.a = Hb + r0 * D;
-        g1.lda = D;
-        g1.a_mn_major = false;
-        g1.b = W;
-        g1.ldb = D;
-        g1.b_mn_major = false;
-        g1.M = rows;
-        g1.N = static_cast<int>(V);
-        g1.K = static_cast<int>(D);
-        g1.out = z;
-        g1.ldo = ldz;
-        g1.mode = kGemmOutBf16Stats;
-        g1.err = gemm_err;
-        g1.labels = labels + r0;
-        g1.stats = ws.stats;
-        g1.stats_ld = tiles;
-        g1.zlab = ws.zlab;
-        {
-            const GemmDesc grp[2] = {g1, pend_dh};  // Z(c) writes the other Z slot than dH(c-1) reads
-            e = launch_gemm_bf16_group(grp, have_dh ? 2 : 1, stream);
-            if (e != cudaSuccess) return e;
-        }
-        // 2. lse and row terms of the chunk's rows (into the batch's row_loss)
-        e = launch_dependent(chunk_lse_kernel, dim3((rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32)),
-                             dim3(kMergeThreads), 0, stream, ws.stats, tiles, ws.zlab, labels + r0, rows, V,
-                             ignore_index, ws.lse, ws.row_loss + r0);
-        if (e != cudaSuccess) return e;
-        // 3. dZ = (softmax(Z) - onehot) * g / D in place
-        e = launch_ce_backward(2, z, z, ldz, labels + r0, rows, V, ignore_index, ws.lse, nullptr, denom,
-                               ws.chunk_err + c, stream, g, denom_dev);
-        if (e != cudaSuccess) return e;
-        // 4. dH_c = dZ W     (W is [V][D]: MN-major as the [K][N] operand), launched later
-        GemmDesc& g2 = pend_dh;
-        g2 = GemmDesc{};
-        g2.a = z;
-        g2.lda = ldz;
-        g2.a_mn_major = false;
-        g2.b = W;
-        g2.ldb = D;
-        g2.b_mn_major = true;
-        g2.M = rows;
-        g2.N = static_cast<int>(D);
-        g2.K = static_cast<int>(V);
-        g2.out = dHb + r0 * D;
-        g2.ldo = D;
-        g2.mode = kGemmOutBf16;
-        g2.err = gemm_err;
-        have_dh = true;
-        // 5. once the group is complete: dW (+)= dZ_g^T H_g over the group's rows
-        //    (dZ_g is [rows_g][V] = [K][M], H_g is [rows_g][D] = [K][N])
-        if (slot == kDeferChunks - 1 || c == nchunks - 1) {
-            const int64_t g0 = (c - slot) * chunk;
-            const int rows_g = static_cast<int>(r0 + rows - g0);
-            GemmDesc g3 = {};
-            g3.a = zbuf;
-            g3.lda = ldz;
-            g3.a_mn_major = true;
-            g3.b = Hb + g0 * D;
-            g3.ldb = D;
-            g3.b_mn_major = true;
-            g3.M = static_cast<int>(V);
-            g3.N = static_cast<int>(D);
-            g3.K = rows_g;
-            g3.out = dW;
-            g3.ldo = D;
-            g3.mode = g0 == 0 ? kGemmOutF32 : kGemmOutF32Acc;
-            g3.err = gemm_err;
-            if (c == nchunks - 1) {
-                const GemmDesc fin[2] = {pend_dh, g3};
-                e = launch_gemm_bf16_group(fin, 2, stream);
-                have_dh = false;
-            } else {
-                e = launch_gemm_bf16(g3, stream);
+        GemmDesc grp[2] = {z_desc(c), c >= 2 ? dh_desc(c - 2) : GemmDesc{}};
+        const int np = c >= 2 ? 2 : 1;
+        if (c >= 1) {
+            const GemmSideDz side = side_of(c - 1);
+            if (V % 8 == 0 && gemm_group_fits(grp, np)) {
+                e = launch_gemm_bf16_group(grp, np, stream, &side);
+            } else {  // single-CTA tiles or a ragged vocabulary: the dZ kernel by itself first
+                e = dz_alone(c - 1);
+                if (e == cudaSuccess) e = launch_gemm_bf16_group(grp, np, stream);
             }
+        } else {
+            e = launch_gemm_bf16_group(grp, np, stream);
+        }
+        if (e != cudaSuccess) return e;
+        // 2. lse and row terms of chunk c's rows (into the batch's row_loss)
+        const int rows = rows_of(c);
+        e = launch_dependent(chunk_lse_kernel, dim3((rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32)),
+                             dim3(kMergeThreads), 0, stream, ws.stats, tiles, ws.zlab, labels + c * chunk, rows, V,
+                             ignore_index, ws.lse, ws.row_loss + c * chunk);
+        if (e != cudaSuccess) return e;
+        // a group whose last dZ that launch wrote, unless it is the batch's last group
+        if (c >= 1 && (c - 1) % kDeferChunks == kDeferChunks - 1) {
+            e = launch_gemm_bf16(dw_desc(c - 1), stream);
             if (e != cudaSuccess) return e;
         }
+    }
+    if (nchunks > 0) {
+        // the last chunk's dZ, then the last dH products and the last group's dW together
+        const int64_t cl = nchunks - 1;
+        e = dz_alone(cl);
+        if (e != cudaSuccess) return e;
+        GemmDesc fin[3];
+        int nf = 0;
+        if (cl >= 1) fin[nf++] = dh_desc(cl - 1);
+        fin[nf++] = dh_desc(cl);
+        fin[nf++] = dw_desc(cl);
+        e = launch_gemm_bf16_group(fin, nf, stream);
+        if (e != cudaSuccess) return e;
     }
     return launch_dependent(linear_ce_finalize, dim3(1), dim3(kFinThreads), 0, stream, ws.row_loss, labels, N, V,
                             ignore_index, denom, ws.chunk_err, nchunks + 1, loss, n_valid, err);

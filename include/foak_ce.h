@@ -336,8 +336,9 @@ foak_status foak_rope_apply_qk(void* Q, int64_t Hq, int64_t ldq, void* K, int64_
  * Bytes of device workspace foak_linear_ce_chunked needs: the batch's label
  * count, N float32 per-row loss terms, a few error words, one chunk's per-tile
  * softmax statistics (chunk x ceil(V / 256) float pairs), its label logits and
- * log-sum-exps, and four chunks of bf16 logits (min(4 chunk, N) x V, rows padded
- * to 64 elements: dW is updated once per group of four chunks).  256-byte aligned; its
+ * log-sum-exps, and eight chunks of bf16 logits (min(8 chunk, N) x V, rows padded
+ * to 64 elements: dW is updated once per group of four chunks, and one group is
+ * computed while the last one is used).  256-byte aligned; its
  * contents need no initialisation and every call may reuse it.
  */
 size_t foak_linear_ce_workspace_size(int64_t N, int64_t V, int64_t D, int64_t chunk);

@@ -39,7 +39,12 @@ def _run(ce, H, W, y, chunk, g=1.0, denom=0.0):
             out["dW"].cpu().numpy().astype(np.float64), out["n_valid"].item(), out["err"].item())
 
 
-@pytest.mark.parametrize("N,V,D,chunk", [(300, 1000, 256, 128), (129, 520, 64, 1024), (1024, 4096, 512, 256)])
+# (2600, 4096, 512, 256): 11 chunks -- dZ passes inside the grouped launches, a dW group
+# launched mid-loop, Z slots reused, a partial last group and a 40-row last chunk on
+# single-CTA tiles; (600, 1001, 128, 256): a vocabulary that is not a multiple of 8
+# (the dZ pass runs by itself)
+@pytest.mark.parametrize("N,V,D,chunk", [(300, 1000, 256, 128), (129, 520, 64, 1024), (1024, 4096, 512, 256),
+                                         (2600, 4096, 512, 256), (600, 1001, 128, 256)])
 def test_linear_ce_small(cuda_lib, N, V, D, chunk):
     H, W, y = _case(N, V, D, seed=N + V + D, n_ignore=N // 10)
     ref = oracle.linear_ce(H, W, y, g=1.5)
