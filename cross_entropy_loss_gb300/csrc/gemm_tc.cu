@@ -7,7 +7,7 @@
 //   gemm_bf16_tc_pair_kernel  clusters of two CTAs whose tensor cores compute one
 //                             256 x 256 tile together (tcgen05 cta_group::2): each
 //                             CTA loads its own 128 rows of A and its own 128 rows of
-//                             B (plain TMA, no multicast), the even CTA issues the
+//                             B (plain tiled TMA of its own tiles), the even CTA issues the
 //                             M = 256 MMAs over both CTAs' shared memory, and each
 //                             CTA's TMEM receives its 128 rows of the accumulator.
 //                             Per CTA a 64-deep k-block is 32 KB instead of 48 KB, so
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
 // m0 + 128r .. m0 + 128r + 127 of the unit's A and rows n0 + 128r .. of its B; the
 // even CTA's full barriers count both CTAs' bytes (the odd CTA's copies complete on
 // them), its MMA thread commits each stage to both CTAs' empty barriers and each
-// accumulator to both CTAs' acc_full barriers (one commit each, no multicast), and
+// accumulator to both CTAs' acc_full barriers (one commit per barrier), and
 // both CTAs' epilogue warps arrive on the even CTA's acc_empty barriers.
 // The side job of a grouped launch for one epilogue warp (gw of nw): work items are
 // (row, 256-vector segment); lane l takes vectors l, l + 32, ... of the segment, all
