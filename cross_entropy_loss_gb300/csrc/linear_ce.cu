@@ -254,10 +254,17 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
     };
     // Launch c holds Z(c) and dH(c - 2), and its epilogue warps turn Z(c - 1) into dZ(c - 1)
     // before their first accumulator (they are idle then); the three touch three different
-    // slots.  The lse of chunk c - 1 is in ws.lse from the kernel after launch c - 1.
+    // slots.  The lse of chunk c - 1 is in ws.lse from the kernel after launch c - 1.  A
+    // group's dW, ready after the launch that finished its last dZ, rides in the next
+    // launch (it reads its own half of the slots; Z(c) goes to the other half).
+    int64_t dw_pending = -1;  // last chunk of a finished group whose dW is not launched yet
     for (int64_t c = 0; c < nchunks; ++c) {
-        GemmDesc grp[2] = {z_desc(c), c >= 2 ? dh_desc(c - 2) : GemmDesc{}};
-        const int np = c >= 2 ? 2 : 1;
+        GemmDesc grp[3] = {z_desc(c), c >= 2 ? dh_desc(c - 2) : GemmDesc{}, GemmDesc{}};
+        int np = c >= 2 ? 2 : 1;
+        if (dw_pending >= 0) {
+            grp[np++] = dw_desc(dw_pending);
+            dw_pending = -1;
+        }
         if (c >= 1) {
             const GemmSideDz side = side_of(c - 1);
             if (V % 8 == 0 && gemm_group_fits(grp, np)) {
@@ -276,10 +283,15 @@ cudaError_t launch_linear_ce(const void* H, const void* W, const int64_t* labels
                              dim3(kMergeThreads), 0, stream, ws.stats, tiles, ws.zlab, labels + c * chunk, rows, V,
                              ignore_index, ws.lse, ws.row_loss + c * chunk);
         if (e != cudaSuccess) return e;
-        // a group whose last dZ that launch wrote, unless it is the batch's last group
+        // a group whose last dZ that launch wrote, unless it is the batch's last group:
+        // its dW goes with the next launch, or by itself when there is none
         if (c >= 1 && (c - 1) % kDeferChunks == kDeferChunks - 1) {
-            e = launch_gemm_bf16(dw_desc(c - 1), stream);
-            if (e != cudaSuccess) return e;
+            if (c + 1 < nchunks) {
+                dw_pending = c - 1;
+            } else {
+                e = launch_gemm_bf16(dw_desc(c - 1), stream);
+                if (e != cudaSuccess) return e;
+            }
         }
     }
     if (nchunks > 0) {
