@@ -403,3 +403,20 @@ def test_loss_sum_within_one_ulp_of_exact(cuda_lib, dtype):
     for t in terms:
         naive = np.float32(naive + t)
     assert abs(int(np.float32(naive / np.float32(n)).view(np.int32)) - int(want.view(np.int32))) > 50
+
+
+def test_forward_counts_on_the_way_with_bad_labels(cuda_lib):
+    """The forward of aligned rows counts each CTA's labels on the way and adds the counts
+    at the end: n_valid, the label-range bit and the loss must come out as the oracle's
+    with ignored and out-of-range labels among 700 rows (several per CTA)."""
+    N, V = 700, 4000
+    x, y = _rand(N, V, wl.BF16, seed=31, n_ignore=60)
+    y[[3, 401]] = [V, -7]  # out of range: counted as bad, treated as ignored
+    ref = oracle.ce(x, y, V)
+    f = cuda_lib.foak_ce_forward(to_device(x, wl.BF16), torch.from_numpy(y).cuda(), want_lse=True)
+    torch.cuda.synchronize()
+    assert ref["n_bad"] == 2
+    assert f["n_valid"].item() == ref["n_valid"] and f["err"].item() == 1
+    assert_loss_close(f["loss"].item(), ref["loss"], wl.BF16)
+    valid = ref["state"] == oracle.VALID
+    np.testing.assert_allclose(to_f64(f["lse"])[valid], ref["lse"][valid], rtol=2e-6, atol=2e-6)
