@@ -67,6 +67,7 @@ SIGNATURES = {
                                        _vp]),
     "foak_gemm_bf16": (_i32, [_vp, _i64, _i32, _vp, _i64, _i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _vp]),
     "foak_gemm_bf16_group": (_i32, [_vp, _i32, _vp, _vp]),
+    "foak_test_gemm_group_schedule": (_i32, [_vp, _i32, _i32, _vp, _vp, _i32]),
     "foak_linear_ce_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
     "foak_linear_ce_chunked": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _f32, _f32, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _sz, _vp]),

@@ -588,6 +588,11 @@ void foak_test_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns == 0 ? 
 
 void foak_test_skip_row_load(int64_t row) { g_skip_load_row.store(row < 0 ? -1 : row); }
 
+int32_t foak_test_gemm_group_schedule(const int64_t* mnk, int32_t n, int32_t pairs, int32_t* start, int32_t* ent,
+                                      int32_t ent_cap) {
+    return gemm_group_schedule(mnk, n, pairs, start, ent, ent_cap);
+}
+
 void foak_test_set_row_path(int32_t path) { g_row_path.store(path >= 1 && path <= 3 ? path : 0); }
 
 }  // extern "C"

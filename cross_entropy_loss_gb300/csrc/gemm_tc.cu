@@ -807,6 +807,25 @@ cudaError_t launch_gemm_bf16(const GemmDesc& d, cudaStream_t stream) {
     return launch_pair(p, std::min(units, max_pairs), stream);
 }
 
+int gemm_group_schedule(const int64_t* mnk, int n, int pairs, int32_t* start, int32_t* ent, int ent_cap) {
+    if (n < 1 || n > kGroupMax || pairs < 1 || !mnk || !start || !ent) return -1;
+    GemmParams ps[kGroupMax] = {};
+    int total = 0;
+    for (int q = 0; q < n; ++q) {
+        const int64_t M = mnk[3 * q], N = mnk[3 * q + 1], K = mnk[3 * q + 2];
+        if (M <= kBM || N <= 0 || K <= 0 || M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff) return -1;
+        ps[q].units_m = static_cast<int>((M + kBM - 1) / kBM + 1) / 2;
+        ps[q].tiles_n = static_cast<int>((N + kBN - 1) / kBN);
+        ps[q].K = static_cast<int>(K);
+        total += ps[q].units_m * ps[q].tiles_n;
+    }
+    if (total > ent_cap) return -1;
+    const Schedule s = build_schedule(ps, n, pairs);
+    for (size_t i = 0; i < s.start.size(); ++i) start[i] = s.start[i];
+    for (size_t i = 0; i < s.ent.size(); ++i) ent[i] = s.ent[i];
+    return s.clusters;
+}
+
 bool gemm_group_fits(const GemmDesc* d, int n) {
     int total = 0, live = 0;
     for (int i = 0; i < n; ++i) {

@@ -75,4 +75,8 @@ cudaError_t launch_gemm_bf16_group(const GemmDesc* d, int n, cudaStream_t stream
 // take a side job): every product on CTA pairs (M > 128), at most 8192 units.
 bool gemm_group_fits(const GemmDesc* d, int n);
 
+// The grouped launch's unit list for products of shapes mnk[3 q ..] on `pairs` SM
+// pairs (host only); returns the clusters used or -1.
+int gemm_group_schedule(const int64_t* mnk, int n, int pairs, int32_t* start, int32_t* ent, int ent_cap);
+
 }  // namespace foak

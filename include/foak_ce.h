@@ -481,6 +481,18 @@ void foak_test_skip_row_load(int64_t row);
  */
 void foak_test_set_row_path(int32_t path);
 
+/*
+ * Test hook (host only, no device work): the unit list foak_gemm_bf16_group would
+ * give products of these shapes on `pairs` SM pairs.
+ *   mnk      host int64[3 n]: M, N, K of each product (every M > 128), n in 1 .. 3
+ *   start    host int32[pairs + 1]: cluster c takes entries start[c] .. start[c+1] - 1
+ *   ent      host int32[ent_cap]: entries, product << 14 | output unit
+ * Returns the number of clusters used (<= pairs), or -1 for bad arguments or when
+ * ent_cap is too small.
+ */
+int32_t foak_test_gemm_group_schedule(const int64_t* mnk, int32_t n, int32_t pairs, int32_t* start, int32_t* ent,
+                                      int32_t ent_cap);
+
 #ifdef __cplusplus
 }
 #endif

@@ -232,3 +232,43 @@ def test_gemm_group_argument_errors(so):
     assert group(prob(K=-1)) == E.FOAK_ERR_INVALID_ARG
     assert group(n=0) == E.FOAK_OK
     assert group(prob(M=0), prob(N=0, ldo=0)) == E.FOAK_OK
+
+
+def _group_schedule(so, shapes, pairs, cap=20000):
+    mnk = (ctypes.c_int64 * (3 * len(shapes)))(*[v for s in shapes for v in s])
+    start = (ctypes.c_int32 * (pairs + 1))()
+    ent = (ctypes.c_int32 * cap)()
+    nc = so.lib.foak_test_gemm_group_schedule(mnk, len(shapes), pairs, start, ent, cap)
+    if nc < 0:
+        return nc, None, None
+    return nc, list(start[:nc + 1]), list(ent[:start[nc]])
+
+
+@pytest.mark.parametrize("shapes", [
+    [(1024, 32000, 4096), (1024, 4096, 32000)],                      # {Z(c), dH(c-2)}
+    [(1024, 32000, 4096), (1024, 4096, 32000), (32000, 4096, 4096)],  # ... with a group's dW
+    [(300, 700, 192), (512, 256, 4096)],                             # ragged shapes
+])
+def test_gemm_group_schedule_every_unit_once_longest_first_balanced(so, shapes):
+    """The grouped GEMM's unit list (host logic): each (product, 256 x 256 unit) exactly
+    once, every SM pair's list longest first, and the estimated work per pair (k-blocks
+    + 8 per unit) within 10% of the mean or one unit of the longest kind."""
+    pairs = 76
+    nc, start, ent = _group_schedule(so, shapes, pairs)
+    units = [((M + 127) // 128 + 1) // 2 * ((N + 255) // 256) for M, N, K in shapes]
+    cost = [(K + 63) // 64 + 8 for M, N, K in shapes]
+    assert nc == min(pairs, sum(units)) and start[0] == 0
+    assert sorted(ent) == sorted((q << 14) | u for q in range(len(shapes)) for u in range(units[q]))
+    loads = []
+    for c in range(nc):
+        mine = [cost[e >> 14] for e in ent[start[c]:start[c + 1]]]
+        assert mine == sorted(mine, reverse=True)
+        loads.append(sum(mine))
+    mean = sum(loads) / nc
+    assert max(loads) <= max(1.10 * mean, mean + max(cost))
+
+
+def test_gemm_group_schedule_argument_errors(so):
+    assert _group_schedule(so, [(128, 256, 64)], 76)[0] == -1        # single-CTA tiles
+    assert _group_schedule(so, [(1024, 32000, 4096)], 76, cap=10)[0] == -1
+    assert so.lib.foak_test_gemm_group_schedule(None, 1, 76, None, None, 0) == -1
