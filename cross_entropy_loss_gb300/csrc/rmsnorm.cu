@@ -253,16 +253,24 @@ __global__ void __launch_bounds__(1024) rmsnorm_bwd_fused_kernel(const char* __r
          row0 += static_cast<int64_t>(gridDim.x) * kFuseRows, par ^= 1) {
         uint4 xv[kFuseRows], dv[kFuseRows];  // kept packed: 8 registers per row
         float r[kFuseRows];
+        // every load of the batch first (the loads are ordered asm: a row's arithmetic
+        // placed between them would cost a round trip per row)
 #pragma unroll
         for (int q = 0; q < kFuseRows; ++q) {
             const int64_t row = row0 + q;
-            float dot = 0.f;
             r[q] = 0.f;
             xv[q] = dv[q] = make_uint4(0u, 0u, 0u, 0u);
             if (row < N && active) {
                 xv[q] = ld_global_v4(reinterpret_cast<const uint4*>(X + (row * ldx + static_cast<int64_t>(v) * EPV) * ES));
                 dv[q] = ld_global_v4(reinterpret_cast<const uint4*>(dY + (row * lddy + static_cast<int64_t>(v) * EPV) * ES));
                 r[q] = rstd[row];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kFuseRows; ++q) {
+            const int64_t row = row0 + q;
+            float dot = 0.f;
+            if (row < N && active) {
                 float fx[EPV], fd[EPV];
                 unpack<ES>(xv[q], fx);
                 unpack<ES>(dv[q], fd);

@@ -103,16 +103,17 @@ __global__ void __launch_bounds__(kRopeThreads) rope_apply_kernel(const RopeTens
         const int64_t th = w / per_head;
         const int h = static_cast<int>(th % H);
         const int64_t t = th / H;
+        // the data loads do not depend on the position: they go out with its load
+        char* lo_p = X + ((t * ldt) + static_cast<int64_t>(h) * d + static_cast<int64_t>(j) * EPV) * ES;
+        char* hi_p = lo_p + static_cast<int64_t>(half) * ES;
+        float lo[EPV], hi[EPV], c[EPV], s[EPV];
         const int64_t p = __ldg(positions + t);
+        ld8<ES>(lo_p, lo);
+        ld8<ES>(hi_p, hi);
         if (p < 0 || p >= P) {  // left untouched, flagged
             if (err && j == 0 && h == 0) atomicOr(reinterpret_cast<unsigned*>(err), FOAK_ERRBIT_LABEL_RANGE);
             continue;
         }
-        char* lo_p = X + ((t * ldt) + static_cast<int64_t>(h) * d + static_cast<int64_t>(j) * EPV) * ES;
-        char* hi_p = lo_p + static_cast<int64_t>(half) * ES;
-        float lo[EPV], hi[EPV], c[EPV], s[EPV];
-        ld8<ES>(lo_p, lo);
-        ld8<ES>(hi_p, hi);
         const float* cr = cos_t + p * half + j * EPV;
         const float* sr = sin_t + p * half + j * EPV;
 #pragma unroll
