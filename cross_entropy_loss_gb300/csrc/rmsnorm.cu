@@ -50,6 +50,13 @@ __device__ __forceinline__ void unpack(const uint4& v, float (&f)[16 / ES]) {
     }
 }
 
+__device__ __forceinline__ uint4 ldv(const char* p) { return ld_global_v4(reinterpret_cast<const uint4*>(p)); }
+
+// The loops below take four 16-byte vectors (or rows) at a time and issue all of their
+// loads before any arithmetic: the loads are ordered asm, so arithmetic placed between
+// them would cost a round trip per vector.  The arithmetic keeps the one-at-a-time order.
+constexpr int kBatch = 4;
+
 template <int ES>
 __device__ __forceinline__ void store8(char* p, const float (&f)[16 / ES]) {
     uint4 v;
@@ -77,24 +84,44 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const char* _
     for (int64_t row = blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); row < N; row += warps) {
         const char* x = X + row * ldx * ES;
         float ss = 0.f;
-#pragma unroll 4
-        for (int64_t v = lane; v < nvec; v += 32) {  // unrolled: several 16-byte loads in flight per lane
-            float f[EPV];
-            load8<ES>(x + v * 16, f);
+        for (int64_t v0 = lane; v0 < nvec; v0 += kBatch * 32) {
+            uint4 w[kBatch];
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) ss = fmaf(f[k], f[k], ss);
+            for (int u = 0; u < kBatch; ++u)
+                if (v0 + 32 * u < nvec) w[u] = ldv(x + (v0 + 32 * u) * 16);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (v0 + 32 * u < nvec) {
+                    float f[EPV];
+                    unpack<ES>(w[u], f);
+#pragma unroll
+                    for (int k = 0; k < EPV; ++k) ss = fmaf(f[k], f[k], ss);
+                }
+            }
         }
         ss = warp_sum(ss);
         const float r = rsqrtf(ss / static_cast<float>(D) + eps);
         char* y = Y + row * ldy * ES;
-#pragma unroll 4
-        for (int64_t v = lane; v < nvec; v += 32) {
-            float f[EPV], gm[EPV];
-            load8<ES>(x + v * 16, f);
-            load8<ES>(gamma + v * 16, gm);
+        for (int64_t v0 = lane; v0 < nvec; v0 += kBatch * 32) {
+            uint4 w[kBatch], gw[kBatch];
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) f[k] = f[k] * r * gm[k];
-            store8<ES>(y + v * 16, f);
+            for (int u = 0; u < kBatch; ++u) {
+                if (v0 + 32 * u < nvec) {
+                    w[u] = ldv(x + (v0 + 32 * u) * 16);
+                    gw[u] = ldv(gamma + (v0 + 32 * u) * 16);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (v0 + 32 * u < nvec) {
+                    float f[EPV], gm[EPV];
+                    unpack<ES>(w[u], f);
+                    unpack<ES>(gw[u], gm);
+#pragma unroll
+                    for (int k = 0; k < EPV; ++k) f[k] = f[k] * r * gm[k];
+                    store8<ES>(y + (v0 + 32 * u) * 16, f);
+                }
+            }
         }
         if (lane == 0 && rstd) rstd[row] = r;
     }
@@ -168,25 +195,56 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_bwd_kernel(const char* _
         const char* dy = dY + row * lddy * ES;
         const float r = rstd[row];
         float dot = 0.f;  // sum of xh * u over the row
-        for (int64_t v = lane; v < nvec; v += 32) {
-            float fx[EPV], fd[EPV], gm[EPV];
-            load8<ES>(x + v * 16, fx);
-            load8<ES>(dy + v * 16, fd);
-            load8<ES>(gamma + v * 16, gm);
+        for (int64_t v0 = lane; v0 < nvec; v0 += kBatch * 32) {
+            uint4 wx[kBatch], wd[kBatch], wg[kBatch];
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) dot = fmaf(fx[k] * r, gm[k] * fd[k], dot);
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t v = v0 + 32 * u;
+                if (v < nvec) {
+                    wx[u] = ldv(x + v * 16);
+                    wd[u] = ldv(dy + v * 16);
+                    wg[u] = ldv(gamma + v * 16);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (v0 + 32 * u < nvec) {
+                    float fx[EPV], fd[EPV], gm[EPV];
+                    unpack<ES>(wx[u], fx);
+                    unpack<ES>(wd[u], fd);
+                    unpack<ES>(wg[u], gm);
+#pragma unroll
+                    for (int k = 0; k < EPV; ++k) dot = fmaf(fx[k] * r, gm[k] * fd[k], dot);
+                }
+            }
         }
         dot = warp_sum(dot);
         const float m = dot / static_cast<float>(D);
         char* dx = dX + row * lddx * ES;
-        for (int64_t v = lane; v < nvec; v += 32) {
-            float fx[EPV], fd[EPV], gm[EPV], o[EPV];
-            load8<ES>(x + v * 16, fx);
-            load8<ES>(dy + v * 16, fd);
-            load8<ES>(gamma + v * 16, gm);
+        for (int64_t v0 = lane; v0 < nvec; v0 += kBatch * 32) {
+            uint4 wx[kBatch], wd[kBatch], wg[kBatch];
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) o[k] = r * (gm[k] * fd[k] - fx[k] * r * m);
-            store8<ES>(dx + v * 16, o);
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t v = v0 + 32 * u;
+                if (v < nvec) {
+                    wx[u] = ldv(x + v * 16);
+                    wd[u] = ldv(dy + v * 16);
+                    wg[u] = ldv(gamma + v * 16);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t v = v0 + 32 * u;
+                if (v < nvec) {
+                    float fx[EPV], fd[EPV], gm[EPV], o[EPV];
+                    unpack<ES>(wx[u], fx);
+                    unpack<ES>(wd[u], fd);
+                    unpack<ES>(wg[u], gm);
+#pragma unroll
+                    for (int k = 0; k < EPV; ++k) o[k] = r * (gm[k] * fd[k] - fx[k] * r * m);
+                    store8<ES>(dx + v * 16, o);
+                }
+            }
         }
     }
 }
@@ -206,14 +264,28 @@ __global__ void __launch_bounds__(kGammaThreads) rmsnorm_dgamma_kernel(const cha
     float acc[EPV];
 #pragma unroll
     for (int k = 0; k < EPV; ++k) acc[k] = 0.f;
-#pragma unroll 4
-    for (int64_t i = grp; i < N; i += G) {  // unrolled: several rows' loads in flight per thread
-        float fx[EPV], fd[EPV];
-        load8<ES>(X + (i * ldx + v * EPV) * ES, fx);
-        load8<ES>(dY + (i * lddy + v * EPV) * ES, fd);
-        const float r = rstd[i];
+    for (int64_t i0 = grp; i0 < N; i0 += kBatch * G) {
+        uint4 wx[kBatch], wd[kBatch];
+        float r[kBatch];
 #pragma unroll
-        for (int k = 0; k < EPV; ++k) acc[k] = fmaf(fd[k], fx[k] * r, acc[k]);
+        for (int u = 0; u < kBatch; ++u) {
+            const int64_t i = i0 + u * G;
+            if (i < N) {
+                wx[u] = ldv(X + (i * ldx + v * EPV) * ES);
+                wd[u] = ldv(dY + (i * lddy + v * EPV) * ES);
+                r[u] = rstd[i];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (i0 + u * G < N) {
+                float fx[EPV], fd[EPV];
+                unpack<ES>(wx[u], fx);
+                unpack<ES>(wd[u], fd);
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) acc[k] = fmaf(fd[k], fx[k] * r[u], acc[k]);
+            }
+        }
     }
     float* p = part + grp * D + v * EPV;
 #pragma unroll

@@ -126,3 +126,18 @@ def test_decoder_tail_full_size(cuda_lib):
     out = _run_tail(cuda_lib, c["X"], c["gamma"], c["W"], c["labels"], c["chunk"], eps=c["eps"])
     _check_tail(out, ref)
     assert out["n_valid"].item() == 8192 - 819 and out["err"].item() == 0
+
+
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
+def test_rmsnorm_backward_without_dgamma(cuda_lib, dtype):
+    """dX alone (no dgamma wanted) runs the warp-per-row backward."""
+    N, D = 301, 4096
+    X, gamma = _inputs(N, D, dtype, seed=17)
+    dY = wl.normal_matrix(N, D, seed=19, sigma=1.0, dtype=dtype, stream=wl.S_H)
+    ref_dx, _ = oracle.rmsnorm_backward(dY, X, gamma, 1e-5)
+    x, g = _dev(X, dtype), _dev(gamma, dtype)
+    _, rstd = cuda_lib.foak_rmsnorm_forward(x, g, eps=1e-5)
+    dx, dg = cuda_lib.foak_rmsnorm_backward(_dev(dY, dtype), x, g, rstd, want_dgamma=False)
+    torch.cuda.synchronize()
+    assert dg is None
+    assert _frob(to_f64(dx), ref_dx) < (4e-3 if dtype == wl.BF16 else 1e-5)
