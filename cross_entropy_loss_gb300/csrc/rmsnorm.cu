@@ -163,15 +163,23 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_reg_kernel(const cha
         const float r = rsqrtf(ss / static_cast<float>(D) + eps);
         char* y = Y + row * ldy * ES;
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int j = lane + 32 * i;
-            if (j < nvec) {
-                float f[EPV], gm[EPV];
-                unpack<ES>(v[i], f);
-                load8<ES>(gamma + static_cast<int64_t>(j) * 16, gm);
+        for (int i0 = 0; i0 < VPL; i0 += kBatch) {  // gamma's loads (L1) a batch at a time
+            uint4 gw[kBatch];
 #pragma unroll
-                for (int k = 0; k < EPV; ++k) f[k] = f[k] * r * gm[k];
-                store8<ES>(y + static_cast<int64_t>(j) * 16, f);
+            for (int u = 0; u < kBatch; ++u)
+                if (i0 + u < VPL && lane + 32 * (i0 + u) < nvec) gw[u] = ldv(gamma + static_cast<int64_t>(lane + 32 * (i0 + u)) * 16);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = i0 + u;
+                const int j = lane + 32 * i;
+                if (i < VPL && j < nvec) {
+                    float f[EPV], gm[EPV];
+                    unpack<ES>(v[i], f);
+                    unpack<ES>(gw[u], gm);
+#pragma unroll
+                    for (int k = 0; k < EPV; ++k) f[k] = f[k] * r * gm[k];
+                    store8<ES>(y + static_cast<int64_t>(j) * 16, f);
+                }
             }
         }
         if (lane == 0 && rstd) rstd[row] = r;
