@@ -380,6 +380,8 @@ def run_ours(args, rank, world, dist):
                        else "dp1",
         "l2": "inputs larger than L2: each timed step has its own 262 MB-class logits copy"
               + (" (ring reused: steps > ring)" if reused else ""),
+        # the rows whose label counts (ignored rows are in `value`, not here)
+        "valid_tokens_per_s": world * int(((main["labels"] >= 0) & (main["labels"] < main["V"])).sum()) / (ms * 1e-3),
         "hbm_GBps_algorithmic": achieved,
         "hbm_GBps_stated_2NVs": stated / (ms * 1e-3) / 1e9,
         "loss": loss, "err": err,
@@ -490,7 +492,9 @@ def secondary(ce, torch, dev, stream, upload, fused_timing, args):
         out.append({"key": name, "workload_key": f"{name}: N={cfg['logits'].shape[0]} V={cfg['V']}",
                     "path": "foak_ce_fwd_bwd", "kernel": _row_kernel(cfg)[0], "workload": WORKLOAD_DESC[name],
                     "steps": k, "ms_per_step": ms,
-                    "tokens_per_s": cfg["logits"].shape[0] / (ms * 1e-3), "GBps_algorithmic": gbs,
+                    "tokens_per_s": cfg["logits"].shape[0] / (ms * 1e-3),
+                    "valid_tokens_per_s": int(((cfg["labels"] >= 0) & (cfg["labels"] < cfg["V"])).sum()) / (ms * 1e-3),
+                    "GBps_algorithmic": gbs,
                     "GBps_stated_2NVs": _stated_bytes(cfg) / (ms * 1e-3) / 1e9, "frac": gbs / peak,
                     "peak": peak, "peak_source": peak_src, "loss": loss, "err": err,
                     "l2": "distinct logits buffers in turn (8 at most), each larger than L2"
