@@ -15,6 +15,7 @@
 // consecutive columns and one of 128 row groups, writes per-group partials, and a
 // last kernel sums the 128 partials in a fixed order -- deterministic, no atomics.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "foak_ce.h"
@@ -300,7 +301,8 @@ __global__ void __launch_bounds__(kGammaThreads) rmsnorm_dgamma_kernel(const cha
     for (int k = 0; k < EPV; ++k) p[k] = acc[k];
 }
 
-// Backward in one pass over dY and X, for rows of at most 1024 vectors: thread v
+// Backward in one pass over dY and X, for rows of 513 to 1024 vectors (shorter rows
+// take the ring kernel below): thread v
 // owns column vector v of every row; a CTA takes kFuseRows rows at a time, reduces
 // their sums of xh * u in one round (warp shuffles, one barrier; the buffer is
 // double-buffered by batch parity), writes dX from registers and keeps its
@@ -385,11 +387,200 @@ __global__ void __launch_bounds__(1024) rmsnorm_bwd_fused_kernel(const char* __r
     }
 }
 
-// dgamma[j] = sum of part[g][j] over g < G, in a fixed order: 32 slices of 32
-// columns per CTA, slice sl summing g = sl, sl + 32, ... (four interleaved running
-// sums), then slice 0 adding the 32 slice sums in slice order.  (8 slices of 64
-// columns, 64 CTAs for D = 4096, took 7.8 us: each thread walked ~38 partials.)
-constexpr int kRedCols = 32, kRedSlices = 32;
+// 16-byte copy global -> shared by this thread, completed by its own wait_group
+// (a hardware wait, no spin): the pre-bulk asynchronous copy, used here because every
+// thread reads back exactly the vectors it copied.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int PENDING>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
+}
+
+// The one-pass backward with the rows streamed through a shared-memory ring: thread v
+// owns column vectors v, v + threads, ... (VPT of them), each CTA takes one contiguous
+// range of rows in batches of RR, and every thread copies its own vectors of X and dY
+// for the batch kRingStages - 1 ahead of the one it works on, so copies stay in flight
+// through each batch's reduction barrier.  Per row, with u = gamma * dY and s = sum_j x_j u_j:
+//     m = r s / D,   dX = r u - (r m) (x r),   dgamma += dY (x r)
+// (r factored out of the row sum), on element pairs with the two-wide FP32
+// instructions (each half rounded as the scalar operation): the kernel is bound by
+// instruction issue before it is by memory.
+constexpr int kRingStages = 3;
+constexpr int kRingSmemMax = 220 * 1024;
+constexpr int kRingRows = 2;        // rows per batch (one barrier each)
+constexpr int kRingVpt = 2;         // 16-byte column vectors per thread
+constexpr int kRingMaxThreads = 256;  // rows of up to 4096 bf16 / 2048 fp32 elements
+constexpr int kRingMinBlocks = 2;   // two CTAs per SM at 4096 bf16 (96 KB of ring each)
+
+__host__ __device__ constexpr size_t ring_stage_bytes(int rows, int vpt, int threads) {
+    return static_cast<size_t>(rows) * 2 * vpt * static_cast<size_t>(threads) * 16;
+}
+static_assert(kRingStages * ring_stage_bytes(kRingRows, kRingVpt, kRingMaxThreads) <= static_cast<size_t>(kRingSmemMax),
+              "ring too large");
+
+// A 16-byte vector as element pairs, and back (bf16 rounded to nearest even).
+template <int ES>
+__device__ __forceinline__ void unpack_pairs(const uint4& w, float2 (&p)[8 / ES]) {
+    if constexpr (ES == 2) {
+        p[0] = make_float2(bf16_lo(w.x), bf16_hi(w.x));
+        p[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
+        p[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
+        p[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
+    } else {
+        p[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+        p[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+    }
+}
+
+template <int ES>
+__device__ __forceinline__ void store_pairs(char* dst, const float2 (&p)[8 / ES]) {
+    uint4 w;
+    if constexpr (ES == 2) {
+        w = make_uint4(pack_bf16x2(p[0].x, p[0].y), pack_bf16x2(p[1].x, p[1].y), pack_bf16x2(p[2].x, p[2].y),
+                       pack_bf16x2(p[3].x, p[3].y));
+    } else {
+        w = make_uint4(__float_as_uint(p[0].x), __float_as_uint(p[0].y), __float_as_uint(p[1].x),
+                       __float_as_uint(p[1].y));
+    }
+    *reinterpret_cast<uint4*>(dst) = w;
+}
+
+template <int ES, int RR, int VPT>
+__global__ void __launch_bounds__(kRingMaxThreads, kRingMinBlocks)
+    rmsnorm_bwd_ring_kernel(const char* __restrict__ dY, int64_t lddy, const char* __restrict__ X, int64_t ldx,
+                            const char* __restrict__ gamma, const float* __restrict__ rstd, int64_t N, int64_t D,
+                            char* __restrict__ dX, int64_t lddx, float* __restrict__ part) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
+    constexpr int EPV = 16 / ES, NP = EPV / 2;
+    extern __shared__ uint4 ring[];  // [kRingStages][RR][X, dY][VPT][threads]
+    __shared__ float red[2][RR][32];
+    const int v = threadIdx.x, lane = v & 31, warp = v >> 5, nt = blockDim.x, warps = nt >> 5;
+    bool act[VPT];  // thread v owns column vectors v, v + nt, ...
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) act[j] = static_cast<int64_t>(v + j * nt) * EPV < D;
+    const int64_t G = gridDim.x;
+    const int64_t r_begin = N * static_cast<int64_t>(blockIdx.x) / G;
+    const int64_t r_end = N * (static_cast<int64_t>(blockIdx.x) + 1) / G;
+    const int64_t nb = (r_end - r_begin + RR - 1) / RR;
+    const float inv_d = 1.f / static_cast<float>(D);
+    // batch b's copies into slot b % kRingStages, one commit group per batch (empty
+    // past the last batch, so that the group count stays in step)
+    auto issue = [&](int64_t b) {
+        if (b < nb) {
+            uint4* slot = ring + static_cast<size_t>(b % kRingStages) * (RR * 2 * VPT) * nt;
+#pragma unroll
+            for (int q = 0; q < RR; ++q) {
+                const int64_t row = r_begin + b * RR + q;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    if (row < r_end && act[j]) {
+                        const int64_t col = static_cast<int64_t>(v + j * nt) * EPV;
+                        cp_async16(slot + ((2 * q) * VPT + j) * nt + v, X + (row * ldx + col) * ES);
+                        cp_async16(slot + ((2 * q + 1) * VPT + j) * nt + v, dY + (row * lddy + col) * ES);
+                    }
+                }
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int s = 0; s < kRingStages - 1; ++s) issue(s);
+    float2 gm2[VPT][NP], acc2[VPT][NP];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        unpack_pairs<ES>(act[j] ? ldv(gamma + static_cast<int64_t>(v + j * nt) * 16) : make_uint4(0u, 0u, 0u, 0u),
+                         gm2[j]);
+#pragma unroll
+        for (int k = 0; k < NP; ++k) acc2[j][k] = make_float2(0.f, 0.f);
+    }
+    float rn[RR];
+#pragma unroll
+    for (int q = 0; q < RR; ++q) rn[q] = r_begin + q < r_end ? rstd[r_begin + q] : 0.f;
+    int par = 0;
+    for (int64_t b = 0; b < nb; ++b, par ^= 1) {
+        // the slot of batch b - 1, read before the last barrier, takes batch b + kRingStages - 1
+        issue(b + kRingStages - 1);
+        const int64_t row0 = r_begin + b * RR;
+        float r[RR];
+#pragma unroll
+        for (int q = 0; q < RR; ++q) {
+            r[q] = rn[q];
+            const int64_t nxt = row0 + RR + q;
+            rn[q] = nxt < r_end ? rstd[nxt] : 0.f;
+        }
+        cp_async_wait<kRingStages - 1>();  // this thread's copies of batch b have landed
+        const uint4* slot = ring + static_cast<size_t>(b % kRingStages) * (RR * 2 * VPT) * nt;
+        // the batch is read from the ring twice, before and after the barrier (nothing
+        // held through it; the slot is refilled only in the next round)
+#pragma unroll
+        for (int q = 0; q < RR; ++q) {
+            float2 d2 = make_float2(0.f, 0.f);
+            if (row0 + q < r_end) {
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    if (act[j]) {
+                        float2 x[NP], d[NP];
+                        unpack_pairs<ES>(slot[((2 * q) * VPT + j) * nt + v], x);
+                        unpack_pairs<ES>(slot[((2 * q + 1) * VPT + j) * nt + v], d);
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) d2 = __ffma2_rn(x[k], __fmul2_rn(gm2[j][k], d[k]), d2);
+                    }
+                }
+            }
+            const float dot = warp_sum(d2.x + d2.y);
+            if (lane == 0) red[par][q][warp] = dot;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < RR; ++q) {
+            const int64_t row = row0 + q;
+            const float s = warp_sum(lane < warps ? red[par][q][lane] : 0.f);
+            if (row < r_end) {
+                const float rm = r[q] * (r[q] * s * inv_d);
+                const float2 r2 = make_float2(r[q], r[q]), nrm2 = make_float2(-rm, -rm);
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    if (act[j]) {
+                        float2 x[NP], d[NP], o[NP];
+                        unpack_pairs<ES>(slot[((2 * q) * VPT + j) * nt + v], x);
+                        unpack_pairs<ES>(slot[((2 * q + 1) * VPT + j) * nt + v], d);
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) {
+                            const float2 xh = __fmul2_rn(x[k], r2);
+                            o[k] = __ffma2_rn(nrm2, xh, __fmul2_rn(r2, __fmul2_rn(gm2[j][k], d[k])));
+                            acc2[j][k] = __ffma2_rn(d[k], xh, acc2[j][k]);
+                        }
+                        store_pairs<ES>(dX + (row * lddx + static_cast<int64_t>(v + j * nt) * EPV) * ES, o);
+                    }
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();  // no copy outlives the CTA (the trailing groups are empty)
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        if (act[j]) {
+            float* p = part + static_cast<int64_t>(blockIdx.x) * D + static_cast<int64_t>(v + j * nt) * EPV;
+#pragma unroll
+            for (int k = 0; k < NP; ++k) {
+                p[2 * k] = acc2[j][k].x;
+                p[2 * k + 1] = acc2[j][k].y;
+            }
+        }
+    }
+}
+
+// dgamma[j] = sum of part[g][j] over g < G (G <= kRedMaxG for every caller), in a
+// fixed order: 32 slices of 32 columns per CTA, slice sl loading g = sl, sl + 32, ...
+// all at once (one round trip) and adding them in g order, then slice 0 adding the 32
+// slice sums in slice order.  (Four running sums walked in rounds of four loads took
+// 4.9 us for 304 partials of 4096; 8 slices of 64 columns took 7.8 us.)
+constexpr int kRedCols = 32, kRedSlices = 32, kRedMaxG = 512;
+static_assert(kFuseMaxGrid <= kRedMaxG && kRmsGammaGroups <= kRedMaxG, "partials beyond the reduce's reach");
 __global__ void __launch_bounds__(kRedCols * kRedSlices) rmsnorm_dgamma_reduce(const float* __restrict__ part, int G,
                                                                              int64_t D, float* __restrict__ dgamma) {
     griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
@@ -397,18 +588,18 @@ __global__ void __launch_bounds__(kRedCols * kRedSlices) rmsnorm_dgamma_reduce(c
     __shared__ float ss[kRedSlices][kRedCols];
     const int c = threadIdx.x % kRedCols, sl = threadIdx.x / kRedCols;
     const int64_t j = static_cast<int64_t>(blockIdx.x) * kRedCols + c;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float s = 0.f;
     if (j < D) {
-        int g = sl;
-        for (; g + 3 * kRedSlices < G; g += 4 * kRedSlices) {
-            s0 += part[static_cast<int64_t>(g) * D + j];
-            s1 += part[static_cast<int64_t>(g + kRedSlices) * D + j];
-            s2 += part[static_cast<int64_t>(g + 2 * kRedSlices) * D + j];
-            s3 += part[static_cast<int64_t>(g + 3 * kRedSlices) * D + j];
+        float val[kRedMaxG / kRedSlices];
+#pragma unroll
+        for (int i = 0; i < kRedMaxG / kRedSlices; ++i) {
+            const int g = sl + i * kRedSlices;
+            val[i] = g < G ? part[static_cast<int64_t>(g) * D + j] : 0.f;
         }
-        for (; g < G; g += kRedSlices) s0 += part[static_cast<int64_t>(g) * D + j];
+#pragma unroll
+        for (int i = 0; i < kRedMaxG / kRedSlices; ++i) s += val[i];
     }
-    ss[sl][c] = (s0 + s1) + (s2 + s3);
+    ss[sl][c] = s;
     __syncthreads();
     if (sl == 0 && j < D) {
         float t = 0.f;
@@ -422,6 +613,26 @@ int norm_grid(int64_t N) {
     const int64_t rows_per_cta = kNormThreads / 32;
     const int64_t want = (N + rows_per_cta - 1) / rows_per_cta;
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(device_sm_count()) * 8)));
+}
+
+std::mutex g_ring_mu;
+bool g_ring_attr[64][2] = {};
+
+// The ring kernel's shared memory limit, set once per device and element size.
+template <int ES>
+cudaError_t ring_attr() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_ring_mu);
+    if (!g_ring_attr[dev][ES == 2 ? 0 : 1]) {
+        e = cudaFuncSetAttribute(rmsnorm_bwd_ring_kernel<ES, kRingRows, kRingVpt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kRingSmemMax);
+        if (e != cudaSuccess) return e;
+        g_ring_attr[dev][ES == 2 ? 0 : 1] = true;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -456,8 +667,27 @@ cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void*
     const dim3 rgrid(static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols))),
         rblock(kRedCols * kRedSlices);
     cudaError_t e = cudaSuccess;
+    const int ring_threads = static_cast<int>(((nvec + kRingVpt - 1) / kRingVpt + 31) / 32 * 32);
+    const size_t ring_smem = kRingStages * ring_stage_bytes(kRingRows, kRingVpt, ring_threads);
+    if (dgamma && N > 0 && ring_threads <= kRingMaxThreads) {
+        // one pass through the shared-memory ring: as many CTAs per SM as its shared
+        // memory and threads allow, each with a contiguous range of rows
+        e = es == 2 ? ring_attr<2>() : ring_attr<4>();
+        if (e != cudaSuccess) return e;
+        const int64_t per_sm = std::max<int64_t>(
+            1, std::min<int64_t>(2048 / ring_threads, static_cast<int64_t>(227 * 1024) / static_cast<int64_t>(ring_smem + 1024)));
+        const int grid = static_cast<int>(
+            std::min<int64_t>({N, static_cast<int64_t>(device_sm_count()) * per_sm, kFuseMaxGrid}));
+        const dim3 block(static_cast<unsigned>(ring_threads));
+        e = es == 2 ? launch_dependent(rmsnorm_bwd_ring_kernel<2, kRingRows, kRingVpt>, dim3(grid), block, ring_smem, s, dy, lddy,
+                                       x, ldx, g, rstd, N, D, dx, lddx, part)
+                    : launch_dependent(rmsnorm_bwd_ring_kernel<4, kRingRows, kRingVpt>, dim3(grid), block, ring_smem, s, dy, lddy,
+                                       x, ldx, g, rstd, N, D, dx, lddx, part);
+        if (e != cudaSuccess) return e;
+        return launch_dependent(rmsnorm_dgamma_reduce, rgrid, rblock, 0, s, part, grid, D, dgamma);
+    }
     if (dgamma && N > 0 && nvec <= 1024) {
-        // one pass: dX and the dgamma partials of each CTA, then the fixed-order reduce
+        // longer rows in one pass: dX and the dgamma partials of each CTA, then the reduce
         const dim3 block(static_cast<unsigned>((nvec + 31) / 32 * 32));
         const int grid = static_cast<int>(std::min<int64_t>(
             {(N + kFuseRows - 1) / kFuseRows, static_cast<int64_t>(device_sm_count()) * 2, kFuseMaxGrid}));
