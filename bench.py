@@ -578,6 +578,31 @@ def chunked_timing(ce, torch, dev, stream, steps=10, warmup=3):
         e1.synchronize()
         return e0.elapsed_time(e1) / k
 
+    def timed_graph(fn, k, w):
+        """k calls captured in one CUDA graph, replayed once: the kernels' time without the
+        host's per-call issue cost (a binding call costs ~15-20 us of Python, close to
+        these kernels' own time)."""
+        for _ in range(w):
+            fn()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(graph):
+                for _ in range(k):
+                    fn()
+        except RuntimeError as exc:  # no capture here: say so and time the calls eagerly
+            print(f"graph capture failed ({exc}); timing eagerly", file=sys.stderr)
+            return timed(fn, k, 0), "eager (graph capture failed)"
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+        del graph
+        return e0.elapsed_time(e1) / k, f"CUDA graph of {k} calls (host issue cost excluded)"
+
     ms = timed(lambda: ce.foak_linear_ce_chunked(H, W, y, chunk=chunk, dH=dH, dW=dW), steps, warmup)
     out = ce.foak_linear_ce_chunked(H, W, y, chunk=chunk, dH=dH, dW=dW)
     flops = 6.0 * N * V * D
@@ -605,14 +630,18 @@ def chunked_timing(ce, torch, dev, stream, steps=10, warmup=3):
     hbm, hsrc = _peak_hbm()
     Y = torch.empty_like(X)
     _, rstd = ce.foak_rmsnorm_forward(X, gam, eps=t["eps"], Y=Y)
-    ms_f = timed(lambda: ce.foak_rmsnorm_forward(X, gam, eps=t["eps"], Y=Y), 20, 3)
-    ms_b = timed(lambda: ce.foak_rmsnorm_backward(Y, X, gam, rstd, dX=dX), 20, 3)
+    fwd = lambda: ce.foak_rmsnorm_forward(X, gam, eps=t["eps"], Y=Y)
+    bwd = lambda: ce.foak_rmsnorm_backward(Y, X, gam, rstd, dX=dX)
+    (ms_f, how_f), ms_fe = timed_graph(fwd, 20, 3), timed(fwd, 20, 3)
+    (ms_b, how_b), ms_be = timed_graph(bwd, 20, 3), timed(bwd, 20, 3)
     nd2 = N * D * 2
-    for name, ms_k, byts in (("foak_rmsnorm_forward", ms_f, 2 * nd2 + 4 * N),
-                             ("foak_rmsnorm_backward (dX and dgamma)", ms_b, 3 * nd2 + 4 * N)):
+    for name, ms_k, how, ms_e, byts in (("foak_rmsnorm_forward", ms_f, how_f, ms_fe, 2 * nd2 + 4 * N),
+                                        ("foak_rmsnorm_backward (dX and dgamma)", ms_b, how_b, ms_be,
+                                         3 * nd2 + 4 * N)):
         gbs = byts / (ms_k * 1e-3) / 1e9
         res.append({"path": name, "workload": "X 8192x4096 bf16 (the decoder tail's norm)", "steps": 20,
-                    "ms_per_step": ms_k, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm,
+                    "ms_per_step": ms_k, "timing": how,
+                    "ms_per_step_eager": ms_e, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm,
                     "peak_source": hsrc,
                     "bytes": "forward: read X, write Y; backward (one pass): read dY and X, write dX"})
     del X, dX, Y
@@ -626,11 +655,12 @@ def chunked_timing(ce, torch, dev, stream, steps=10, warmup=3):
     def rope_step():
         ce.foak_rope_apply_qk(q, k, pos, cache)
 
-    ms_r = timed(rope_step, 20, 3)
+    (ms_r, how_r), ms_re = timed_graph(rope_step, 20, 3), timed(rope_step, 20, 3)
     byts = 2 * (q.numel() + k.numel()) * 2 + 8 * pos.numel()
     gbs = byts / (ms_r * 1e-3) / 1e9
     res.append({"path": "foak_rope_apply_qk (Q and K in one launch, in place)", "workload": ROPE_DESC, "steps": 20,
-                "ms_per_step": ms_r, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm, "peak_source": hsrc,
+                "ms_per_step": ms_r, "timing": how_r,
+                "ms_per_step_eager": ms_re, "GBps_algorithmic": gbs, "frac": gbs / hbm, "peak": hbm, "peak_source": hsrc,
                 "bytes": "Q and K read and written once, positions; the 4 MB cos/sin table stays in L2"})
     del q, k, cache
     # the products of the call at the shapes it runs them: a chunk's logits product and the
