@@ -56,7 +56,7 @@ def test_rmsnorm_forward(cuda_lib, dtype, N, D, ld):
 
 
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
-@pytest.mark.parametrize("N,D", [(1, 8), (77, 4096), (1024, 1000), (300, 8192), (2000, 4096), (1500, 2304), (9, 64)])
+@pytest.mark.parametrize("N,D", [(1, 8), (77, 4096), (1024, 1000), (300, 8192), (2000, 4096), (1500, 2304), (9, 64), (611, 2048)])
 def test_rmsnorm_backward(cuda_lib, dtype, N, D):
     X, gamma = _inputs(N, D, dtype, seed=3 * N + D)
     dY = wl.normal_matrix(N, D, seed=N + 7, sigma=1.0, dtype=dtype, stream=wl.S_H)
