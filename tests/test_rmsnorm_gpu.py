@@ -69,6 +69,23 @@ def test_rmsnorm_backward(cuda_lib, dtype, N, D):
     assert _frob(to_f64(dg), ref_dg) < (1e-4 if dtype == wl.BF16 else 1e-5)
 
 
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
+def test_rmsnorm_backward_padded_rows(cuda_lib, dtype):
+    """dY, X and dX as views of wider row-major buffers (three different row strides)."""
+    N, D = 700, 1024
+    X, gamma = _inputs(N, D, dtype, seed=41, ld=D + 24)
+    dY = wl.normal_matrix(N, D, seed=43, sigma=1.0, dtype=dtype, ld=D + 8, stream=wl.S_H)
+    ref_dx, ref_dg = oracle.rmsnorm_backward(dY[:, :D], X[:, :D], gamma, 1e-5)
+    x, g = _dev(X, dtype)[:, :D], _dev(gamma, dtype)
+    _, rstd = cuda_lib.foak_rmsnorm_forward(x, g, eps=1e-5)
+    dx_buf = torch.full((N, D + 40), 7.0, device="cuda").to(x.dtype)
+    dx, dg = cuda_lib.foak_rmsnorm_backward(_dev(dY, dtype)[:, :D], x, g, rstd, dX=dx_buf[:, :D])
+    torch.cuda.synchronize()
+    assert _frob(to_f64(dx), ref_dx) < (4e-3 if dtype == wl.BF16 else 1e-5)
+    assert _frob(to_f64(dg), ref_dg) < (1e-4 if dtype == wl.BF16 else 1e-5)
+    assert bool((dx_buf[:, D:] == 7.0).all()), "a write past the rows' D elements"
+
+
 def test_rmsnorm_backward_empty_batch_zero_dgamma(cuda_lib):
     x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
     g = torch.ones(64, dtype=torch.bfloat16, device="cuda")
