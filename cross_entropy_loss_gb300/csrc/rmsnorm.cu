@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kRingMaxThreads, kRingMinBlocks)
         cp_async_wait<kRingStages - 1>();  // this thread's copies of batch b have landed
         const uint4* slot = ring + static_cast<size_t>(b % kRingStages) * (RR * 2 * VPT) * nt;
         // the batch is read from the ring twice, before and after the barrier (nothing
-        // held through it; the slot is refilled only in the next round)
+        // held through it; the slot is refilled only in the next iteration)
 #pragma unroll
         for (int q = 0; q < RR; ++q) {
             float2 d2 = make_float2(0.f, 0.f);
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kRingMaxThreads, kRingMinBlocks)
 // dgamma[j] = sum of part[g][j] over g < G (G <= kRedMaxG for every caller), in a
 // fixed order: 32 slices of 32 columns per CTA, slice sl loading g = sl, sl + 32, ...
 // all at once (one round trip) and adding them in g order, then slice 0 adding the 32
-// slice sums in slice order.  (Four running sums walked in rounds of four loads took
+// slice sums in slice order.  (Four running sums fed four loads at a time took
 // 4.9 us for 304 partials of 4096; 8 slices of 64 columns took 7.8 us.)
 constexpr int kRedCols = 32, kRedSlices = 32, kRedMaxG = 512;
 static_assert(kFuseMaxGrid <= kRedMaxG && kRmsGammaGroups <= kRedMaxG, "partials beyond the reduce's reach");
