@@ -301,91 +301,8 @@ __global__ void __launch_bounds__(kGammaThreads) rmsnorm_dgamma_kernel(const cha
     for (int k = 0; k < EPV; ++k) p[k] = acc[k];
 }
 
-// Backward in one pass over dY and X, for rows of 513 to 1024 vectors (shorter rows
-// take the ring kernel below): thread v
-// owns column vector v of every row; a CTA takes kFuseRows rows at a time, reduces
-// their sums of xh * u in one round (warp shuffles, one barrier; the buffer is
-// double-buffered by batch parity), writes dX from registers and keeps its
-// columns' dgamma sums in registers; each CTA writes one partial row at the end.
-constexpr int kFuseRows = 4;
-constexpr int kFuseMaxGrid = 512;
-
-template <int ES>
-__global__ void __launch_bounds__(1024) rmsnorm_bwd_fused_kernel(const char* __restrict__ dY, int64_t lddy,
-                                                                 const char* __restrict__ X, int64_t ldx,
-                                                                 const char* __restrict__ gamma,
-                                                                 const float* __restrict__ rstd, int64_t N,
-                                                                 int64_t D, char* __restrict__ dX, int64_t lddx,
-                                                                 float* __restrict__ part) {
-    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
-    griddep_wait();
-    constexpr int EPV = 16 / ES;
-    __shared__ float red[2][kFuseRows][32];
-    const int v = threadIdx.x, lane = v & 31, warp = v >> 5, warps = blockDim.x >> 5;
-    const bool active = static_cast<int64_t>(v) * EPV < D;
-    float gm[EPV], acc[EPV];
-#pragma unroll
-    for (int k = 0; k < EPV; ++k) {
-        gm[k] = 0.f;
-        acc[k] = 0.f;
-    }
-    if (active) load8<ES>(gamma + static_cast<int64_t>(v) * 16, gm);
-    int par = 0;
-    for (int64_t row0 = static_cast<int64_t>(blockIdx.x) * kFuseRows; row0 < N;
-         row0 += static_cast<int64_t>(gridDim.x) * kFuseRows, par ^= 1) {
-        uint4 xv[kFuseRows], dv[kFuseRows];  // kept packed: 8 registers per row
-        float r[kFuseRows];
-        // every load of the batch first (the loads are ordered asm: a row's arithmetic
-        // placed between them would cost a round trip per row)
-#pragma unroll
-        for (int q = 0; q < kFuseRows; ++q) {
-            const int64_t row = row0 + q;
-            r[q] = 0.f;
-            xv[q] = dv[q] = make_uint4(0u, 0u, 0u, 0u);
-            if (row < N && active) {
-                xv[q] = ld_global_v4(reinterpret_cast<const uint4*>(X + (row * ldx + static_cast<int64_t>(v) * EPV) * ES));
-                dv[q] = ld_global_v4(reinterpret_cast<const uint4*>(dY + (row * lddy + static_cast<int64_t>(v) * EPV) * ES));
-                r[q] = rstd[row];
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < kFuseRows; ++q) {
-            const int64_t row = row0 + q;
-            float dot = 0.f;
-            if (row < N && active) {
-                float fx[EPV], fd[EPV];
-                unpack<ES>(xv[q], fx);
-                unpack<ES>(dv[q], fd);
-#pragma unroll
-                for (int k = 0; k < EPV; ++k) dot = fmaf(fx[k] * r[q], gm[k] * fd[k], dot);
-            }
-            dot = warp_sum(dot);
-            if (lane == 0) red[par][q][warp] = dot;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int q = 0; q < kFuseRows; ++q) {
-            const int64_t row = row0 + q;
-            const float m = warp_sum(lane < warps ? red[par][q][lane] : 0.f) / static_cast<float>(D);
-            if (row < N && active) {
-                float fx[EPV], fd[EPV], o[EPV];
-                unpack<ES>(xv[q], fx);
-                unpack<ES>(dv[q], fd);
-#pragma unroll
-                for (int k = 0; k < EPV; ++k) {
-                    o[k] = r[q] * (gm[k] * fd[k] - fx[k] * r[q] * m);
-                    acc[k] = fmaf(fd[k], fx[k] * r[q], acc[k]);
-                }
-                store8<ES>(dX + (row * lddx + static_cast<int64_t>(v) * EPV) * ES, o);
-            }
-        }
-    }
-    if (active) {
-        float* p = part + static_cast<int64_t>(blockIdx.x) * D + static_cast<int64_t>(v) * EPV;
-#pragma unroll
-        for (int k = 0; k < EPV; ++k) p[k] = acc[k];
-    }
-}
+// At most this many CTAs write dgamma partials (the workspace holds 512 x D floats).
+constexpr int kPartMaxGrid = 512;
 
 // 16-byte copy global -> shared by this thread, completed by its own wait_group
 // (a hardware wait, no spin): the pre-bulk asynchronous copy, used here because every
@@ -411,14 +328,17 @@ __device__ __forceinline__ void cp_async_wait() {
 constexpr int kRingStages = 3;
 constexpr int kRingSmemMax = 220 * 1024;
 constexpr int kRingRows = 2;        // rows per batch (one barrier each)
-constexpr int kRingVpt = 2;         // 16-byte column vectors per thread
-constexpr int kRingMaxThreads = 256;  // rows of up to 4096 bf16 / 2048 fp32 elements
-constexpr int kRingMinBlocks = 2;   // two CTAs per SM at 4096 bf16 (96 KB of ring each)
+constexpr int kRingVpt = 2;         // 16-byte column vectors per thread, rows of <= 512 vectors
+constexpr int kRingVptWide = 4;     // the same for rows of 513 to 1024 vectors
+constexpr int kRingMaxThreads = 256;  // rows of up to 8192 bf16 / 4096 fp32 elements
+// two CTAs per SM at 4096 bf16 (96 KB of ring each), one for the wide rows (192 KB)
+constexpr int ring_min_blocks(int vpt) { return vpt <= 2 ? 2 : 1; }
 
 __host__ __device__ constexpr size_t ring_stage_bytes(int rows, int vpt, int threads) {
     return static_cast<size_t>(rows) * 2 * vpt * static_cast<size_t>(threads) * 16;
 }
-static_assert(kRingStages * ring_stage_bytes(kRingRows, kRingVpt, kRingMaxThreads) <= static_cast<size_t>(kRingSmemMax),
+static_assert(kRingStages * ring_stage_bytes(kRingRows, kRingVptWide, kRingMaxThreads) <=
+                  static_cast<size_t>(kRingSmemMax),
               "ring too large");
 
 // A 16-byte vector as element pairs, and back (bf16 rounded to nearest even).
@@ -449,7 +369,7 @@ __device__ __forceinline__ void store_pairs(char* dst, const float2 (&p)[8 / ES]
 }
 
 template <int ES, int RR, int VPT>
-__global__ void __launch_bounds__(kRingMaxThreads, kRingMinBlocks)
+__global__ void __launch_bounds__(kRingMaxThreads, ring_min_blocks(VPT))
     rmsnorm_bwd_ring_kernel(const char* __restrict__ dY, int64_t lddy, const char* __restrict__ X, int64_t ldx,
                             const char* __restrict__ gamma, const float* __restrict__ rstd, int64_t N, int64_t D,
                             char* __restrict__ dX, int64_t lddx, float* __restrict__ part) {
@@ -580,7 +500,7 @@ __global__ void __launch_bounds__(kRingMaxThreads, kRingMinBlocks)
 // slice sums in slice order.  (Four running sums fed four loads at a time took
 // 4.9 us for 304 partials of 4096; 8 slices of 64 columns took 7.8 us.)
 constexpr int kRedCols = 32, kRedSlices = 32, kRedMaxG = 512;
-static_assert(kFuseMaxGrid <= kRedMaxG && kRmsGammaGroups <= kRedMaxG, "partials beyond the reduce's reach");
+static_assert(kPartMaxGrid <= kRedMaxG && kRmsGammaGroups <= kRedMaxG, "partials beyond the reduce's reach");
 __global__ void __launch_bounds__(kRedCols * kRedSlices) rmsnorm_dgamma_reduce(const float* __restrict__ part, int G,
                                                                              int64_t D, float* __restrict__ dgamma) {
     griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
@@ -616,23 +536,46 @@ int norm_grid(int64_t N) {
 }
 
 std::mutex g_ring_mu;
-bool g_ring_attr[64][2] = {};
+bool g_ring_attr[64][4] = {};
 
-// The ring kernel's shared memory limit, set once per device and element size.
-template <int ES>
+// The ring kernel's shared memory limit, set once per device, element size and width.
+template <int ES, int VPT>
 cudaError_t ring_attr() {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int k = (ES == 2 ? 0 : 2) + (VPT == kRingVpt ? 0 : 1);
     std::lock_guard<std::mutex> lock(g_ring_mu);
-    if (!g_ring_attr[dev][ES == 2 ? 0 : 1]) {
-        e = cudaFuncSetAttribute(rmsnorm_bwd_ring_kernel<ES, kRingRows, kRingVpt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kRingSmemMax);
+    if (!g_ring_attr[dev][k]) {
+        e = cudaFuncSetAttribute(rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemMax);
         if (e != cudaSuccess) return e;
-        g_ring_attr[dev][ES == 2 ? 0 : 1] = true;
+        g_ring_attr[dev][k] = true;
     }
     return cudaSuccess;
+}
+
+// The one-pass backward through the shared-memory ring: as many CTAs per SM as its
+// shared memory and threads allow, each with a contiguous range of rows; then the
+// fixed-order dgamma reduce over the CTAs' partials.
+template <int ES, int VPT>
+cudaError_t launch_bwd_ring(const char* dy, int64_t lddy, const char* x, int64_t ldx, const char* g, const float* rstd,
+                            int64_t N, int64_t D, char* dx, int64_t lddx, float* part, float* dgamma, cudaStream_t s) {
+    const int64_t nvec = D / (16 / ES);
+    const int threads = static_cast<int>(((nvec + VPT - 1) / VPT + 31) / 32 * 32);
+    const size_t smem = kRingStages * ring_stage_bytes(kRingRows, VPT, threads);
+    cudaError_t e = ring_attr<ES, VPT>();
+    if (e != cudaSuccess) return e;
+    const int64_t per_sm = std::max<int64_t>(
+        1, std::min<int64_t>(2048 / threads, static_cast<int64_t>(227 * 1024) / static_cast<int64_t>(smem + 1024)));
+    const int grid = static_cast<int>(std::min<int64_t>({N, static_cast<int64_t>(device_sm_count()) * per_sm, kPartMaxGrid}));
+    e = launch_dependent(rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT>, dim3(grid), dim3(static_cast<unsigned>(threads)),
+                         smem, s, dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part);
+    if (e != cudaSuccess) return e;
+    const dim3 rgrid(static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols))),
+        rblock(kRedCols * kRedSlices);
+    return launch_dependent(rmsnorm_dgamma_reduce, rgrid, rblock, 0, s, part, grid, D, dgamma);
 }
 
 }  // namespace
@@ -667,37 +610,12 @@ cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void*
     const dim3 rgrid(static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols))),
         rblock(kRedCols * kRedSlices);
     cudaError_t e = cudaSuccess;
-    const int ring_threads = static_cast<int>(((nvec + kRingVpt - 1) / kRingVpt + 31) / 32 * 32);
-    const size_t ring_smem = kRingStages * ring_stage_bytes(kRingRows, kRingVpt, ring_threads);
-    if (dgamma && N > 0 && ring_threads <= kRingMaxThreads) {
-        // one pass through the shared-memory ring: as many CTAs per SM as its shared
-        // memory and threads allow, each with a contiguous range of rows
-        e = es == 2 ? ring_attr<2>() : ring_attr<4>();
-        if (e != cudaSuccess) return e;
-        const int64_t per_sm = std::max<int64_t>(
-            1, std::min<int64_t>(2048 / ring_threads, static_cast<int64_t>(227 * 1024) / static_cast<int64_t>(ring_smem + 1024)));
-        const int grid = static_cast<int>(
-            std::min<int64_t>({N, static_cast<int64_t>(device_sm_count()) * per_sm, kFuseMaxGrid}));
-        const dim3 block(static_cast<unsigned>(ring_threads));
-        e = es == 2 ? launch_dependent(rmsnorm_bwd_ring_kernel<2, kRingRows, kRingVpt>, dim3(grid), block, ring_smem, s, dy, lddy,
-                                       x, ldx, g, rstd, N, D, dx, lddx, part)
-                    : launch_dependent(rmsnorm_bwd_ring_kernel<4, kRingRows, kRingVpt>, dim3(grid), block, ring_smem, s, dy, lddy,
-                                       x, ldx, g, rstd, N, D, dx, lddx, part);
-        if (e != cudaSuccess) return e;
-        return launch_dependent(rmsnorm_dgamma_reduce, rgrid, rblock, 0, s, part, grid, D, dgamma);
-    }
-    if (dgamma && N > 0 && nvec <= 1024) {
-        // longer rows in one pass: dX and the dgamma partials of each CTA, then the reduce
-        const dim3 block(static_cast<unsigned>((nvec + 31) / 32 * 32));
-        const int grid = static_cast<int>(std::min<int64_t>(
-            {(N + kFuseRows - 1) / kFuseRows, static_cast<int64_t>(device_sm_count()) * 2, kFuseMaxGrid}));
-        e = es == 2 ? launch_dependent(rmsnorm_bwd_fused_kernel<2>, dim3(grid), block, 0, s, dy, lddy, x, ldx, g, rstd, N,
-                                       D, dx, lddx, part)
-                    : launch_dependent(rmsnorm_bwd_fused_kernel<4>, dim3(grid), block, 0, s, dy, lddy, x, ldx, g, rstd, N,
-                                       D, dx, lddx, part);
-        if (e != cudaSuccess) return e;
-        return launch_dependent(rmsnorm_dgamma_reduce, rgrid, rblock, 0, s, part, grid, D, dgamma);
-    }
+    if (dgamma && N > 0 && nvec <= static_cast<int64_t>(kRingVpt) * kRingMaxThreads)
+        return es == 2 ? launch_bwd_ring<2, kRingVpt>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s)
+                       : launch_bwd_ring<4, kRingVpt>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s);
+    if (dgamma && N > 0 && nvec <= static_cast<int64_t>(kRingVptWide) * kRingMaxThreads)
+        return es == 2 ? launch_bwd_ring<2, kRingVptWide>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s)
+                       : launch_bwd_ring<4, kRingVptWide>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s);
     if (N > 0) {
         const dim3 grid(static_cast<unsigned>(norm_grid(N))), block(kNormThreads);
         e = es == 2 ? launch_dependent(rmsnorm_bwd_kernel<2>, grid, block, 0, s, dy, lddy, x, ldx, g, rstd, N, D, dx, lddx)
