@@ -494,6 +494,100 @@ __global__ void __launch_bounds__(kRingMaxThreads, ring_min_blocks(VPT))
     }
 }
 
+// The forward through the same kind of ring, for rows too wide for one warp's
+// registers: thread v owns column vectors v, v + threads, ... (VPT of them) of every
+// row, each CTA takes one contiguous range of rows in batches of RR, and every thread
+// copies its own vectors of X kRingStages - 1 batches ahead.  Per row the CTA sums
+// x^2 (pairs on the two-wide FP32 instructions, then warp shuffles and one barrier per
+// batch), and each thread writes y = x r gamma for its vectors (x r rounded, then times
+// gamma, as the other forward kernels).
+template <int ES, int RR, int VPT>
+__global__ void __launch_bounds__(kRingMaxThreads, 2)
+    rmsnorm_fwd_cta_ring_kernel(const char* __restrict__ X, int64_t ldx, const char* __restrict__ gamma, int64_t N,
+                                int64_t D, float eps, char* __restrict__ Y, int64_t ldy, float* __restrict__ rstd) {
+    griddep_launch_dependents();  // programmatic dependent launch: no global access before the wait
+    griddep_wait();
+    constexpr int EPV = 16 / ES, NP = EPV / 2;
+    extern __shared__ uint4 ring[];  // [kRingStages][RR][VPT][threads]
+    __shared__ float red[2][RR][32];
+    const int v = threadIdx.x, lane = v & 31, warp = v >> 5, nt = blockDim.x, warps = nt >> 5;
+    bool act[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) act[j] = static_cast<int64_t>(v + j * nt) * EPV < D;
+    const int64_t G = gridDim.x;
+    const int64_t r_begin = N * static_cast<int64_t>(blockIdx.x) / G;
+    const int64_t r_end = N * (static_cast<int64_t>(blockIdx.x) + 1) / G;
+    const int64_t nb = (r_end - r_begin + RR - 1) / RR;
+    auto issue = [&](int64_t b) {  // one commit group per batch (empty past the last)
+        if (b < nb) {
+            uint4* slot = ring + static_cast<size_t>(b % kRingStages) * (RR * VPT) * nt;
+#pragma unroll
+            for (int q = 0; q < RR; ++q) {
+                const int64_t row = r_begin + b * RR + q;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j)
+                    if (row < r_end && act[j])
+                        cp_async16(slot + (q * VPT + j) * nt + v,
+                                   X + (row * ldx + static_cast<int64_t>(v + j * nt) * EPV) * ES);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int s = 0; s < kRingStages - 1; ++s) issue(s);
+    float2 gm2[VPT][NP];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+        unpack_pairs<ES>(act[j] ? ldv(gamma + static_cast<int64_t>(v + j * nt) * 16) : make_uint4(0u, 0u, 0u, 0u),
+                         gm2[j]);
+    int par = 0;
+    for (int64_t b = 0; b < nb; ++b, par ^= 1) {
+        issue(b + kRingStages - 1);  // into the slot read before the last barrier
+        cp_async_wait<kRingStages - 1>();
+        const int64_t row0 = r_begin + b * RR;
+        const uint4* slot = ring + static_cast<size_t>(b % kRingStages) * (RR * VPT) * nt;
+#pragma unroll
+        for (int q = 0; q < RR; ++q) {
+            float2 s2 = make_float2(0.f, 0.f);
+            if (row0 + q < r_end) {
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    if (act[j]) {
+                        float2 x[NP];
+                        unpack_pairs<ES>(slot[(q * VPT + j) * nt + v], x);
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) s2 = __ffma2_rn(x[k], x[k], s2);
+                    }
+                }
+            }
+            const float ss = warp_sum(s2.x + s2.y);
+            if (lane == 0) red[par][q][warp] = ss;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < RR; ++q) {
+            const int64_t row = row0 + q;
+            const float ss = warp_sum(lane < warps ? red[par][q][lane] : 0.f);
+            if (row < r_end) {
+                const float r = rsqrtf(ss / static_cast<float>(D) + eps);
+                const float2 r2 = make_float2(r, r);
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    if (act[j]) {
+                        float2 x[NP];
+                        unpack_pairs<ES>(slot[(q * VPT + j) * nt + v], x);
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) x[k] = __fmul2_rn(__fmul2_rn(x[k], r2), gm2[j][k]);
+                        store_pairs<ES>(Y + (row * ldy + static_cast<int64_t>(v + j * nt) * EPV) * ES, x);
+                    }
+                }
+                if (v == 0 && rstd) rstd[row] = r;
+            }
+        }
+    }
+    cp_async_wait<0>();  // no copy outlives the CTA (the trailing groups are empty)
+}
+
 // dgamma[j] = sum of part[g][j] over g < G (G <= kRedMaxG for every caller), in a
 // fixed order: 32 slices of 32 columns per CTA, slice sl loading g = sl, sl + 32, ...
 // all at once (one round trip) and adding them in g order, then slice 0 adding the 32
@@ -567,15 +661,48 @@ cudaError_t launch_bwd_ring(const char* dy, int64_t lddy, const char* x, int64_t
     const size_t smem = kRingStages * ring_stage_bytes(kRingRows, VPT, threads);
     cudaError_t e = ring_attr<ES, VPT>();
     if (e != cudaSuccess) return e;
-    const int64_t per_sm = std::max<int64_t>(
-        1, std::min<int64_t>(2048 / threads, static_cast<int64_t>(227 * 1024) / static_cast<int64_t>(smem + 1024)));
-    const int grid = static_cast<int>(std::min<int64_t>({N, static_cast<int64_t>(device_sm_count()) * per_sm, kPartMaxGrid}));
+    int per_sm = 0;  // every CTA resident at once: the row ranges are contiguous
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT>, threads, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = static_cast<int>(std::min<int64_t>(
+        {N, static_cast<int64_t>(device_sm_count()) * std::max(per_sm, 1), kPartMaxGrid}));
     e = launch_dependent(rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT>, dim3(grid), dim3(static_cast<unsigned>(threads)),
                          smem, s, dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part);
     if (e != cudaSuccess) return e;
     const dim3 rgrid(static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols))),
         rblock(kRedCols * kRedSlices);
     return launch_dependent(rmsnorm_dgamma_reduce, rgrid, rblock, 0, s, part, grid, D, dgamma);
+}
+
+bool g_fwd_attr[64][4] = {};
+
+template <int ES, int VPT>
+cudaError_t launch_fwd_cta_ring(const char* x, int64_t ldx, const char* g, int64_t N, int64_t D, float eps, char* y,
+                                int64_t ldy, float* rstd, cudaStream_t s) {
+    const int64_t nvec = D / (16 / ES);
+    const int threads = static_cast<int>(((nvec + VPT - 1) / VPT + 31) / 32 * 32);
+    const size_t smem = static_cast<size_t>(kRingStages) * kRingRows * VPT * threads * 16;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_ring_mu);
+        const int k = (ES == 2 ? 0 : 2) + (VPT == kRingVptWide ? 1 : 0);
+        if (!g_fwd_attr[dev][k]) {
+            e = cudaFuncSetAttribute(rmsnorm_fwd_cta_ring_kernel<ES, kRingRows, VPT>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemMax);
+            if (e != cudaSuccess) return e;
+            g_fwd_attr[dev][k] = true;
+        }
+    }
+    int per_sm = 0;  // every CTA resident at once: the row ranges are contiguous
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_fwd_cta_ring_kernel<ES, kRingRows, VPT>, threads,
+                                                      smem);
+    if (e != cudaSuccess) return e;
+    const int grid = static_cast<int>(std::min<int64_t>(N, static_cast<int64_t>(device_sm_count()) * std::max(per_sm, 1)));
+    return launch_dependent(rmsnorm_fwd_cta_ring_kernel<ES, kRingRows, VPT>, dim3(grid),
+                            dim3(static_cast<unsigned>(threads)), smem, s, x, ldx, g, N, D, eps, y, ldy, rstd);
 }
 
 }  // namespace
@@ -587,14 +714,21 @@ cudaError_t launch_rmsnorm_fwd(int es, const void* X, int64_t ldx, const void* g
     const char* x = static_cast<const char*>(X);
     const char* g = static_cast<const char*>(gamma);
     char* y = static_cast<char*>(Y);
-    // rows of at most 512 vectors in registers (D <= 4096 bf16 / 2048 fp32)
+    // rows of at most 256 vectors (D <= 2048 bf16 / 1024 fp32) in one warp's registers
     const int64_t nvec = D / (16 / es);
     if (nvec <= 128)
         return es == 2 ? launch_dependent(rmsnorm_fwd_reg_kernel<2, 4>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd)
                        : launch_dependent(rmsnorm_fwd_reg_kernel<4, 4>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd);
-    if (nvec <= 512)
+    if (nvec <= 256)  // (16 vectors a lane held, 8 used: 17.7 us at 8192 x 2048 bf16 against 18.6 with 8)
         return es == 2 ? launch_dependent(rmsnorm_fwd_reg_kernel<2, 16>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd)
                        : launch_dependent(rmsnorm_fwd_reg_kernel<4, 16>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd);
+    // up to 1024 vectors (D <= 8192 bf16 / 4096 fp32): the CTA-wide ring
+    if (nvec <= static_cast<int64_t>(kRingVpt) * kRingMaxThreads)
+        return es == 2 ? launch_fwd_cta_ring<2, kRingVpt>(x, ldx, g, N, D, eps, y, ldy, rstd, s)
+                       : launch_fwd_cta_ring<4, kRingVpt>(x, ldx, g, N, D, eps, y, ldy, rstd, s);
+    if (nvec <= static_cast<int64_t>(kRingVptWide) * kRingMaxThreads)
+        return es == 2 ? launch_fwd_cta_ring<2, kRingVptWide>(x, ldx, g, N, D, eps, y, ldy, rstd, s)
+                       : launch_fwd_cta_ring<4, kRingVptWide>(x, ldx, g, N, D, eps, y, ldy, rstd, s);
     return es == 2 ? launch_dependent(rmsnorm_fwd_kernel<2>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd)
                    : launch_dependent(rmsnorm_fwd_kernel<4>, grid, block, 0, s, x, ldx, g, N, D, eps, y, ldy, rstd);
 }

@@ -41,7 +41,7 @@ def _inputs(N, D, dtype, seed, ld=None):
 
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
 @pytest.mark.parametrize("N,D,ld", [(1, 8, None), (37, 4096, None), (513, 1000, None), (64, 8192, None),
-                                    (100, 2048, 2056)])
+                                    (100, 2048, 2056), (1500, 4096, None), (700, 3000, 3016)])
 def test_rmsnorm_forward(cuda_lib, dtype, N, D, ld):
     X, gamma = _inputs(N, D, dtype, seed=N + D, ld=ld)
     ref_y, ref_r = oracle.rmsnorm(X[:, :D], gamma, 1e-5)
