@@ -368,7 +368,8 @@ __device__ __forceinline__ void store_pairs(char* dst, const float2 (&p)[8 / ES]
     *reinterpret_cast<uint4*>(dst) = w;
 }
 
-template <int ES, int RR, int VPT>
+// DG: dgamma wanted (the partials are written); without it part is not touched.
+template <int ES, int RR, int VPT, bool DG>
 __global__ void __launch_bounds__(kRingMaxThreads, ring_min_blocks(VPT))
     rmsnorm_bwd_ring_kernel(const char* __restrict__ dY, int64_t lddy, const char* __restrict__ X, int64_t ldx,
                             const char* __restrict__ gamma, const float* __restrict__ rstd, int64_t N, int64_t D,
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(kRingMaxThreads, ring_min_blocks(VPT))
                         for (int k = 0; k < NP; ++k) {
                             const float2 xh = __fmul2_rn(x[k], r2);
                             o[k] = __ffma2_rn(nrm2, xh, __fmul2_rn(r2, __fmul2_rn(gm2[j][k], d[k])));
-                            acc2[j][k] = __ffma2_rn(d[k], xh, acc2[j][k]);
+                            if constexpr (DG) acc2[j][k] = __ffma2_rn(d[k], xh, acc2[j][k]);
                         }
                         store_pairs<ES>(dX + (row * lddx + static_cast<int64_t>(v + j * nt) * EPV) * ES, o);
                     }
@@ -481,14 +482,16 @@ __global__ void __launch_bounds__(kRingMaxThreads, ring_min_blocks(VPT))
         }
     }
     cp_async_wait<0>();  // no copy outlives the CTA (the trailing groups are empty)
+    if constexpr (DG) {
 #pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        if (act[j]) {
-            float* p = part + static_cast<int64_t>(blockIdx.x) * D + static_cast<int64_t>(v + j * nt) * EPV;
+        for (int j = 0; j < VPT; ++j) {
+            if (act[j]) {
+                float* p = part + static_cast<int64_t>(blockIdx.x) * D + static_cast<int64_t>(v + j * nt) * EPV;
 #pragma unroll
-            for (int k = 0; k < NP; ++k) {
-                p[2 * k] = acc2[j][k].x;
-                p[2 * k + 1] = acc2[j][k].y;
+                for (int k = 0; k < NP; ++k) {
+                    p[2 * k] = acc2[j][k].x;
+                    p[2 * k + 1] = acc2[j][k].y;
+                }
             }
         }
     }
@@ -630,19 +633,19 @@ int norm_grid(int64_t N) {
 }
 
 std::mutex g_ring_mu;
-bool g_ring_attr[64][4] = {};
+bool g_ring_attr[64][8] = {};
 
 // The ring kernel's shared memory limit, set once per device, element size and width.
-template <int ES, int VPT>
+template <int ES, int VPT, bool DG>
 cudaError_t ring_attr() {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const int k = (ES == 2 ? 0 : 2) + (VPT == kRingVpt ? 0 : 1);
+    const int k = (ES == 2 ? 0 : 4) + (VPT == kRingVpt ? 0 : 2) + (DG ? 0 : 1);
     std::lock_guard<std::mutex> lock(g_ring_mu);
     if (!g_ring_attr[dev][k]) {
-        e = cudaFuncSetAttribute(rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT>,
+        e = cudaFuncSetAttribute(rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT, DG>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemMax);
         if (e != cudaSuccess) return e;
         g_ring_attr[dev][k] = true;
@@ -653,22 +656,23 @@ cudaError_t ring_attr() {
 // The one-pass backward through the shared-memory ring: as many CTAs per SM as its
 // shared memory and threads allow, each with a contiguous range of rows; then the
 // fixed-order dgamma reduce over the CTAs' partials.
-template <int ES, int VPT>
+template <int ES, int VPT, bool DG>
 cudaError_t launch_bwd_ring(const char* dy, int64_t lddy, const char* x, int64_t ldx, const char* g, const float* rstd,
                             int64_t N, int64_t D, char* dx, int64_t lddx, float* part, float* dgamma, cudaStream_t s) {
     const int64_t nvec = D / (16 / ES);
     const int threads = static_cast<int>(((nvec + VPT - 1) / VPT + 31) / 32 * 32);
     const size_t smem = kRingStages * ring_stage_bytes(kRingRows, VPT, threads);
-    cudaError_t e = ring_attr<ES, VPT>();
+    cudaError_t e = ring_attr<ES, VPT, DG>();
     if (e != cudaSuccess) return e;
     int per_sm = 0;  // every CTA resident at once: the row ranges are contiguous
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT>, threads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT, DG>, threads,
+                                                      smem);
     if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(std::min<int64_t>(
         {N, static_cast<int64_t>(device_sm_count()) * std::max(per_sm, 1), kPartMaxGrid}));
-    e = launch_dependent(rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT>, dim3(grid), dim3(static_cast<unsigned>(threads)),
-                         smem, s, dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part);
-    if (e != cudaSuccess) return e;
+    e = launch_dependent(rmsnorm_bwd_ring_kernel<ES, kRingRows, VPT, DG>, dim3(grid),
+                         dim3(static_cast<unsigned>(threads)), smem, s, dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part);
+    if (e != cudaSuccess || !DG) return e;
     const dim3 rgrid(static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols))),
         rblock(kRedCols * kRedSlices);
     return launch_dependent(rmsnorm_dgamma_reduce, rgrid, rblock, 0, s, part, grid, D, dgamma);
@@ -744,12 +748,21 @@ cudaError_t launch_rmsnorm_bwd(int es, const void* dY, int64_t lddy, const void*
     const dim3 rgrid(static_cast<unsigned>(std::max<int64_t>(1, (D + kRedCols - 1) / kRedCols))),
         rblock(kRedCols * kRedSlices);
     cudaError_t e = cudaSuccess;
-    if (dgamma && N > 0 && nvec <= static_cast<int64_t>(kRingVpt) * kRingMaxThreads)
-        return es == 2 ? launch_bwd_ring<2, kRingVpt>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s)
-                       : launch_bwd_ring<4, kRingVpt>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s);
-    if (dgamma && N > 0 && nvec <= static_cast<int64_t>(kRingVptWide) * kRingMaxThreads)
-        return es == 2 ? launch_bwd_ring<2, kRingVptWide>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s)
-                       : launch_bwd_ring<4, kRingVptWide>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s);
+    if (N > 0 && nvec <= static_cast<int64_t>(kRingVptWide) * kRingMaxThreads) {
+        const bool narrow = nvec <= static_cast<int64_t>(kRingVpt) * kRingMaxThreads;
+        if (es == 2) {
+            if (narrow)
+                return dgamma ? launch_bwd_ring<2, kRingVpt, true>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s)
+                              : launch_bwd_ring<2, kRingVpt, false>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s);
+            return dgamma ? launch_bwd_ring<2, kRingVptWide, true>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s)
+                          : launch_bwd_ring<2, kRingVptWide, false>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s);
+        }
+        if (narrow)
+            return dgamma ? launch_bwd_ring<4, kRingVpt, true>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s)
+                          : launch_bwd_ring<4, kRingVpt, false>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s);
+        return dgamma ? launch_bwd_ring<4, kRingVptWide, true>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s)
+                      : launch_bwd_ring<4, kRingVptWide, false>(dy, lddy, x, ldx, g, rstd, N, D, dx, lddx, part, dgamma, s);
+    }
     if (N > 0) {
         const dim3 grid(static_cast<unsigned>(norm_grid(N))), block(kNormThreads);
         e = es == 2 ? launch_dependent(rmsnorm_bwd_kernel<2>, grid, block, 0, s, dy, lddy, x, ldx, g, rstd, N, D, dx, lddx)

@@ -146,9 +146,10 @@ def test_decoder_tail_full_size(cuda_lib):
 
 
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
-def test_rmsnorm_backward_without_dgamma(cuda_lib, dtype):
-    """dX alone (no dgamma wanted) runs the warp-per-row backward."""
-    N, D = 301, 4096
+@pytest.mark.parametrize("N,D", [(301, 4096), (50, 16384)])
+def test_rmsnorm_backward_without_dgamma(cuda_lib, dtype, N, D):
+    """dX alone (no dgamma wanted): the ring without its dgamma partials up to 1024
+    vectors a row, the warp-per-row two-pass kernel beyond."""
     X, gamma = _inputs(N, D, dtype, seed=17)
     dY = wl.normal_matrix(N, D, seed=19, sigma=1.0, dtype=dtype, stream=wl.S_H)
     ref_dx, _ = oracle.rmsnorm_backward(dY, X, gamma, 1e-5)
