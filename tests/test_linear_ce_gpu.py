@@ -57,6 +57,21 @@ def test_linear_ce_small(cuda_lib, N, V, D, chunk):
     assert np.all(dH[ign] == 0.0)
 
 
+def test_linear_ce_ragged_vocabulary_and_last_chunk(cuda_lib):
+    """V = 40000 (a partial last 256-column tile) in chunks of 512 rows with a 300-row
+    last chunk: parity with the oracle, and dH identical to a one-chunk call."""
+    H, W, y = _case(1836, 40000, 256, seed=77, n_ignore=180)
+    ref = oracle.linear_ce(H, W, y)
+    a = _run(cuda_lib, H, W, y, chunk=512)
+    assert abs(a[0] - ref["loss"]) <= 2e-3 * abs(ref["loss"])
+    assert a[3] == ref["n_valid"] and a[4] == 0
+    assert _frob(a[1], ref["dH"]) < 1e-2
+    assert _frob(a[2], ref["dW"]) < 1e-2
+    b = _run(cuda_lib, H, W, y, chunk=2048)
+    np.testing.assert_array_equal(a[1], b[1])
+    assert a[0] == pytest.approx(b[0], rel=1e-6)
+
+
 def test_linear_ce_chunk_size_invariance(cuda_lib):
     H, W, y = _case(512, 777, 128, seed=3, n_ignore=40)
     a = _run(cuda_lib, H, W, y, chunk=512)
