@@ -63,6 +63,10 @@ int elem_bytes_of(int32_t dtype) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Vocabularies the chunked linear + CE calls take: 1024 columns of 256-column tiles
+// (their logits slots, statistics and grouped unit lists are sized and tested up to it).
+constexpr int64_t kLinearMaxVocab = 262144;
+
 // Checks common to the row calls.
 foak_status check_rows(const void* logits, int32_t dtype, int64_t ld, const int64_t* labels, int64_t N,
                        int64_t V, int* es) {
@@ -346,7 +350,7 @@ foak_status foak_linear_ce_chunked(const void* H, const void* W, const int64_t* 
                                    void* workspace, size_t workspace_bytes, void* stream) {
     if (N < 0 || V < 1 || D < 1 || chunk < 1) return FOAK_ERR_INVALID_ARG;
     if (N > 0x7fffffffLL || V > 0x7fffffffLL || D > 0x7fffffffLL) return FOAK_ERR_UNSUPPORTED;
-    if (V > ce_rows_max_vocab(2)) return FOAK_ERR_UNSUPPORTED;
+    if (V > kLinearMaxVocab) return FOAK_ERR_UNSUPPORTED;
     if (D % 8) return FOAK_ERR_UNSUPPORTED;  // 16-byte rows for the tensor maps
     if (!W || !dW || !loss || !aligned(W, 16) || !aligned(dW, 16) || !aligned(loss, 4)) return FOAK_ERR_INVALID_ARG;
     if (N > 0 && (!H || !labels || !dH || !aligned(H, 16) || !aligned(dH, 16) || !aligned(labels, 8)))
@@ -408,7 +412,7 @@ foak_status foak_rmsnorm_linear_ce_chunked(const void* X, const void* gamma, con
                                            size_t workspace_bytes, void* stream) {
     if (N < 0 || V < 1 || D < 8 || chunk < 1 || !(eps >= 0.f)) return FOAK_ERR_INVALID_ARG;
     if (N > 0x7fffffffLL || V > 0x7fffffffLL || D > 0x7fffffffLL) return FOAK_ERR_UNSUPPORTED;
-    if (V > ce_rows_max_vocab(2) || D % 8) return FOAK_ERR_UNSUPPORTED;
+    if (V > kLinearMaxVocab || D % 8) return FOAK_ERR_UNSUPPORTED;
     if (!W || !dW || !loss || !gamma || !dgamma || !aligned(W, 16) || !aligned(dW, 16) || !aligned(loss, 4) ||
         !aligned(gamma, 16) || !aligned(dgamma, 4))
         return FOAK_ERR_INVALID_ARG;

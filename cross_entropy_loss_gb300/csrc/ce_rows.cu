@@ -499,7 +499,10 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 2 : 1) ce_rows_kerne
 // ------------------------------------------------------------------ host side
 
 int64_t ce_rows_max_vocab(int elem_bytes) {
-    return static_cast<int64_t>(kRowMaxCluster) * kRowSliceVecMax * (16 / elem_bytes);
+    // rows past the one-pass plans (8 CTAs x 64 KB) are streamed twice by one CTA,
+    // whose chunk and column indexes are 32-bit
+    (void)elem_bytes;
+    return 0x7fffffffLL;
 }
 
 namespace {
@@ -673,7 +676,7 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
                            int32_t* err, CeWsHeader* ws, cudaStream_t stream, const int64_t* count_labels,
                            int64_t count_N, const int64_t* denom_dev) {
     Plan pl;
-    if (!plan_rows(elem_bytes, V, &pl)) return cudaErrorInvalidValue;
+    const bool planned = plan_rows(elem_bytes, V, &pl);  // false past the one-pass plans' reach
     CeRowParams prm = {};
     prm.x = static_cast<const char*>(x);
     prm.dx = static_cast<char*>(dx);
@@ -696,11 +699,13 @@ cudaError_t launch_ce_rows(bool grad, int elem_bytes, const void* x, void* dx, i
     prm.wait_ns = test_wait_limit_ns();
     prm.skip_load_row = test_skip_load_row();
     // Rows longer than one 512-thread CTA's slice are streamed twice by one CTA
-    // (every SM busy, no cluster exchange) unless the one-pass cluster kernel is asked for.
+    // (every SM busy, no cluster exchange) unless the one-pass cluster kernel is asked
+    // for; rows too long for any one-pass plan always are.
     const int hook = test_row_path();
     const bool warp_ok = hook != 1 && hook != 2;  // 3 asks for the independent-warp kernel, like 0
     const int path = hook == 3 ? 0 : hook;
-    if (path == 2 || (path == 0 && plan_needs_cluster(elem_bytes, V))) return launch_ce_rows_long(grad, elem_bytes, prm, stream);
+    if (!planned || path == 2 || (path == 0 && plan_needs_cluster(elem_bytes, V)))
+        return launch_ce_rows_long(grad, elem_bytes, prm, stream);
     // Aligned: every row (base + i * ld elements) starts on 16 bytes and ends on a vector.
     const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld * elem_bytes) % 16 == 0 &&
                          (V * elem_bytes) % 16 == 0 && (dx == x || dx == nullptr || !grad);

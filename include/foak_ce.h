@@ -80,7 +80,9 @@ const char* foak_status_string(int32_t status);
 /* ABI version of the loaded library (FOAK_CE_ABI_VERSION at build time). */
 int32_t foak_abi_version(void);
 
-/* Largest V the row kernels accept for a dtype (rows up to 8 CTAs x 64 KB). */
+/* Largest V the row calls accept for a dtype: 2^31 - 1 (rows past 8 CTAs x 64 KB,
+ * the one-pass plans' reach, are streamed twice by one CTA).  The chunked linear +
+ * CE calls take V <= 262144. */
 int64_t foak_ce_max_vocab(int32_t dtype);
 
 /*

@@ -118,6 +118,25 @@ def test_tiny_config_all_entry_points(cuda_lib):
 
 
 @pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+def test_vocabulary_past_the_one_pass_plans(cuda_lib, dtype):
+    """V = 600011: past what 8 CTAs x 64 KB hold in either dtype, so every call streams
+    the rows twice; fused, forward and backward against the oracle."""
+    N, V = 3, 600011
+    assert cuda_lib.foak_ce_max_vocab(cuda_lib.FOAK_F32 if dtype == wl.F32 else cuda_lib.FOAK_BF16) >= V
+    x, y = _rand(N, V, dtype, seed=61, sigma=3.0, n_ignore=1, spikes=1e-4)
+    y[0] = V - 1
+    ref = oracle.ce(x, y, g=1.0)
+    _check_fused(cuda_lib, x, y, V, dtype)
+    t, yd = to_device(x, dtype), torch.from_numpy(y).cuda()
+    f = cuda_lib.foak_ce_forward(t, yd, want_lse=True)
+    d, err = cuda_lib.foak_ce_backward(t, yd, f["lse"])
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert_loss_close(f["loss"].item(), ref["loss"], dtype)
+    assert_grad_close(to_f64(d), ref["grad"])
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
 def test_forward_backward_padded_unaligned(cuda_lib, dtype):
     N, V, ld, off = 21, 33001, 33013, 1
     x = wl.normal_matrix(N, ld, seed=9, sigma=2.0, dtype=dtype)
